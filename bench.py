@@ -1,0 +1,402 @@
+"""Benchmark of one fused SSD round (verify + fan-out cache build + lookup) on GB300.
+
+Workload: B=256 sequences, K=4 drafted tokens, V=128256, bf16 logits, half the
+sequences greedy (tau=0) and half sampled (tau=1), cache budget 32 with the
+geometric fan-out a_p=0.75, r=0.5 -- the largest of the five synthetic
+workloads.  A step is one ssd_round call over the whole batch; the metric is
+verified speculation rounds per second (whole job), with the achieved HBM
+bandwidth of the kernel against the measured copy bandwidth.
+
+Arms:
+  (default)          libssd through its Python binding (C ABI, CUDA kernels)
+  --impl reference   the float64 CPU oracle on the host cores (the only other
+                     implementation of this path; there is no upstream code)
+
+Multi-GPU (torchrun): every rank runs its own batch of 256 sequences (weak
+scaling, no collective on the data path); a barrier and a max over ranks
+bracket the timed region.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+WORKLOAD = "c5"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def workload_config(wl) -> dict:
+    return {"workload": f"{wl.name}: {wl.description}", "B": wl.B, "K": wl.K, "V": wl.V,
+            "logits": wl.dtype, "mode": wl.mode, "greedy_sequences": min(wl.greedy_first, wl.B),
+            "budget": wl.budget, "a_p": wl.a_p, "r": wl.r,
+            "l2": "inputs larger than L2 (logits %.0f MB vs 129 MB L2), no flush" %
+                  ((wl.B * (2 * wl.K + 1) * wl.V * wl.elem_bytes) / 1e6)}
+
+
+def metric_name():
+    return "verified speculation rounds/sec (HBM GB/s vs measured copy bandwidth)"
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# Clock sampling (nvidia-smi, during the timed region).
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float) -> dict:
+        inside = [r for (t, r) in self.rows if t0 <= t <= t1]
+        window = "timed"
+        if not inside:
+            inside = [r for (_, r) in self.rows]
+            window = "run"
+        mhz, maxes, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in inside:
+            parts = [p.strip() for p in r.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                mhz.append(float(parts[1]))
+                maxes.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not mhz:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": max(maxes),
+                "reasons": sorted(reasons), "samples": len(mhz), "window": window}
+
+
+# ---------------------------------------------------------------------------
+# Our arm.
+# ---------------------------------------------------------------------------
+def to_device(inp, torch, dev):
+    wl = inp["workload"]
+
+    def logits(a):
+        if wl.dtype == synth.F32:
+            return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    return {"tgt": logits(inp["tgt"]), "drf": logits(inp["drf"]),
+            "tokens": torch.from_numpy(inp["tokens"]).to(dev),
+            "uniforms": torch.from_numpy(inp["uniforms"]).to(dev),
+            "temperature": torch.from_numpy(inp["temperature"]).to(dev)}
+
+
+def traffic_record(kernel_digest: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken of this build."""
+    path = os.path.join(ROOT, "profiles", "ssd_unit_kernel_c5_traffic.json")
+    try:
+        d = json.load(open(path))
+    except Exception:
+        return None
+    if d.get("source_digest") != kernel_digest:
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+def cpu_baseline(inp, wl, off, sample_per_half: int = 128):
+    import oracle
+    B = wl.B
+    g = min(wl.greedy_first, B)
+    idx = np.concatenate([np.arange(0, min(g, sample_per_half)),
+                          np.arange(g, min(B, g + sample_per_half))])
+    sub = {k: inp[k][idx] for k in ("tgt", "drf", "tokens", "uniforms", "temperature")}
+    threads = oracle.default_threads()
+    t0 = time.perf_counter()
+    oracle.round_(sub["tgt"], sub["drf"], sub["tokens"], sub["uniforms"], sub["temperature"],
+                  wl.dtype, off, wl.budget, threads=threads)
+    dt = time.perf_counter() - t0
+    rounds = len(idx) / B
+    return {"value": rounds / dt, "unit": "rounds/s", "cores": threads, "kind": "oracle",
+            "sample": f"{len(idx)} of {B} sequences of one round ({len(idx)//2} greedy, "
+                      f"{len(idx) - len(idx)//2} sampled), float64 C oracle, {threads} host threads; "
+                      f"{dt:.2f} s wall"}
+
+
+def run_ours(args):
+    import torch
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    import speculative_decoding_verification_ssd_gb300 as ssd
+    from speculative_decoding_verification_ssd_gb300 import _build
+
+    wl = synth.WORKLOADS[args.workload]
+    inp = synth.make_inputs(wl, synth.BENCH_SEED[wl.name] + rank)
+    F, off = ssd.ssd_fanout(wl.K, max(wl.budget, 0), wl.a_p or 0.5, wl.r, wl.V) if wl.budget else (
+        np.zeros(wl.K + 1, np.int32), np.zeros(wl.K + 2, np.int32))
+    d = to_device(inp, torch, dev)
+    ws = ssd.workspace(wl.B, wl.K, dev)
+    stream = torch.cuda.current_stream(dev)
+    out = None
+
+    def step():
+        if wl.mode == "round":
+            return ssd.ssd_round(d["tgt"], d["drf"], d["tokens"], d["uniforms"], d["temperature"], F,
+                                 wl.budget, out=out, probs=False, workspace=ws, stream=stream)
+        return ssd.ssd_verify(d["tgt"], d["drf"], d["tokens"], d["uniforms"], d["temperature"],
+                              probs=False, workspace=ws, stream=stream)
+
+    out = step()
+    torch.cuda.synchronize(dev)
+    acc = out["accept_len"].cpu().numpy()
+    alg_bytes = synth.algorithmic_bytes(wl, inp["temperature"], acc)
+    dense_bytes = wl.B * (2 * wl.K + 1) * wl.V * wl.elem_bytes
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.time()
+    start.record(stream)
+    for i in range(args.steps):
+        ev0[i].record(stream)
+        step()
+        ev1[i].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall1 = time.time()
+    if pg:
+        pg.barrier()
+    time.sleep(0.05)
+    sampler.stop()
+    elapsed_ms = start.elapsed_time(end)
+    kernel_ms = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
+    if pg:
+        t = torch.tensor([elapsed_ms], device=dev, dtype=torch.float64)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    clocks = sampler.summary(t_wall0, t_wall1)
+
+    # end to end: pinned host inputs -> device, round, outputs -> host, every step
+    host = {k: v.cpu().pin_memory() for k, v in d.items()}
+    dev_in = {k: torch.empty_like(v) for k, v in d.items()}
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    res_keys = ["accept_len", "bonus"] + (["cache_tok", "hit", "slot"] if wl.mode == "round" else [])
+    host_out = {k: torch.empty(out[k].shape, dtype=out[k].dtype).pin_memory() for k in res_keys}
+    d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+
+    def e2e_step():
+        for k in dev_in:
+            dev_in[k].copy_(host[k], non_blocking=True)
+        if wl.mode == "round":
+            o = ssd.ssd_round(dev_in["tgt"], dev_in["drf"], dev_in["tokens"], dev_in["uniforms"],
+                              dev_in["temperature"], F, wl.budget, out=out, probs=False,
+                              workspace=ws, stream=stream)
+        else:
+            o = ssd.ssd_verify(dev_in["tgt"], dev_in["drf"], dev_in["tokens"], dev_in["uniforms"],
+                               dev_in["temperature"], probs=False, workspace=ws, stream=stream)
+        for k in res_keys:
+            host_out[k].copy_(o[k], non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    if pg:
+        pg.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1)
+    if pg:
+        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    peak, peak_kind = measured_peak()
+    kmean = statistics.mean(kernel_ms)
+    achieved = alg_bytes / (kmean * 1e-3) / 1e9
+    value = world * args.steps / (elapsed_ms * 1e-3)
+    line = {
+        "metric": metric_name(), "value": value, "unit": "rounds/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded Gaussian + Zipf log-bias logits; no datasets, no weights)",
+        "config": workload_config(wl),
+        "sequence_rounds_per_s": value * wl.B,
+        "hbm_gbs_algorithmic": achieved,
+        "algorithmic_bytes_per_round": alg_bytes, "dense_logit_bytes_per_round": dense_bytes,
+        "kernel_ms": {"mean": kmean, "p10": float(np.percentile(kernel_ms, 10)),
+                      "median": float(np.median(kernel_ms)), "p90": float(np.percentile(kernel_ms, 90))},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback 6.8 TB/s",
+                     "traffic": traffic_record(_build.source_digest()),
+                     "kernel": "ssd_unit_kernel<BF16Tag>"},
+        "e2e": {"value": world * args.e2e_steps / (e2e_ms * 1e-3), "unit": "rounds/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "accept_mean": float(np.mean(acc[acc >= 0])) if (acc >= 0).any() else None,
+        "hit_rate": float(out["hit"].float().mean().item()) if wl.mode == "round" else None,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(inp, wl, off)
+    if pg:
+        pg.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# Reference arm: the float64 oracle on the host cores.
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    wl = synth.WORKLOADS[args.workload]
+    inp = synth.make_inputs(wl, synth.BENCH_SEED[wl.name])
+    F, off, _ = oracle.fanout(wl.K, wl.budget, wl.a_p, wl.r, wl.V) if wl.budget else (
+        None, np.zeros(wl.K + 2, np.int32), None)
+    threads = oracle.default_threads()
+    g = min(wl.greedy_first, wl.B)
+    # each step: one sequence per host thread, alternating greedy / sampled, cycling the batch
+    order = np.ravel(np.column_stack([np.arange(0, g), np.arange(g, 2 * g)])) if 0 < g < wl.B \
+        else np.arange(wl.B)
+    per_step = max(1, min(threads, wl.B))
+    cursor = [0]
+
+    def step():
+        idx = np.array([order[(cursor[0] + j) % len(order)] for j in range(per_step)])
+        cursor[0] += per_step
+        sub = {k: inp[k][idx] for k in ("tgt", "drf", "tokens", "uniforms", "temperature")}
+        if wl.mode == "round":
+            oracle.round_(sub["tgt"], sub["drf"], sub["tokens"], sub["uniforms"], sub["temperature"],
+                          wl.dtype, off, wl.budget, threads=threads)
+        else:
+            oracle.verify(sub["tgt"], sub["drf"], sub["tokens"], sub["uniforms"], sub["temperature"],
+                          wl.dtype, wl.reshape_F, wl.reshape_C, threads=threads)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    value = args.steps * per_step / wl.B / dt
+    line = {
+        "impl": "reference", "metric": metric_name(), "value": value, "unit": "rounds/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded Gaussian + Zipf log-bias logits; no datasets, no weights)",
+        "config": workload_config(wl),
+        "cpu_baseline": {"value": value, "unit": "rounds/s", "cores": threads, "kind": "oracle",
+                         "sample": f"each step: {per_step} of {wl.B} sequences of one round "
+                                   "(alternating greedy / sampled), float64 C oracle"},
+        "e2e": {"value": value, "unit": "rounds/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,207 @@
+/*
+ * ssd.h -- C ABI of libssd: the batched verify-and-sample step of speculative
+ * decoding and the cache side of Saguaro (speculative speculative decoding),
+ * as hand-written CUDA for sm_103a (GB300).
+ *
+ * Sources of the operations (page titles and sections):
+ *   [SD]  "Speculative decoding" (brentwoodlivery.com): "The Algorithm
+ *         (Step-by-Step)", "Derivation of Acceptance Criterion", "Temperature
+ *         and Sampling", "Batching Speculation".
+ *   [WHY] "Why does speculative decoding exist?" (til.phipham141.dev): "How it
+ *         works" (Fix 2: longest accepted prefix plus one bonus token; greedy
+ *         acceptance = draft token is the target argmax; Fix 3: min(1, p/q)
+ *         acceptance and the residual (p - q)+).
+ *   [SSD] "Speculative Speculative Decoding" notes (papernotes.org): "整体框架"
+ *         (outcome v = (k, t*), speculation cache S_T, hit test), "关键设计" item 1
+ *         (geometric fan-out F_k) and item 2 (SAGUARO sampling sigma_{F,C}).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Array arguments are DEVICE pointers owned by the caller, dense row-major,
+ *   unless the argument name ends in _host.  The library never allocates or
+ *   frees memory and never synchronises the stream: every device call only
+ *   enqueues work on `stream` (a cudaStream_t; NULL = the legacy default
+ *   stream) and returns.
+ * - Shapes: B sequences, K drafted tokens per sequence, V vocabulary entries.
+ *   Target logits  tgt [B, K+1, V]   (row i scores position i, row K is the
+ *                                     extra row used when all K are accepted)
+ *   Draft logits   drf [B, drf_rows, V], drf_rows in {K, K+1} (only rows 0..K-1
+ *                                     are read)
+ *   Draft tokens   tokens [B, K] int32
+ *   Uniforms       uniforms [B, K+1] fp32 in [0, 1): column i < K is the accept
+ *                  draw of position i, column K draws the bonus token.
+ *   Temperature    temperature [B] fp32 per sequence; 0 selects greedy
+ *                  decoding; negative or NaN marks the sequence invalid.
+ * - dtype is SSD_F32 or SSD_BF16 (storage type of both logit tensors).
+ * - Every call returns an ssd status (SSD_OK = 0).  Host-side validation
+ *   failures return before anything is enqueued.  SSD_ERR_CUDA reports a launch
+ *   or attribute error from the CUDA runtime.
+ * - Data errors found on the device (a drafted token outside [0, V), a bad
+ *   temperature, non-finite logits, a bounded wait that ran out) do not abort
+ *   the call: the affected sequence gets accept_len = -1 and bonus = -1, and
+ *   the matching SSD_DEV_* bits are OR-ed into *dev_status when dev_status is
+ *   not NULL (a device int32 the caller zeroes and reads).
+ * - Workspace: calls that take one need ssd_workspace_size(B, K) bytes of
+ *   device memory, 256-byte aligned, zero-filled before its first use (for
+ *   example one cudaMemsetAsync after allocation).  Each completed call leaves
+ *   its per-sequence counters at zero again, so the workspace is ready for the
+ *   next call without another fill.  Calls sharing one workspace must not
+ *   overlap on the GPU (use one workspace per stream).
+ * - Limits: 1 <= K <= SSD_MAX_K, 2 <= V, 1 <= B, every cache segment and the
+ *   reshape F at most SSD_MAX_F, and a row slice of at most SSD_MAX_V_F32 /
+ *   SSD_MAX_V_BF16 vocabulary entries (larger V returns SSD_ERR_UNSUPPORTED).
+ */
+#ifndef SSD_H
+#define SSD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+#define SSD_OK 0
+#define SSD_ERR_INVALID_ARG 1
+#define SSD_ERR_DTYPE 2
+#define SSD_ERR_CUDA 3
+#define SSD_ERR_WORKSPACE 4
+#define SSD_ERR_UNSUPPORTED 5
+
+/* Logit storage types. */
+#define SSD_F32 0
+#define SSD_BF16 1
+
+/* Device status bits. */
+#define SSD_DEV_BAD_TOKEN 1
+#define SSD_DEV_BAD_TEMPERATURE 2
+#define SSD_DEV_NONFINITE 4
+#define SSD_DEV_TIMEOUT 8
+
+/* Limits. */
+#define SSD_MAX_K 32
+#define SSD_MAX_F 256
+#define SSD_MAX_V_F32 400000
+#define SSD_MAX_V_BF16 800000
+
+/*
+ * sigma_{F,C} descriptor of one draft row ([SSD] item 2).  Token t is in the
+ * reshaped top-F set iff  z_t > thr_val  or  (z_t == thr_val and t <= thr_id),
+ * compared on the raw stored logit z_t; thr_val/thr_id are the value and id of
+ * the F-th largest logit (ties to the lowest id).  F == 0 is encoded as
+ * thr_val = +inf, thr_id = -1 (empty set).  The reshaped draft distribution is
+ * q'_t proportional to c_t * exp(z_t / tau), c_t = C inside the set, 1 outside.
+ */
+typedef struct ssd_reshape_desc {
+    float thr_val;
+    int32_t thr_id;
+    int32_t F;
+    float C;
+} ssd_reshape_desc;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *ssd_strerror(int status);
+
+/* Library version string. */
+const char *ssd_version(void);
+
+/* Bytes of workspace needed by ssd_verify / ssd_build_cache / ssd_round for a
+ * batch of B sequences with K drafted tokens (0 when B or K is out of range). */
+size_t ssd_workspace_size(int B, int K);
+
+/*
+ * ssd_verify -- [SD] "The Algorithm (Step-by-Step)" step 3 for a batch
+ * ([SD] "Batching Speculation": every sequence accepts 0..K tokens
+ * independently).  Per sequence b with temperature tau > 0 ([SD] "Temperature
+ * and Sampling": p = softmax(target row / tau), q = softmax(draft row / tau),
+ * or q = sigma_{F,C} when `reshape` is given):
+ *   accept x~_i  iff  u_i * q_i(x~_i) < p_i(x~_i)        (min(1, p/q) against u_i)
+ *   a = first rejected position, or K when none is rejected
+ *   bonus = inverse CDF over ascending token id of max(0, p_a - q_a) / Z at
+ *           u_K * Z (a < K; Z == 0 falls back to p_a), or of p_K (a == K).
+ * tau == 0 ([WHY] Fix 2): accept iff x~_i is the target argmax (raw logits,
+ * lowest id on ties); bonus = target argmax of row a.
+ * Inputs: tgt, drf, tokens, uniforms, temperature as in the conventions;
+ *   reshape: [B, K] descriptors from ssd_reshape_draft, or NULL.
+ * Outputs: accept_len [B] int32 in [0, K] (-1 for an invalid sequence);
+ *   bonus [B] int32 in [0, V); p_tok, q_tok [B, K] fp32 (may be NULL):
+ *   p_i(x~_i) and q_i(x~_i) for i <= a, NaN for i > a (tau == 0: p_tok is 1
+ *   when x~_i is the argmax else 0, q_tok is 1).
+ * Rows after the first rejection are not needed; the kernel may skip them.
+ */
+int ssd_verify(const void *tgt, const void *drf, int dtype, int B, int K, int V, int drf_rows,
+               const int32_t *tokens, const float *uniforms, const float *temperature,
+               const ssd_reshape_desc *reshape, int32_t *accept_len, int32_t *bonus,
+               float *p_tok, float *q_tok, void *workspace, size_t workspace_bytes,
+               int32_t *dev_status, void *stream);
+
+/*
+ * ssd_fanout -- [SSD] item 1, host only.  F_k = F_0 a_p^{k/(1+r)} for k < K and
+ * F_K = F_0 a_p^{K/(1+r)} (1 - a_p)^{-1/(1+r)}, with F_0 chosen so that the
+ * real-valued F_k sum to `budget`; made integer by the largest-remainder
+ * method (floor, then +1 to the largest fractional parts, lowest k on ties),
+ * so the F_k sum to budget; each F_k is then clamped to V.
+ * Outputs (host arrays): F_host [K+1], off_host [K+2] (off[0] = 0,
+ * off[k+1] = off[k] + F_k).  Requires 0 < a_p < 1, r > -1, budget >= 0, V >= 1.
+ */
+int ssd_fanout(int K, int budget, double a_p, double r, int V, int32_t *F_host,
+               int32_t *off_host);
+
+/*
+ * ssd_reshape_draft -- [SSD] item 2 on `rows` independent draft rows
+ * drf [rows, V]: the top-F set of each row (raw logits, lowest id on ties) and,
+ * when q_out is not NULL, the reshaped distribution
+ *   q_out[r, t] = c_t exp(z_t / tau_r) / sum_j c_j exp(z_j / tau_r),
+ * c_t = C for the top-F tokens, 1 otherwise (tau_r = temperature_rows[r] > 0).
+ * desc [rows] receives the descriptor (see ssd_reshape_desc).  Requires
+ * 0 <= F <= SSD_MAX_F, 0 <= C <= 1, and not (C == 0 and F >= V).
+ */
+int ssd_reshape_draft(const void *drf, int dtype, int rows, int V, const float *temperature_rows,
+                      int F, float C, ssd_reshape_desc *desc, float *q_out, int32_t *dev_status,
+                      void *stream);
+
+/*
+ * ssd_build_cache -- the speculation-cache keys of [SSD] "整体框架" / item 1:
+ * for each sequence b and accepted length k = 0..K, the F_k bonus tokens most
+ * likely to be drawn at outcome (k, t*), ranked by (score desc, id asc):
+ *   tau > 0:  score = max(0, p_k - q_k) for k < K,  p_K for k = K;
+ *   tau == 0: score = raw target logit of row k, x~_k ranked last (k < K).
+ * F_host [K+1] (host) is the fan-out (ssd_fanout); segment k of a cache row is
+ * cache_tok[b, off[k] .. off[k+1]) with off the prefix sums of F_host, and
+ * budget >= off[K+1] is the row length of cache_tok [B, budget] int32.
+ * Entries beyond off[K+1] are left untouched.
+ */
+int ssd_build_cache(const void *tgt, const void *drf, int dtype, int B, int K, int V,
+                    int drf_rows, const int32_t *tokens, const float *temperature,
+                    const ssd_reshape_desc *reshape, const int32_t *F_host, int budget,
+                    int32_t *cache_tok, void *workspace, size_t workspace_bytes,
+                    int32_t *dev_status, void *stream);
+
+/*
+ * ssd_cache_lookup -- [SSD] "整体框架": the true outcome (a, t*) hits iff t* is
+ * in segment a of the sequence's cache row.  hit [B] uint8 (1 = hit),
+ * slot [B] int32 = column of t* in cache_tok (-1 on a miss or when
+ * accept_len[b] < 0).
+ */
+int ssd_cache_lookup(const int32_t *cache_tok, int B, int K, int budget, const int32_t *F_host,
+                     const int32_t *accept_len, const int32_t *bonus, uint8_t *hit,
+                     int32_t *slot, void *stream);
+
+/*
+ * ssd_round -- one fused launch of ssd_verify + ssd_build_cache +
+ * ssd_cache_lookup: every logit row is read from HBM once.  Arguments and
+ * outputs as in those three calls.
+ */
+int ssd_round(const void *tgt, const void *drf, int dtype, int B, int K, int V, int drf_rows,
+              const int32_t *tokens, const float *uniforms, const float *temperature,
+              const ssd_reshape_desc *reshape, const int32_t *F_host, int budget,
+              int32_t *accept_len, int32_t *bonus, float *p_tok, float *q_tok,
+              int32_t *cache_tok, uint8_t *hit, int32_t *slot, void *workspace,
+              size_t workspace_bytes, int32_t *dev_status, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSD_H */

@@ -1,0 +1,306 @@
+"""Python binding of libssd: batched speculative-decoding verification and the
+Saguaro speculation-cache kernels for GB300 (sm_103a).
+
+The functions here carry the names of the C ABI in ``include/ssd.h`` and only
+marshal arguments: torch tensors provide device memory and the CUDA stream,
+every step of the computation runs in libssd's kernels.  If ``libssd.so`` has
+not been built (``__graft_entry__.build()`` or ``python -m
+speculative_decoding_verification_ssd_gb300._build``), every call raises:
+there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+import torch
+
+from . import _build
+
+SSD_OK = 0
+SSD_ERR_INVALID_ARG = 1
+SSD_ERR_DTYPE = 2
+SSD_ERR_CUDA = 3
+SSD_ERR_WORKSPACE = 4
+SSD_ERR_UNSUPPORTED = 5
+
+SSD_F32 = 0
+SSD_BF16 = 1
+
+SSD_DEV_BAD_TOKEN = 1
+SSD_DEV_BAD_TEMPERATURE = 2
+SSD_DEV_NONFINITE = 4
+SSD_DEV_TIMEOUT = 8
+
+SSD_MAX_K = 32
+SSD_MAX_F = 256
+
+LIB_PATH = _build.LIB
+
+# Symbols declared in include/ssd.h.
+ABI_SYMBOLS = ("ssd_strerror", "ssd_version", "ssd_workspace_size", "ssd_verify", "ssd_fanout",
+               "ssd_reshape_draft", "ssd_build_cache", "ssd_cache_lookup", "ssd_round")
+
+
+class SSDError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {strerror(status)}")
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libssd (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libssd is not built ({LIB_PATH} missing); run "
+                               "`python -m speculative_decoding_verification_ssd_gb300._build`")
+        L = ctypes.CDLL(LIB_PATH)
+        P, i, d, z = ctypes.c_void_p, ctypes.c_int, ctypes.c_double, ctypes.c_size_t
+        f = ctypes.c_float
+        L.ssd_strerror.argtypes = [i]
+        L.ssd_strerror.restype = ctypes.c_char_p
+        L.ssd_version.argtypes = []
+        L.ssd_version.restype = ctypes.c_char_p
+        L.ssd_workspace_size.argtypes = [i, i]
+        L.ssd_workspace_size.restype = z
+        L.ssd_verify.argtypes = [P, P, i, i, i, i, i, P, P, P, P, P, P, P, P, P, z, P, P]
+        L.ssd_verify.restype = i
+        L.ssd_fanout.argtypes = [i, i, d, d, i, P, P]
+        L.ssd_fanout.restype = i
+        L.ssd_reshape_draft.argtypes = [P, i, i, i, P, i, f, P, P, P, P]
+        L.ssd_reshape_draft.restype = i
+        L.ssd_build_cache.argtypes = [P, P, i, i, i, i, i, P, P, P, P, i, P, P, z, P, P]
+        L.ssd_build_cache.restype = i
+        L.ssd_cache_lookup.argtypes = [P, i, i, i, P, P, P, P, P, P]
+        L.ssd_cache_lookup.restype = i
+        L.ssd_round.argtypes = [P, P, i, i, i, i, i, P, P, P, P, P, i, P, P, P, P, P, P, P, P, z,
+                                P, P]
+        L.ssd_round.restype = i
+        _lib = L
+    return _lib
+
+
+def strerror(status: int) -> str:
+    try:
+        return lib().ssd_strerror(int(status)).decode()
+    except RuntimeError:
+        return f"status {status}"
+
+
+def version() -> str:
+    return lib().ssd_version().decode()
+
+
+def _check(status: int, where: str):
+    if status != SSD_OK:
+        raise SSDError(status, where)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, np.ndarray):
+        return t.ctypes.data_as(ctypes.c_void_p)
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None) -> torch.Tensor:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _logit_dtype(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return SSD_F32
+    if t.dtype == torch.bfloat16:
+        return SSD_BF16
+    raise TypeError(f"logits must be float32 or bfloat16, got {t.dtype}")
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+# ---------------------------------------------------------------------------
+# Host-only calls.
+# ---------------------------------------------------------------------------
+
+def ssd_workspace_size(B: int, K: int) -> int:
+    return int(lib().ssd_workspace_size(int(B), int(K)))
+
+
+def ssd_fanout(K: int, budget: int, a_p: float, r: float, V: int):
+    """Geometric fan-out: (F [K+1], off [K+2]) as numpy int32 arrays."""
+    F = np.empty(K + 1, np.int32)
+    off = np.empty(K + 2, np.int32)
+    _check(lib().ssd_fanout(int(K), int(budget), float(a_p), float(r), int(V), _ptr(F), _ptr(off)),
+           "ssd_fanout")
+    return F, off
+
+
+def workspace(B: int, K: int, device=None) -> torch.Tensor:
+    """A zero-filled workspace for B sequences of K drafted tokens."""
+    n = ssd_workspace_size(B, K)
+    if n == 0:
+        raise ValueError("invalid B or K")
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def _workspace(ws, B, K, device):
+    if ws is None:
+        ws = workspace(B, K, device)
+    _dev(ws, "workspace", torch.uint8)
+    return ws
+
+
+def _shapes(tgt, drf, tokens):
+    _dev(tgt, "tgt")
+    _dev(drf, "drf")
+    if tgt.dim() != 3 or drf.dim() != 3:
+        raise ValueError("tgt must be [B, K+1, V] and drf [B, K or K+1, V]")
+    B, K1, V = tgt.shape
+    K = K1 - 1
+    if drf.shape[0] != B or drf.shape[2] != V or drf.dtype != tgt.dtype:
+        raise ValueError("drf must match tgt in batch, vocabulary and dtype")
+    _dev(tokens, "tokens", torch.int32)
+    if tuple(tokens.shape) != (B, K):
+        raise ValueError("tokens must be [B, K]")
+    return B, K, V, int(drf.shape[1])
+
+
+def _opt(t, name, dtype):
+    return None if t is None else _dev(t, name, dtype)
+
+
+def _F_host(F):
+    return np.ascontiguousarray(np.asarray(F, dtype=np.int32))
+
+
+# ---------------------------------------------------------------------------
+# Device calls.
+# ---------------------------------------------------------------------------
+
+def ssd_verify(tgt, drf, tokens, uniforms, temperature, reshape=None, *, accept_len=None,
+               bonus=None, p_tok=None, q_tok=None, probs=True, workspace=None, dev_status=None,
+               stream=None):
+    """Verify one batch: returns dict(accept_len, bonus[, p_tok, q_tok])."""
+    B, K, V, drf_rows = _shapes(tgt, drf, tokens)
+    dev = tgt.device
+    _dev(uniforms, "uniforms", torch.float32)
+    _dev(temperature, "temperature", torch.float32)
+    accept_len = accept_len if accept_len is not None else torch.empty(B, dtype=torch.int32, device=dev)
+    bonus = bonus if bonus is not None else torch.empty(B, dtype=torch.int32, device=dev)
+    if probs:
+        p_tok = p_tok if p_tok is not None else torch.empty((B, K), dtype=torch.float32, device=dev)
+        q_tok = q_tok if q_tok is not None else torch.empty((B, K), dtype=torch.float32, device=dev)
+    ws = _workspace(workspace, B, K, dev)
+    _opt(reshape, "reshape", torch.int32)
+    _check(lib().ssd_verify(
+        _ptr(tgt), _ptr(drf), _logit_dtype(tgt), B, K, V, drf_rows, _ptr(tokens), _ptr(uniforms),
+        _ptr(temperature), _ptr(reshape), _ptr(accept_len), _ptr(bonus), _ptr(p_tok), _ptr(q_tok),
+        _ptr(ws), ws.numel(), _ptr(_opt(dev_status, "dev_status", torch.int32)), _stream(stream)),
+        "ssd_verify")
+    out = {"accept_len": accept_len, "bonus": bonus}
+    if probs:
+        out.update(p_tok=p_tok, q_tok=q_tok)
+    return out
+
+
+def ssd_build_cache(tgt, drf, tokens, temperature, F, budget, reshape=None, *, cache_tok=None,
+                    workspace=None, dev_status=None, stream=None):
+    """Speculation-cache keys: cache_tok [B, budget] int32 (segment k = top-F_k)."""
+    B, K, V, drf_rows = _shapes(tgt, drf, tokens)
+    dev = tgt.device
+    _dev(temperature, "temperature", torch.float32)
+    Fh = _F_host(F)
+    cache_tok = cache_tok if cache_tok is not None else torch.full((B, budget), -1, dtype=torch.int32, device=dev)
+    ws = _workspace(workspace, B, K, dev)
+    _check(lib().ssd_build_cache(
+        _ptr(tgt), _ptr(drf), _logit_dtype(tgt), B, K, V, drf_rows, _ptr(tokens),
+        _ptr(temperature), _ptr(_opt(reshape, "reshape", torch.int32)), _ptr(Fh), int(budget),
+        _ptr(cache_tok), _ptr(ws), ws.numel(), _ptr(_opt(dev_status, "dev_status", torch.int32)),
+        _stream(stream)), "ssd_build_cache")
+    return cache_tok
+
+
+def ssd_cache_lookup(cache_tok, F, accept_len, bonus, *, hit=None, slot=None, stream=None):
+    """Hit test of the true outcome (a, t*): (hit [B] uint8, slot [B] int32)."""
+    _dev(cache_tok, "cache_tok", torch.int32)
+    B, budget = cache_tok.shape
+    Fh = _F_host(F)
+    K = len(Fh) - 1
+    dev = cache_tok.device
+    hit = hit if hit is not None else torch.empty(B, dtype=torch.uint8, device=dev)
+    slot = slot if slot is not None else torch.empty(B, dtype=torch.int32, device=dev)
+    _check(lib().ssd_cache_lookup(
+        _ptr(cache_tok), B, K, budget, _ptr(Fh), _ptr(_dev(accept_len, "accept_len", torch.int32)),
+        _ptr(_dev(bonus, "bonus", torch.int32)), _ptr(hit), _ptr(slot), _stream(stream)),
+        "ssd_cache_lookup")
+    return hit, slot
+
+
+def ssd_round(tgt, drf, tokens, uniforms, temperature, F, budget, reshape=None, *, out=None,
+              probs=True, workspace=None, dev_status=None, stream=None):
+    """One fused SSD round: verify + cache build + lookup.  Returns a dict of outputs."""
+    B, K, V, drf_rows = _shapes(tgt, drf, tokens)
+    dev = tgt.device
+    _dev(uniforms, "uniforms", torch.float32)
+    _dev(temperature, "temperature", torch.float32)
+    Fh = _F_host(F)
+    o = dict(out) if out is not None else {}
+    o.setdefault("accept_len", torch.empty(B, dtype=torch.int32, device=dev))
+    o.setdefault("bonus", torch.empty(B, dtype=torch.int32, device=dev))
+    if probs:
+        o.setdefault("p_tok", torch.empty((B, K), dtype=torch.float32, device=dev))
+        o.setdefault("q_tok", torch.empty((B, K), dtype=torch.float32, device=dev))
+    o.setdefault("cache_tok", torch.full((B, budget), -1, dtype=torch.int32, device=dev))
+    o.setdefault("hit", torch.empty(B, dtype=torch.uint8, device=dev))
+    o.setdefault("slot", torch.empty(B, dtype=torch.int32, device=dev))
+    ws = _workspace(workspace, B, K, dev)
+    _check(lib().ssd_round(
+        _ptr(tgt), _ptr(drf), _logit_dtype(tgt), B, K, V, drf_rows, _ptr(tokens), _ptr(uniforms),
+        _ptr(temperature), _ptr(_opt(reshape, "reshape", torch.int32)), _ptr(Fh), int(budget),
+        _ptr(o["accept_len"]), _ptr(o["bonus"]), _ptr(o.get("p_tok")), _ptr(o.get("q_tok")),
+        _ptr(o["cache_tok"]), _ptr(o["hit"]), _ptr(o["slot"]), _ptr(ws), ws.numel(),
+        _ptr(_opt(dev_status, "dev_status", torch.int32)), _stream(stream)), "ssd_round")
+    return o
+
+
+def ssd_reshape_draft(drf, F, C, temperature_rows=None, *, want_q=False, desc=None, q_out=None,
+                      dev_status=None, stream=None):
+    """sigma_{F,C} descriptors of every draft row (drf [..., V] viewed as [rows, V]).
+
+    Returns (desc [rows, 4] int32 holding {thr_val (fp32 bits), thr_id, F, C (fp32 bits)},
+    q' [rows, V] fp32 or None)."""
+    _dev(drf, "drf")
+    V = int(drf.shape[-1])
+    rows = drf.numel() // V
+    dev = drf.device
+    desc = desc if desc is not None else torch.empty((rows, 4), dtype=torch.int32, device=dev)
+    if want_q:
+        q_out = q_out if q_out is not None else torch.empty((rows, V), dtype=torch.float32, device=dev)
+        _dev(temperature_rows, "temperature_rows", torch.float32)
+    _check(lib().ssd_reshape_draft(
+        _ptr(drf), _logit_dtype(drf), rows, V, _ptr(temperature_rows), int(F), float(C), _ptr(desc),
+        _ptr(q_out if want_q else None), _ptr(_opt(dev_status, "dev_status", torch.int32)),
+        _stream(stream)), "ssd_reshape_draft")
+    return desc, (q_out if want_q else None)
+
+
+def desc_fields(desc: torch.Tensor):
+    """Decodes reshape descriptors: (thr_val fp32, thr_id int32, F int32, C fp32) tensors."""
+    return desc[:, 0].view(torch.float32), desc[:, 1], desc[:, 2], desc[:, 3].view(torch.float32)

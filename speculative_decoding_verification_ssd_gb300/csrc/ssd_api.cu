@@ -1,0 +1,302 @@
+// ssd_api.cu -- the C ABI of libssd (declared in include/ssd.h): host-side
+// validation, launch geometry and kernel launches.  No entry point allocates
+// or frees memory or synchronises the stream.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+#include <vector>
+
+#include "../../include/ssd.h"
+#include "ssd_device.cuh"
+#include "ssd_launch.cuh"
+#include "ssd_reshape.cuh"
+#include "ssd_unit.cuh"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+// Per-device facts and one-time kernel attribute set-up.
+struct DeviceInfo {
+    bool ready = false;
+    int status = SSD_OK;
+    int sm_count = 0;
+    int max_cluster = 8;       // 16 when the non-portable size is available
+    size_t max_dyn[5] = {0};   // max dynamic smem: unit f32, unit bf16, reshape f32, reshape bf16
+};
+
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_mu;
+
+int device_info(DeviceInfo **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SSD_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceInfo &d = g_dev[dev];
+    if (!d.ready) {
+        cudaDeviceProp prop;
+        if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return SSD_ERR_CUDA;
+        if (prop.major < 10) return SSD_ERR_UNSUPPORTED;
+        d.sm_count = prop.multiProcessorCount;
+        const size_t optin = prop.sharedMemPerBlockOptin;
+        bool allow16 = true;
+        int st = SSD_OK;
+        st = st ? st : ssd::unit_setup(SSD_F32, optin, &d.max_dyn[0], &allow16);
+        st = st ? st : ssd::unit_setup(SSD_BF16, optin, &d.max_dyn[1], &allow16);
+        st = st ? st : ssd::reshape_setup(SSD_F32, optin, &d.max_dyn[2], &allow16);
+        st = st ? st : ssd::reshape_setup(SSD_BF16, optin, &d.max_dyn[3], &allow16);
+        if (st != SSD_OK) return st;
+        d.max_cluster = allow16 ? 16 : 8;
+        d.ready = true;
+    }
+    *out = &d;
+    return SSD_OK;
+}
+
+struct Geometry {
+    int CL = 0;
+    int slice = 0;
+    int row_buf_bytes = 0;
+    size_t dyn = 0;
+};
+
+int ceil_div(int a, int b) { return (a + b - 1) / b; }
+int round_up(int a, int b) { return ceil_div(a, b) * b; }
+
+// Chooses the cluster size CL and the per-CTA vocabulary slice.  Prefers the
+// smallest cluster whose staged rows leave room for 3 (then 2, then 1) CTAs
+// per SM, then widens the cluster while the grid would not fill the GPU.
+int choose_geometry(int V, int elem, int rows_staged, int units, const DeviceInfo &dv,
+                    size_t max_dyn, Geometry *g) {
+    const int vec = 16 / elem;
+    auto make = [&](int CL) {
+        Geometry r;
+        r.CL = CL;
+        r.slice = round_up(ceil_div(V, CL), vec);
+        r.row_buf_bytes = round_up(r.slice * elem + 64, 128);
+        r.dyn = static_cast<size_t>(rows_staged) * r.row_buf_bytes;
+        return r;
+    };
+    const size_t tiers[3] = {68 * 1024, 100 * 1024, max_dyn};
+    Geometry pick;
+    bool found = false;
+    for (int t = 0; t < 3 && !found; ++t) {
+        for (int CL = 1; CL <= dv.max_cluster; CL <<= 1) {
+            Geometry cand = make(CL);
+            if (cand.dyn <= tiers[t] && cand.dyn <= max_dyn) {
+                pick = cand;
+                found = true;
+                break;
+            }
+        }
+    }
+    if (!found) return SSD_ERR_UNSUPPORTED;
+    while (static_cast<long long>(units) * pick.CL < 2LL * dv.sm_count &&
+           pick.CL < dv.max_cluster && pick.slice >= 2048) {
+        pick = make(pick.CL * 2);
+    }
+    if (static_cast<long long>(units) * pick.CL > INT_MAX) return SSD_ERR_UNSUPPORTED;
+    *g = pick;
+    return SSD_OK;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_fanout(const int32_t *F_host, int K, int V, int budget, int *off) {
+    if (!F_host) return SSD_ERR_INVALID_ARG;
+    off[0] = 0;
+    for (int k = 0; k <= K; ++k) {
+        const int f = F_host[k];
+        if (f < 0 || f > SSD_MAX_F || f > V) return SSD_ERR_INVALID_ARG;
+        off[k + 1] = off[k] + f;
+    }
+    if (budget < off[K + 1]) return SSD_ERR_INVALID_ARG;
+    return SSD_OK;
+}
+
+// Shared driver of ssd_verify / ssd_build_cache / ssd_round.
+int run_units(int mode, const void *tgt, const void *drf, int dtype, int B, int K, int V,
+              int drf_rows, const int32_t *tokens, const float *uniforms, const float *temperature,
+              const ssd_reshape_desc *reshape, const int32_t *F_host, int budget,
+              int32_t *accept_len, int32_t *bonus, float *p_tok, float *q_tok, int32_t *cache_tok,
+              uint8_t *hit, int32_t *slot, void *workspace, size_t workspace_bytes,
+              int32_t *dev_status, void *stream) {
+    if (dtype != SSD_F32 && dtype != SSD_BF16) return SSD_ERR_DTYPE;
+    if (B < 1 || K < 1 || K > SSD_MAX_K || V < 2) return SSD_ERR_INVALID_ARG;
+    if (drf_rows != K && drf_rows != K + 1) return SSD_ERR_INVALID_ARG;
+    if (!tgt || !temperature || !tokens) return SSD_ERR_INVALID_ARG;
+    const bool verify = (mode & ssd::kModeVerify) != 0;
+    const bool cache = (mode & ssd::kModeCache) != 0;
+    if (!drf) return SSD_ERR_INVALID_ARG;
+    if (verify && (!uniforms || !accept_len || !bonus)) return SSD_ERR_INVALID_ARG;
+    if ((p_tok == nullptr) != (q_tok == nullptr)) return SSD_ERR_INVALID_ARG;
+    if ((mode & ssd::kModeLookup) && (!hit || !slot)) return SSD_ERR_INVALID_ARG;
+    if (V > (dtype == SSD_F32 ? SSD_MAX_V_F32 : SSD_MAX_V_BF16)) return SSD_ERR_UNSUPPORTED;
+    if (static_cast<long long>(B) * (K + 1) > INT_MAX / 16) return SSD_ERR_UNSUPPORTED;
+    ssd::UnitParams P = {};
+    if (cache) {
+        const int st = check_fanout(F_host, K, V, budget, P.off);
+        if (st != SSD_OK) return st;
+        if (P.off[K + 1] > 0 && !cache_tok) return SSD_ERR_INVALID_ARG;
+        for (int k = 0; k <= K; ++k) P.F[k] = F_host[k];
+    }
+    if (!workspace || !aligned(workspace, 256)) return SSD_ERR_WORKSPACE;
+    if (workspace_bytes < ssd::ws_total_bytes(B, K)) return SSD_ERR_WORKSPACE;
+
+    DeviceInfo *dv = nullptr;
+    int st = device_info(&dv);
+    if (st != SSD_OK) return st;
+    const int elem = dtype == SSD_F32 ? 4 : 2;
+    const int units = B * (K + 1);
+    Geometry g;
+    st = choose_geometry(V, elem, 2, units, *dv, dv->max_dyn[dtype == SSD_F32 ? 0 : 1], &g);
+    if (st != SSD_OK) return st;
+
+    P.tgt = tgt;
+    P.drf = drf;
+    P.tgt_seq_stride = static_cast<int64_t>(K + 1) * V;
+    P.drf_seq_stride = static_cast<int64_t>(drf_rows) * V;
+    P.B = B;
+    P.K = K;
+    P.V = V;
+    P.CL = g.CL;
+    P.slice = g.slice;
+    P.row_buf_bytes = g.row_buf_bytes;
+    P.mode = mode;
+    if (verify && !cache) P.mode |= ssd::kModeEarlyExit;
+    P.tokens = tokens;
+    P.uniforms = uniforms;
+    P.temperature = temperature;
+    P.reshape = reshape;
+    P.budget = budget;
+    P.cache_tok = cache_tok;
+    P.accept_len = accept_len;
+    P.bonus = bonus;
+    P.p_tok = p_tok;
+    P.q_tok = q_tok;
+    P.hit = hit;
+    P.slot = slot;
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    P.rec = reinterpret_cast<ssd::UnitRecord *>(ws);
+    P.seq_count = reinterpret_cast<uint32_t *>(ws + ssd::ws_rec_bytes(B, K));
+    P.seq_reject =
+        reinterpret_cast<uint32_t *>(ws + ssd::ws_rec_bytes(B, K) + ssd::ws_count_bytes(B));
+    P.dev_status = dev_status;
+    const int grid = units * g.CL;
+    return ssd::unit_launch(dtype, P, grid, g.CL, g.dyn, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *ssd_strerror(int status) {
+    switch (status) {
+        case SSD_OK: return "SSD_OK";
+        case SSD_ERR_INVALID_ARG: return "SSD_ERR_INVALID_ARG: invalid argument";
+        case SSD_ERR_DTYPE: return "SSD_ERR_DTYPE: unsupported logit dtype";
+        case SSD_ERR_CUDA: return "SSD_ERR_CUDA: CUDA runtime error";
+        case SSD_ERR_WORKSPACE: return "SSD_ERR_WORKSPACE: workspace missing, misaligned or too small";
+        case SSD_ERR_UNSUPPORTED: return "SSD_ERR_UNSUPPORTED: size or device not supported";
+        default: return "unknown ssd status";
+    }
+}
+
+const char *ssd_version(void) { return "libssd 0.1 (sm_103a)"; }
+
+size_t ssd_workspace_size(int B, int K) {
+    if (B < 1 || K < 1 || K > SSD_MAX_K) return 0;
+    return ssd::ws_total_bytes(B, K);
+}
+
+int ssd_verify(const void *tgt, const void *drf, int dtype, int B, int K, int V, int drf_rows,
+               const int32_t *tokens, const float *uniforms, const float *temperature,
+               const ssd_reshape_desc *reshape, int32_t *accept_len, int32_t *bonus,
+               float *p_tok, float *q_tok, void *workspace, size_t workspace_bytes,
+               int32_t *dev_status, void *stream) {
+    return run_units(ssd::kModeVerify, tgt, drf, dtype, B, K, V, drf_rows, tokens, uniforms,
+                     temperature, reshape, nullptr, 0, accept_len, bonus, p_tok, q_tok, nullptr,
+                     nullptr, nullptr, workspace, workspace_bytes, dev_status, stream);
+}
+
+int ssd_build_cache(const void *tgt, const void *drf, int dtype, int B, int K, int V,
+                    int drf_rows, const int32_t *tokens, const float *temperature,
+                    const ssd_reshape_desc *reshape, const int32_t *F_host, int budget,
+                    int32_t *cache_tok, void *workspace, size_t workspace_bytes,
+                    int32_t *dev_status, void *stream) {
+    return run_units(ssd::kModeCache, tgt, drf, dtype, B, K, V, drf_rows, tokens, nullptr,
+                     temperature, reshape, F_host, budget, nullptr, nullptr, nullptr, nullptr,
+                     cache_tok, nullptr, nullptr, workspace, workspace_bytes, dev_status, stream);
+}
+
+int ssd_round(const void *tgt, const void *drf, int dtype, int B, int K, int V, int drf_rows,
+              const int32_t *tokens, const float *uniforms, const float *temperature,
+              const ssd_reshape_desc *reshape, const int32_t *F_host, int budget,
+              int32_t *accept_len, int32_t *bonus, float *p_tok, float *q_tok,
+              int32_t *cache_tok, uint8_t *hit, int32_t *slot, void *workspace,
+              size_t workspace_bytes, int32_t *dev_status, void *stream) {
+    return run_units(ssd::kModeVerify | ssd::kModeCache | ssd::kModeLookup, tgt, drf, dtype, B, K,
+                     V, drf_rows, tokens, uniforms, temperature, reshape, F_host, budget,
+                     accept_len, bonus, p_tok, q_tok, cache_tok, hit, slot, workspace,
+                     workspace_bytes, dev_status, stream);
+}
+
+int ssd_cache_lookup(const int32_t *cache_tok, int B, int K, int budget, const int32_t *F_host,
+                     const int32_t *accept_len, const int32_t *bonus, uint8_t *hit,
+                     int32_t *slot, void *stream) {
+    if (B < 1 || K < 1 || K > SSD_MAX_K) return SSD_ERR_INVALID_ARG;
+    if (!accept_len || !bonus || !hit || !slot) return SSD_ERR_INVALID_ARG;
+    ssd::LookupParams P = {};
+    const int st = check_fanout(F_host, K, INT_MAX, budget, P.off);
+    if (st != SSD_OK) return st;
+    if (P.off[K + 1] > 0 && !cache_tok) return SSD_ERR_INVALID_ARG;
+    P.cache_tok = cache_tok;
+    P.B = B;
+    P.K = K;
+    P.budget = budget;
+    P.accept_len = accept_len;
+    P.bonus = bonus;
+    P.hit = hit;
+    P.slot = slot;
+    return ssd::lookup_launch(P, stream);
+}
+
+int ssd_reshape_draft(const void *drf, int dtype, int rows, int V, const float *temperature_rows,
+                      int F, float C, ssd_reshape_desc *desc, float *q_out, int32_t *dev_status,
+                      void *stream) {
+    if (dtype != SSD_F32 && dtype != SSD_BF16) return SSD_ERR_DTYPE;
+    if (!drf || !desc || rows < 1 || V < 2) return SSD_ERR_INVALID_ARG;
+    if (F < 0 || F > SSD_MAX_F || F > V) return SSD_ERR_INVALID_ARG;
+    if (!(C >= 0.f && C <= 1.f)) return SSD_ERR_INVALID_ARG;
+    if (C == 0.f && F >= V) return SSD_ERR_INVALID_ARG;
+    if (q_out && !temperature_rows) return SSD_ERR_INVALID_ARG;
+    if (V > (dtype == SSD_F32 ? SSD_MAX_V_F32 : SSD_MAX_V_BF16)) return SSD_ERR_UNSUPPORTED;
+    DeviceInfo *dv = nullptr;
+    int st = device_info(&dv);
+    if (st != SSD_OK) return st;
+    const int elem = dtype == SSD_F32 ? 4 : 2;
+    Geometry g;
+    st = choose_geometry(V, elem, 1, rows, *dv, dv->max_dyn[dtype == SSD_F32 ? 2 : 3], &g);
+    if (st != SSD_OK) return st;
+    ssd::ReshapeParams P = {};
+    P.drf = drf;
+    P.rows = rows;
+    P.V = V;
+    P.CL = g.CL;
+    P.slice = g.slice;
+    P.row_buf_bytes = g.row_buf_bytes;
+    P.tau = temperature_rows;
+    P.F = F;
+    P.C = C;
+    P.desc = desc;
+    P.q_out = q_out;
+    P.dev_status = dev_status;
+    const int grid = rows * g.CL;
+    return ssd::reshape_launch(dtype, P, grid, g.CL, g.dyn, stream);
+}
+
+}  // extern "C"
