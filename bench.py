@@ -49,7 +49,17 @@ def parse():
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the workload's batch (greedy share scaled); for profiling")
     return ap.parse_args()
+
+
+def chosen_workload(args):
+    wl = synth.WORKLOADS[args.workload]
+    if args.batch:
+        g = wl.greedy_first * args.batch // wl.B if wl.greedy_first else 0
+        wl = wl.replace(B=args.batch, greedy_first=g)
+    return wl
 
 
 def dist_env():
@@ -207,7 +217,7 @@ def run_ours(args):
     import speculative_decoding_verification_ssd_gb300 as ssd
     from speculative_decoding_verification_ssd_gb300 import _build
 
-    wl = synth.WORKLOADS[args.workload]
+    wl = chosen_workload(args)
     inp = synth.make_inputs(wl, synth.BENCH_SEED[wl.name] + rank)
     F, off = ssd.ssd_fanout(wl.K, max(wl.budget, 0), wl.a_p or 0.5, wl.r, wl.V) if wl.budget else (
         np.zeros(wl.K + 1, np.int32), np.zeros(wl.K + 2, np.int32))
@@ -343,7 +353,7 @@ def run_reference(args):
     if rank != 0:
         return
     import oracle
-    wl = synth.WORKLOADS[args.workload]
+    wl = chosen_workload(args)
     inp = synth.make_inputs(wl, synth.BENCH_SEED[wl.name])
     F, off, _ = oracle.fanout(wl.K, wl.budget, wl.a_p, wl.r, wl.V) if wl.budget else (
         None, np.zeros(wl.K + 2, np.int32), None)

@@ -262,14 +262,24 @@ def ssd_round(tgt, drf, tokens, uniforms, temperature, F, budget, reshape=None, 
     _dev(temperature, "temperature", torch.float32)
     Fh = _F_host(F)
     o = dict(out) if out is not None else {}
-    o.setdefault("accept_len", torch.empty(B, dtype=torch.int32, device=dev))
-    o.setdefault("bonus", torch.empty(B, dtype=torch.int32, device=dev))
-    if probs:
-        o.setdefault("p_tok", torch.empty((B, K), dtype=torch.float32, device=dev))
-        o.setdefault("q_tok", torch.empty((B, K), dtype=torch.float32, device=dev))
-    o.setdefault("cache_tok", torch.full((B, budget), -1, dtype=torch.int32, device=dev))
-    o.setdefault("hit", torch.empty(B, dtype=torch.uint8, device=dev))
-    o.setdefault("slot", torch.empty(B, dtype=torch.int32, device=dev))
+    if not probs:
+        o.pop("p_tok", None)
+        o.pop("q_tok", None)
+    # allocate only what the caller did not supply (no work is enqueued otherwise)
+    if "accept_len" not in o:
+        o["accept_len"] = torch.empty(B, dtype=torch.int32, device=dev)
+    if "bonus" not in o:
+        o["bonus"] = torch.empty(B, dtype=torch.int32, device=dev)
+    if probs and "p_tok" not in o:
+        o["p_tok"] = torch.empty((B, K), dtype=torch.float32, device=dev)
+    if probs and "q_tok" not in o:
+        o["q_tok"] = torch.empty((B, K), dtype=torch.float32, device=dev)
+    if "cache_tok" not in o:
+        o["cache_tok"] = torch.full((B, budget), -1, dtype=torch.int32, device=dev)
+    if "hit" not in o:
+        o["hit"] = torch.empty(B, dtype=torch.uint8, device=dev)
+    if "slot" not in o:
+        o["slot"] = torch.empty(B, dtype=torch.int32, device=dev)
     ws = _workspace(workspace, B, K, dev)
     _check(lib().ssd_round(
         _ptr(tgt), _ptr(drf), _logit_dtype(tgt), B, K, V, drf_rows, _ptr(tokens), _ptr(uniforms),
