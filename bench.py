@@ -329,7 +329,7 @@ def run_ours(args):
                      "frac": achieved / peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
                      "traffic": traffic_record(_build.source_digest()),
-                     "kernel": "ssd_unit_kernel<BF16Tag>"},
+                     "kernel": "ssd_stream_kernel<BF16Tag>"},
         "e2e": {"value": world * args.e2e_steps / (e2e_ms * 1e-3), "unit": "rounds/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps,

@@ -14,6 +14,7 @@
 #include "ssd_device.cuh"
 #include "ssd_launch.cuh"
 #include "ssd_reshape.cuh"
+#include "ssd_stream.cuh"
 #include "ssd_unit.cuh"
 
 namespace {
@@ -26,7 +27,7 @@ struct DeviceInfo {
     int status = SSD_OK;
     int sm_count = 0;
     int max_cluster = 8;       // 16 when the non-portable size is available
-    size_t max_dyn[5] = {0};   // max dynamic smem: unit f32, unit bf16, reshape f32, reshape bf16
+    size_t max_dyn[6] = {0};   // max dynamic smem: unit f32/bf16, reshape f32/bf16, stream f32/bf16
 };
 
 DeviceInfo g_dev[kMaxDevices];
@@ -49,6 +50,8 @@ int device_info(DeviceInfo **out) {
         st = st ? st : ssd::unit_setup(SSD_BF16, optin, &d.max_dyn[1], &allow16);
         st = st ? st : ssd::reshape_setup(SSD_F32, optin, &d.max_dyn[2], &allow16);
         st = st ? st : ssd::reshape_setup(SSD_BF16, optin, &d.max_dyn[3], &allow16);
+        st = st ? st : ssd::stream_setup(SSD_F32, optin, &d.max_dyn[4]);
+        st = st ? st : ssd::stream_setup(SSD_BF16, optin, &d.max_dyn[5]);
         if (st != SSD_OK) return st;
         d.max_cluster = allow16 ? 16 : 8;
         d.ready = true;
@@ -106,6 +109,18 @@ int choose_geometry(int V, int elem, int rows_staged, int units, const DeviceInf
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+int gcd(int a, int b) { return b == 0 ? a : gcd(b, a % b); }
+
+// A multiplier coprime to B near 0.618 B: the streaming kernel visits sequence
+// (i * m) % B for the i-th unit of a position, which interleaves sequences of
+// different kinds (greedy / sampled) across the persistent CTAs.
+int coprime_stride(int B) {
+    if (B <= 2) return 1;
+    for (int m = static_cast<int>(0.618 * B); m > 1; --m)
+        if (gcd(m, B) == 1) return m;
+    return 1;
+}
+
 int check_fanout(const int32_t *F_host, int K, int V, int budget, int *off) {
     if (!F_host) return SSD_ERR_INVALID_ARG;
     off[0] = 0;
@@ -152,9 +167,17 @@ int run_units(int mode, const void *tgt, const void *drf, int dtype, int B, int 
     if (st != SSD_OK) return st;
     const int elem = dtype == SSD_F32 ? 4 : 2;
     const int units = B * (K + 1);
+    // The persistent streaming kernel needs every row on a 16-byte boundary and
+    // its per-group arrays within shared memory; other inputs take the cluster kernel.
+    const size_t sdyn = ssd::stream_dyn_bytes(V);
+    const bool streaming = aligned(tgt, 16) && aligned(drf, 16) &&
+                           (static_cast<long long>(V) * elem) % 16 == 0 &&
+                           sdyn <= dv->max_dyn[dtype == SSD_F32 ? 4 : 5];
     Geometry g;
-    st = choose_geometry(V, elem, 2, units, *dv, dv->max_dyn[dtype == SSD_F32 ? 0 : 1], &g);
-    if (st != SSD_OK) return st;
+    if (!streaming) {
+        st = choose_geometry(V, elem, 2, units, *dv, dv->max_dyn[dtype == SSD_F32 ? 0 : 1], &g);
+        if (st != SSD_OK) return st;
+    }
 
     P.tgt = tgt;
     P.drf = drf;
@@ -186,6 +209,14 @@ int run_units(int mode, const void *tgt, const void *drf, int dtype, int B, int 
     P.seq_reject =
         reinterpret_cast<uint32_t *>(ws + ssd::ws_rec_bytes(B, K) + ssd::ws_count_bytes(B));
     P.dev_status = dev_status;
+    uint32_t *sched = reinterpret_cast<uint32_t *>(ws + ssd::ws_rec_bytes(B, K) + 2 * ssd::ws_count_bytes(B));
+    P.unit_counter = sched;
+    P.exit_counter = sched + 1;
+    P.perm_mul = coprime_stride(B);
+    if (streaming) {
+        const int grid = std::min(dv->sm_count, units);
+        return ssd::stream_launch(dtype, P, grid, sdyn, stream);
+    }
     const int grid = units * g.CL;
     return ssd::unit_launch(dtype, P, grid, g.CL, g.dyn, stream);
 }

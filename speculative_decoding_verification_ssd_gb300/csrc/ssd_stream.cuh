@@ -1,0 +1,27 @@
+// ssd_stream.cuh -- geometry of the persistent streaming kernel (ssd_stream.cu),
+// shared with the host launcher.
+#pragma once
+
+#include <cstddef>
+
+namespace ssd {
+
+constexpr int kStreamConsumerWarps = 16;
+constexpr int kStreamThreads = kStreamConsumerWarps * 32 + 32;  // + one producer warp
+constexpr int kStreamStages = 8;
+constexpr int kStreamStageBytes = 16384;
+constexpr int kGroupTokens = 32;
+
+// Dynamic shared memory of the streaming kernel for a vocabulary of V tokens:
+// the stage ring plus two float arrays with one entry per 32-token group.
+inline size_t stream_dyn_bytes(int V) {
+    const size_t G = (static_cast<size_t>(V) + kGroupTokens - 1) / kGroupTokens;
+    const size_t Gp = (G + 31) & ~static_cast<size_t>(31);
+    return static_cast<size_t>(kStreamStages) * kStreamStageBytes + 2 * Gp * sizeof(float);
+}
+
+struct UnitParams;
+int stream_setup(int dtype, size_t optin, size_t *max_dyn);
+int stream_launch(int dtype, const UnitParams &P, int grid, size_t dyn, void *stream);
+
+}  // namespace ssd

@@ -10,25 +10,27 @@
 // samples (tau > 0) and k < K -- into shared memory with bulk asynchronous
 // copies, so every logit byte crosses HBM exactly once:
 //
-//  pass 1  (smem)   per-slice online softmax statistics in base 2
-//                   (m = max z/tau * log2 e, S = sum 2^(x - m)) of both rows,
-//                   or the largest raw (value, id) key for greedy rows;
+//  pass 1  (smem)   per thread over its own 16-byte vectors: the raw maximum
+//                   (packed, NaN-propagating), then the base-2 partial sum
+//                   S = sum 2^(z c - m c), c = log2(e) / tau; greedy rows find
+//                   the lowest id attaining the maximum instead;
 //  exchange 1       partial statistics merged over distributed shared memory in
-//                   rank order (identical result in every CTA);
-//  gathers          rank 0 evaluates p_k(x~_k), q_k(x~_k) and the accept test
-//                   u_k q < p ([SD] step 3; greedy: x~_k == argmax);
-//  pass 2a (smem)   residual w_t = max(0, p_k(t) - q_k(t)) per token: slice mass
-//                   Z_c and the thread maxima for the top-F selection;
-//  pass 2b (smem)   block top-F_k of the cache scores (only candidates above a
-//                   lower bound are materialised);
-//  exchange 2       slice masses and top-F lists; each CTA places its own list
-//                   entries in the sequence's cache row by global rank;
-//  crossing         the CTA holding the CDF crossing u_K Z re-scans its slice
-//                   and records the bonus token t_k that the round draws if it
-//                   stops at k (inverse CDF over ascending token id);
-//  epilogue         the last CTA of the sequence to finish (atomic counter)
-//                   scans the accept bits -> a, picks t_a, writes the outputs
-//                   and looks (a, t_a) up in the cache segment a.
+//                   rank order (bit-identical result in every CTA);
+//  accept           rank 0 evaluates p_k(x~_k), q_k(x~_k) and the test u_k q < p
+//                   ([SD] step 3; greedy: x~_k outranks every other token);
+//  pass 2a (smem)   residual w_t = max(0, p_k(t) - q_k(t)): slice mass Z_c and the
+//                   per-thread maximum;
+//  pass 2b (smem)   block top-F_k: a lower bound theta on the F-th largest value
+//                   (the smallest over warps of each warp's ceil(F/8)-th largest
+//                   thread maximum), then only vectors with a lane >= theta are
+//                   expanded into (value, id) keys and ranked;
+//  exchange 2       slice masses and top-F lists; rank 0 merges the lists by
+//                   global rank into the cache row;
+//  crossing         the CTA holding the CDF crossing of u_K Z re-scans its slice
+//                   and records t_k, the bonus drawn if the round stops at k;
+//  epilogue         the last CTA of the sequence (atomic counter) scans the
+//                   accept bits -> a, picks t_a, writes the outputs and looks
+//                   (a, t_a) up in cache segment a.
 //
 // Operation sources: [SD] "Speculative decoding" (brentwoodlivery.com), "The
 // Algorithm (Step-by-Step)" and "Temperature and Sampling"; [WHY] "Why does
@@ -37,11 +39,10 @@
 // items 1-2 and "整体框架" (cache keys, sigma_{F,C}, hit test).
 #include <cooperative_groups.h>
 
-#include <type_traits>
-
 #include "ssd_device.cuh"
 #include "ssd_launch.cuh"
 #include "ssd_unit.cuh"
+#include "ssd_vec.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -49,14 +50,17 @@ namespace ssd {
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kSortedAt = kThreads;  // rank-sorted candidate lists live at cand[kSortedAt..]
+constexpr unsigned kFull = 0xFFFFFFFFu;
 
 struct Xchg {
     Stat st[2];     // partial (target, draft) statistics of this CTA's slice
-    uint64_t best;  // largest raw key of the slice (greedy rows, row K)
+    uint64_t best;  // largest raw key of the slice (greedy rows)
     float zsum;     // residual mass of the slice
     int flags;
     int skip;
-    int nlist;      // entries of this CTA's top-F list (in cand[])
+    int nlist;      // entries of this CTA's top-F list
+    int list_at;    // offset of the list in cand[]
 };
 
 struct Slice {
@@ -74,6 +78,13 @@ struct DraftShape {  // sigma_{F,C} membership of the draft row ([SSD] item 2)
 
 __device__ __forceinline__ float draft_bias(const DraftShape &r, float z, int e) {
     return (r.on && (z > r.thr || (z == r.thr && e <= r.thr_id))) ? r.l2C : 0.f;
+}
+
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // Computes the smem placement of row slice [lo, hi) and, when `issue`, starts
@@ -123,72 +134,136 @@ __device__ Slice stage_row(const void *row, int lo, int hi, unsigned char *buf, 
     return sl;
 }
 
-template <class D>
-__device__ __forceinline__ void load_vec(const unsigned char *buf, int v, float (&z)[D::kVec]) {
-    decode_vec<D>(*reinterpret_cast<const uint4 *>(buf + 16 * v), z);
+__device__ __forceinline__ uint4 ld_vec(const unsigned char *buf, int off) {
+    return *reinterpret_cast<const uint4 *>(buf + off);
 }
 
-// Loads the VEC elements starting at byte `off` of a staged row; `off` is a
-// multiple of the element size, and of 16 when `vec16` (the common case where
-// both rows of a unit share their 16-byte phase).
+// Loads 16 bytes of a staged row at byte `off` (a multiple of the element size;
+// of 16 when `al16`, the common case where both rows share their 16-byte phase).
 template <class D>
-__device__ __forceinline__ void load_vec_at(const unsigned char *buf, int off, bool vec16,
-                                            float (&z)[D::kVec]) {
-    if (vec16) {
-        decode_vec<D>(*reinterpret_cast<const uint4 *>(buf + off), z);
-        return;
-    }
+__device__ __forceinline__ uint4 ld_vec_any(const unsigned char *buf, int off, bool al16) {
+    if (al16) return ld_vec(buf, off);
+    uint4 w;
+    uint32_t *p = reinterpret_cast<uint32_t *>(&w);
+    if (D::kBytes == 4) {
 #pragma unroll
-    for (int i = 0; i < D::kVec; ++i) {
-        if (D::kBytes == 4)
-            z[i] = *reinterpret_cast<const float *>(buf + off + 4 * i);
-        else
-            z[i] = __uint_as_float(
-                static_cast<uint32_t>(*reinterpret_cast<const uint16_t *>(buf + off + 2 * i)) << 16);
+        for (int i = 0; i < 4; ++i) p[i] = *reinterpret_cast<const uint32_t *>(buf + off + 4 * i);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            p[i] = static_cast<uint32_t>(*reinterpret_cast<const uint16_t *>(buf + off + 4 * i)) |
+                   (static_cast<uint32_t>(*reinterpret_cast<const uint16_t *>(buf + off + 4 * i + 2))
+                    << 16);
     }
+    return w;
 }
 
-// Online base-2 softmax statistics over one vector of values x (masked = -inf).
-template <int VEC>
-__device__ __forceinline__ void stat_update(Stat &st, const float (&x)[VEC]) {
-    float vm = x[0];
+// Merges the base-2 softmax statistics held by the lanes of a warp: the maximum
+// by an integer reduction of the ordered bits, then every lane rescales its
+// sum and the sums are added over a fixed xor tree (the same bits in every
+// lane, every CTA).
+__device__ __forceinline__ Stat warp_stat(Stat s) {
+    const uint32_t mo = __reduce_max_sync(kFull, ordered_bits(s.m));
+    const float M = value_of_ordered(mo);
+    float S = (s.m == -INFINITY) ? 0.f : s.S * ex2(s.m - M);
 #pragma unroll
-    for (int i = 1; i < VEC; ++i) vm = fmaxf(vm, x[i]);
-    if (vm > st.m) {
-        st.S *= ex2(st.m - vm);
-        st.m = vm;
+    for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(kFull, S, o);
+    return {M, M == -INFINITY ? 0.f : S};
+}
+
+// F-th largest (with multiplicity) of the 256 per-thread values v (ordered
+// bits; 0 = no element).  `tops` is 256 words of shared scratch and `out` one
+// word.  All threads call; returns to every thread.
+__device__ uint32_t block_fth_largest(uint32_t v, int F, uint32_t *tops, uint32_t *out) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int Fw = F < 32 ? F : 32;
+    for (int it = 0; it < Fw; ++it) {  // this warp's Fw largest, in order
+        const uint32_t mx = __reduce_max_sync(kFull, v);
+        const uint32_t who = __ballot_sync(kFull, v == mx);
+        if (lane == __ffs(who) - 1) v = 0;
+        if (lane == 0) tops[warp * 32 + it] = mx;
     }
-    if (st.m != -INFINITY) {
-        float acc = 0.f;
+    __syncthreads();
+    if (warp == 0) {
+        uint32_t vals[kWarps];
+        const int nq = kWarps * Fw;
 #pragma unroll
-        for (int i = 0; i < VEC; ++i) acc += ex2(x[i] - st.m);
-        st.S += acc;
+        for (int i = 0; i < kWarps; ++i) {
+            const int q = lane + 32 * i;
+            vals[i] = q < nq ? tops[(q / Fw) * 32 + (q % Fw)] : 0u;
+        }
+        uint32_t mx = 0;
+        for (int it = 0; it < F; ++it) {
+            uint32_t lm = vals[0];
+#pragma unroll
+            for (int i = 1; i < kWarps; ++i) lm = vals[i] > lm ? vals[i] : lm;
+            mx = __reduce_max_sync(kFull, lm);
+            const uint32_t who = __ballot_sync(kFull, lm == mx);
+            if (lane == __ffs(who) - 1) {
+                bool done = false;
+#pragma unroll
+                for (int i = 0; i < kWarps; ++i)
+                    if (!done && vals[i] == mx) {
+                        vals[i] = 0;
+                        done = true;
+                    }
+            }
+        }
+        if (lane == 0) *out = mx;
     }
+    __syncthreads();
+    return *out;
+}
+
+// Sorts cand[0..n) (n <= kCandCap) descending.  n <= kThreads: rank by
+// counting into cand[kSortedAt..]; otherwise an in-place bitonic sort.  Returns
+// the offset of the sorted list.  All threads call; ends synchronised.
+__device__ int sort_candidates(uint64_t *cand, int n) {
+    if (n <= kThreads) {
+        uint64_t key = 0;
+        int rank = 0;
+        if (threadIdx.x < n) {
+            key = cand[threadIdx.x];
+            for (int j = 0; j < n; ++j) rank += cand[j] > key ? 1 : 0;
+        }
+        __syncthreads();
+        if (threadIdx.x < n) cand[kSortedAt + rank] = key;
+        __syncthreads();
+        return kSortedAt;
+    }
+    const int p2 = next_pow2(n);
+    for (int i = n + threadIdx.x; i < p2; i += kThreads) cand[i] = 0;
+    __syncthreads();
+    block_sort_desc(cand, p2);
+    return 0;
 }
 
 }  // namespace
 
 template <class D>
-__global__ void __launch_bounds__(kThreads) ssd_unit_kernel(const __grid_constant__ UnitParams P) {
+__global__ void __launch_bounds__(kThreads, 3) ssd_unit_kernel(const __grid_constant__ UnitParams P) {
     constexpr int VEC = D::kVec;
     extern __shared__ __align__(128) unsigned char dyn_smem[];
     __shared__ __align__(16) uint64_t cand[kCandCap];
-    __shared__ double dscan[kThreads];
+    __shared__ __align__(16) uint64_t mergebuf[kCandCap];
     __shared__ Xchg xc;
     __shared__ __align__(8) uint64_t bars[2];
-    __shared__ Stat red_stat[kWarps];
-    __shared__ float red_f[kWarps];
-    __shared__ uint64_t red_u[kWarps];
-    __shared__ int s_cnt;
-    __shared__ int s_int[4];
+    __shared__ Stat w_st[2][kWarps];
+    __shared__ uint64_t w_key[kWarps];
+    __shared__ float w_f[kWarps];
+    __shared__ double w_d[kWarps];
+    __shared__ uint32_t w_u[kWarps];
+    __shared__ int w_i[kWarps];
+    __shared__ int s_int[8];
+    __shared__ int s_base[16], s_at[16];
     __shared__ Stat g_stat[2];
     __shared__ uint64_t g_best;
     __shared__ int g_flags, g_skip;
-    __shared__ double pm[16];   // per-rank partial masses (crossing search)
+    __shared__ double pm[16];   // per-rank p-mass of the target row (crossing search)
     __shared__ double s_cut;
 
     cg::cluster_group cluster = cg::this_cluster();
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int CL = P.CL;
     const int rank = static_cast<int>(cluster.block_rank());
     const int unit = blockIdx.x / CL;
@@ -227,8 +302,7 @@ __global__ void __launch_bounds__(kThreads) ssd_unit_kernel(const __grid_constan
         shape.on = d.F > 0;
         shape.thr = d.thr_val;
         shape.thr_id = d.thr_id;
-        shape.l2C = d.C > 0.f ? lg2(d.C) : -INFINITY;
-        if (d.C == 1.f) shape.l2C = 0.f;
+        shape.l2C = d.C > 0.f ? (d.C == 1.f ? 0.f : lg2(d.C)) : -INFINITY;
     }
 
     // ---- staging ----------------------------------------------------------
@@ -260,109 +334,213 @@ __global__ void __launch_bounds__(kThreads) ssd_unit_kernel(const __grid_constan
         const Slice sd = stage_row<D>(drf_row, lo, hi, buf_d, &bars[1], true);
         dshift = (sl.ebase - sd.ebase) * D::kBytes;
     }
-    auto load_d = [&](int v, float (&zd)[VEC]) {
-        load_vec_at<D>(buf_d, 16 * v + dshift, dshift == 0, zd);
-    };
+    const bool dal = dshift == 0;
+    // The accept test's gathers: issued now so their latency hides behind the copy.
+    float ztx = 0.f, zdx = 0.f, u_k = 0.f;
+    if (rank == 0 && tid == 32 && active && !rowK) {
+        ztx = load_logit<D>(tgt_row, xt);
+        if (pair) {
+            zdx = load_logit<D>(drf_row, xt);
+            u_k = P.uniforms ? P.uniforms[static_cast<int64_t>(b) * (K + 1) + k] : 0.f;
+        }
+    }
     __syncthreads();  // scalar head/tail stores visible
     if (active) {
         bool ok = mbar_wait_bounded(&bars[0], 0);
         if (need_d) ok = mbar_wait_bounded(&bars[1], 0) && ok;
         if (!ok) atomicOr(&s_int[1], 1);
     }
+    // Lanes of the edge vectors outside [lo, hi), and the drafted token of a greedy
+    // row (ranked last), are overwritten with -inf once, so the passes below read
+    // the staged rows without per-vector checks.  A draft row staged with another
+    // 16-byte phase than the target keeps per-load masking instead.
+    const bool excl = greedy && !rowK;  // greedy rows rank the drafted token last
+    const int xmask = excl ? xt : -1;
+    if (active && tid < 3 && sl.nv > 0) {
+        int v = -1;
+        if (tid == 0) v = 0;
+        if (tid == 1 && sl.nv > 1) v = sl.nv - 1;
+        if (tid == 2 && xmask >= lo && xmask < hi) {
+            v = (xmask - sl.ebase) / VEC;
+            if (v == 0 || v == sl.nv - 1) v = -1;  // already patched by thread 0 or 1
+        }
+        if (v >= 0) {
+            const int e0 = sl.ebase + v * VEC;
+            uint4 w = ld_vec(buf_t, 16 * v);
+            mask_vec<D>(w, e0, lo, hi, xmask);
+            *reinterpret_cast<uint4 *>(buf_t + 16 * v) = w;
+            if (need_d && dshift == 0 && tid < 2) {
+                uint4 wd = ld_vec(buf_d, 16 * v);
+                mask_vec<D>(wd, e0, lo, hi, -1);
+                *reinterpret_cast<uint4 *>(buf_d + 16 * v) = wd;
+            }
+        }
+    }
     __syncthreads();
     if (s_int[1]) flags |= SSD_DEV_TIMEOUT;  // uniform across the CTA
 
-    // ---- pass 1: statistics / raw maxima ----------------------------------
-    const bool want_raw = active && (greedy || (rowK && Fk > 0));
-    const bool excl = greedy && !rowK;  // greedy rows rank the drafted token last
+    auto load_t = [&](int v) { return ld_vec(buf_t, 16 * v); };
+    auto load_d = [&](int v) {
+        if (dal) return ld_vec(buf_d, 16 * v);
+        uint4 w = ld_vec_any<D>(buf_d, 16 * v + dshift, false);
+        const int e0 = sl.ebase + v * VEC;
+        if (e0 < lo || e0 + VEC > hi) mask_vec<D>(w, e0, lo, hi, -1);
+        return w;
+    };
+
+    // ---- pass 1 -------------------------------------------------------------
     Stat st_t{-INFINITY, 0.f}, st_d{-INFINITY, 0.f};
-    uint64_t best = 0;
+    uint64_t best = 0;           // greedy: largest (value, lowest id) key of the thread
+    float tmax_raw = -INFINITY;  // raw maximum of the thread's target elements
     if (active) {
-        auto body = [&](auto full_c, int v) {
-            constexpr bool FULL = decltype(full_c)::value;
-            const int e0 = sl.ebase + v * VEC;
-            float zt[VEC];
-            load_vec<D>(buf_t, v, zt);
-            if (sampled) {
-                float x[VEC];
+        RawMax<D> rm;
+        for (int v = tid; v < sl.nv; v += kThreads) rm.add(load_t(v));
+        tmax_raw = rm.get();
+        if (sampled && tmax_raw != -INFINITY) {
+            const float mc = tmax_raw * c;
+            float2 acc = make_float2(0.f, 0.f);
+            for (int v = tid; v < sl.nv; v += kThreads) acc = exp_sum<D>(load_t(v), c, mc, acc);
+            st_t = {mc, acc.x + acc.y};
+        }
+        if (greedy) {
+            if (tmax_raw != tmax_raw) {
+                best = ~0ull;  // NaN logits: flagged after the merge
+            } else {
+                // the lowest id attaining the thread maximum
+                for (int v = tid; v < sl.nv; v += kThreads) {
+                    const uint4 w = load_t(v);
+                    if (ge_lanes<D>(w, tmax_raw) == 0) continue;
+                    float z[VEC];
+                    decode_vec<D>(w, z);
+                    const int e0 = sl.ebase + v * VEC;
+                    int e = -1;
 #pragma unroll
-                for (int i = 0; i < VEC; ++i) {
-                    const int e = e0 + i;
-                    x[i] = (FULL || (e >= lo && e < hi)) ? zt[i] * c : -INFINITY;
-                }
-                stat_update<VEC>(st_t, x);
-            }
-            if (want_raw) {
-#pragma unroll
-                for (int i = 0; i < VEC; ++i) {
-                    const int e = e0 + i;
-                    if (FULL || (e >= lo && e < hi)) {
-                        const uint64_t key = (excl && e == xt) ? excluded_key(e) : make_key(zt[i], e);
-                        best = key > best ? key : best;
+                    for (int i = VEC - 1; i >= 0; --i) {
+                        const int ei = e0 + i;
+                        if (z[i] == tmax_raw && ei >= lo && ei < hi && ei != xmask) e = ei;
+                    }
+                    if (e >= 0) {
+                        best = make_key(tmax_raw, e);
+                        break;
                     }
                 }
             }
-            if (pair) {
-                float zd[VEC], x[VEC];
-                load_d(v, zd);
-#pragma unroll
-                for (int i = 0; i < VEC; ++i) {
-                    const int e = e0 + i;
-                    x[i] = (FULL || (e >= lo && e < hi)) ? zd[i] * c + draft_bias(shape, zd[i], e)
-                                                         : -INFINITY;
+        }
+        if (pair) {
+            if (!shape.on) {
+                RawMax<D> rd;
+                for (int v = tid; v < sl.nv; v += kThreads) rd.add(load_d(v));
+                const float dm = rd.get();
+                if (dm != -INFINITY) {
+                    const float mc = dm * c;
+                    float2 acc = make_float2(0.f, 0.f);
+                    for (int v = tid; v < sl.nv; v += kThreads)
+                        acc = exp_sum<D>(load_d(v), c, mc, acc);
+                    st_d = {mc, acc.x + acc.y};
                 }
-                stat_update<VEC>(st_d, x);
+            } else {
+                // reshaped draft: x = z c + log2 c_t, maximum over the weighted values
+                float xm = -INFINITY;
+                for (int v = tid; v < sl.nv; v += kThreads) {
+                    float z[VEC];
+                    decode_vec<D>(load_d(v), z);
+                    const int e0 = sl.ebase + v * VEC;
+#pragma unroll
+                    for (int i = 0; i < VEC; ++i)
+                        xm = fmax_nan(xm, z[i] * c + draft_bias(shape, z[i], e0 + i));
+                }
+                if (xm != -INFINITY) {
+                    float s = 0.f;
+                    for (int v = tid; v < sl.nv; v += kThreads) {
+                        float z[VEC];
+                        decode_vec<D>(load_d(v), z);
+                        const int e0 = sl.ebase + v * VEC;
+#pragma unroll
+                        for (int i = 0; i < VEC; ++i)
+                            s += ex2(z[i] * c + draft_bias(shape, z[i], e0 + i) - xm);
+                    }
+                    st_d = {xm, s};
+                }
             }
-        };
-        for (int v = tid; v < sl.nv; v += kThreads) {
-            const int e0 = sl.ebase + v * VEC;
-            if (e0 >= lo && e0 + VEC <= hi)
-                body(std::true_type{}, v);
-            else
-                body(std::false_type{}, v);
         }
     }
-    const uint64_t my_best = best;  // this thread's raw maximum (top-F lower bound)
-    st_t = block_stat(st_t, red_stat);
-    st_d = block_stat(st_d, red_stat);
-    best = block_max_u64(best, red_u);
+
+    // block reduction: statistics of both rows and the greedy key
+    st_t = warp_stat(st_t);
+    st_d = warp_stat(st_d);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const uint64_t ob = __shfl_xor_sync(kFull, best, o);
+        best = ob > best ? ob : best;
+    }
+    if (lane == 0) {
+        w_st[0][warp] = st_t;
+        w_st[1][warp] = st_d;
+        w_key[warp] = best;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        Stat a{-INFINITY, 0.f}, d{-INFINITY, 0.f};
+        uint64_t bb = 0;
+        if (lane < kWarps) {
+            a = w_st[0][lane];
+            d = w_st[1][lane];
+            bb = w_key[lane];
+        }
+        a = warp_stat(a);
+        d = warp_stat(d);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const uint64_t ob = __shfl_xor_sync(kFull, bb, o);
+            bb = ob > bb ? ob : bb;
+        }
+        if (lane == 0) {
+            xc.st[0] = a;
+            xc.st[1] = d;
+            xc.best = bb;
+            xc.flags = flags;
+            xc.skip = skip;
+            xc.zsum = 0.f;
+            xc.nlist = 0;
+            xc.list_at = 0;
+        }
+    }
 
     // ---- exchange 1 ---------------------------------------------------------
-    if (tid == 0) {
-        xc.st[0] = st_t;
-        xc.st[1] = st_d;
-        xc.best = best;
-        xc.flags = flags;
-        xc.skip = skip;
-        xc.zsum = 0.f;
-        xc.nlist = 0;
-    }
     cluster.sync();
-    if (tid == 0) {
-        Stat gt{-INFINITY, 0.f}, gd{-INFINITY, 0.f};
-        uint64_t gb = 0;
-        int gf = 0, gs = 0;
-        Stat part[16];
-        for (int j = 0; j < CL; ++j) {
-            const Xchg *px = cluster.map_shared_rank(&xc, j);
-            part[j] = px->st[0];
-            gt = stat_merge(gt, part[j]);
-            gd = stat_merge(gd, px->st[1]);
-            const uint64_t pb = px->best;
-            gb = pb > gb ? pb : gb;
-            gf |= px->flags;
-            gs |= px->skip;
+    if (warp == 0) {
+        Stat a{-INFINITY, 0.f}, d{-INFINITY, 0.f};
+        uint64_t pb = 0;
+        uint32_t pf = 0, ps = 0;
+        if (lane < CL) {
+            const Xchg *px = cluster.map_shared_rank(&xc, lane);
+            a = px->st[0];
+            d = px->st[1];
+            pb = px->best;
+            pf = static_cast<uint32_t>(px->flags);
+            ps = static_cast<uint32_t>(px->skip);
         }
-        // target p-mass of each slice relative to the global maximum (crossing search)
-        for (int j = 0; j < CL; ++j)
-            pm[j] = (part[j].m == -INFINITY)
-                        ? 0.0
-                        : static_cast<double>(part[j].S) * static_cast<double>(ex2(part[j].m - gt.m));
-        g_stat[0] = gt;
-        g_stat[1] = gd;
-        g_best = gb;
-        g_flags = gf;
-        g_skip = gs;
+        // every CTA merges the same lanes with the same tree: identical bits
+        const Stat gt = warp_stat(a), gd = warp_stat(d);
+        uint64_t gb = pb;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const uint64_t x = __shfl_xor_sync(kFull, gb, o);
+            gb = x > gb ? x : gb;
+        }
+        const uint32_t gf = __reduce_or_sync(kFull, pf);
+        const uint32_t gs = __reduce_or_sync(kFull, ps);
+        if (lane < CL)
+            pm[lane] = (a.m == -INFINITY)
+                           ? 0.0
+                           : static_cast<double>(a.S) * static_cast<double>(ex2(a.m - gt.m));
+        if (lane == 0) {
+            g_stat[0] = gt;
+            g_stat[1] = gd;
+            g_best = gb;
+            g_flags = static_cast<int>(gf);
+            g_skip = static_cast<int>(gs);
+        }
     }
     __syncthreads();
     const Stat gT = g_stat[0], gD = g_stat[1];
@@ -377,19 +555,14 @@ __global__ void __launch_bounds__(kThreads) ssd_unit_kernel(const __grid_constan
             active = false;
         }
     }
-    if (active && want_raw) {
-        const float bv = key_value(g_best);
-        if (bv != bv) {
-            flags |= SSD_DEV_NONFINITE;
-            active = false;
-        }
+    if (active && greedy && (g_best == ~0ull || g_best == 0)) {
+        flags |= SSD_DEV_NONFINITE;  // NaN logits
+        active = false;
     }
 
-    // ---- gathers and the accept test (rank 0) -------------------------------
-    const float invT = active && sampled ? 1.f / gT.S : 0.f;
-    const float invD = active && pair ? 1.f / gD.S : 0.f;
+    // ---- the accept test (rank 0; thread 32 holds the gathers) --------------
     UnitRecord *rec = P.rec + static_cast<int64_t>(b) * (K + 1) + k;
-    if (rank == 0 && tid == 0) {
+    if (rank == 0 && tid == 32) {
         UnitRecord r{};
         r.flags = flags;
         r.state = skip ? 2 : 1;
@@ -398,15 +571,12 @@ __global__ void __launch_bounds__(kThreads) ssd_unit_kernel(const __grid_constan
         r.p_tok = NAN;
         r.q_tok = NAN;
         if (active && !rowK) {
-            const float ztx = load_logit<D>(tgt_row, xt);
             if (pair) {
-                const float zdx = load_logit<D>(drf_row, xt);
                 const float p = ex2(ztx * c - gT.m) / gT.S;
                 const float q = ex2(zdx * c + draft_bias(shape, zdx, xt) - gD.m) / gD.S;
-                const float u = P.uniforms ? P.uniforms[static_cast<int64_t>(b) * (K + 1) + k] : 0.f;
                 r.p_tok = p;
                 r.q_tok = q;
-                r.accept = (u * q < p) ? 1 : 0;
+                r.accept = (u_k * q < p) ? 1 : 0;
             } else {  // greedy: accepted iff x~ outranks every other token
                 r.accept = make_key(ztx, xt) > g_best ? 1 : 0;
                 r.p_tok = r.accept ? 1.f : 0.f;
@@ -424,260 +594,317 @@ __global__ void __launch_bounds__(kThreads) ssd_unit_kernel(const __grid_constan
     }
 
     // ---- pass 2a: residual mass and thread maxima (pair units) -------------
+    // w_t = 2^(z_p c - L_T) - 2^(z_q c + log2 c_t - L_D) where positive, with
+    // L = m + log2 S the base-2 log-normaliser of each row.
     const bool want_resid = active && pair && (do_verify || Fk > 0);
-    float zsum = 0.f;
-    uint64_t tbest = 0;
-    // gate: p_t > q_t  <=>  (x_p - m_T) - (x_q - m_D) > log2 S_T - log2 S_D
-    const float dthr = want_resid ? lg2(gT.S) - lg2(gD.S) : 0.f;
-    auto resid = [&](float zt, float zd, int e) -> float {
-        const float xp = zt * c - gT.m;
-        const float xq = zd * c + draft_bias(shape, zd, e) - gD.m;
-        float w = 0.f;
-        if (xp - xq > dthr) w = fmaxf(ex2(xp) * invT - ex2(xq) * invD, 0.f);
-        return w;
+    const float LT = active && sampled ? gT.m + lg2(gT.S) : 0.f;
+    const float LD = active && pair ? gD.m + lg2(gD.S) : 0.f;
+    auto resid1 = [&](float zp, float zq, int e) -> float {
+        const float xp = zp * c - LT;
+        const float xq = zq * c + draft_bias(shape, zq, e) - LD;
+        return xp > xq ? fmaxf(ex2(xp) - ex2(xq), 0.f) : 0.f;
     };
+    float zsum = 0.f;
+    float tmax_res = -1.f;
     if (want_resid) {
-        float acc[2] = {0.f, 0.f};
-        float bs = -1.f;
-        int bid = 0;
-        auto body = [&](auto full_c, int v) {
-            constexpr bool FULL = decltype(full_c)::value;
-            const int e0 = sl.ebase + v * VEC;
+        float2 acc = make_float2(0.f, 0.f);
+        for (int v = tid; v < sl.nv; v += kThreads) {
             float zt[VEC], zd[VEC];
-            load_vec<D>(buf_t, v, zt);
-            load_d(v, zd);
+            decode_vec<D>(load_t(v), zt);
+            decode_vec<D>(load_d(v), zd);
+            const int e0 = sl.ebase + v * VEC;
 #pragma unroll
-            for (int i = 0; i < VEC; ++i) {
-                const int e = e0 + i;
-                if (FULL || (e >= lo && e < hi)) {
-                    const float w = resid(zt[i], zd[i], e);
-                    acc[i & 1] += w;
-                    if (w > bs) {
-                        bs = w;
-                        bid = e;
+            for (int i = 0; i < VEC; i += 2) {
+                const float w0 = resid1(zt[i], zd[i], e0 + i);
+                const float w1 = resid1(zt[i + 1], zd[i + 1], e0 + i + 1);
+                acc = __fadd2_rn(acc, make_float2(w0, w1));
+                tmax_res = fmaxf(tmax_res, fmaxf(w0, w1));
+            }
+        }
+        zsum = acc.x + acc.y;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) zsum += __shfl_xor_sync(kFull, zsum, o);
+        if (lane == 0) w_f[warp] = zsum;
+        __syncthreads();
+        zsum = w_f[0];
+        for (int w = 1; w < kWarps; ++w) zsum += w_f[w];
+    }
+
+    // ---- pass 2b: block top-F_k of the cache scores --------------------------
+    int nlist = 0, list_at = 0;
+    if (active && Fk > 0) {
+        // theta: the F-th largest of the 256 thread maxima (F distinct elements reach it)
+        uint32_t tv = 0;  // ordered bits of this thread's maximum (0 = no element)
+        if (tid < sl.nv) {
+            if (pair)
+                tv = tmax_res >= 0.f ? ordered_bits(tmax_res) : 0u;
+            else
+                tv = ordered_bits(tmax_raw);
+        }
+        uint32_t theta_u = block_fth_largest(tv, Fk, reinterpret_cast<uint32_t *>(mergebuf), &w_u[0]);
+        if (tid == 0) s_int[2] = 0;
+        __syncthreads();
+        uint64_t theta = static_cast<uint64_t>(theta_u) << 32;
+        int count = 0;
+        for (int round = 0; round < 64; ++round) {
+            if (pair) {
+                // w_t <= p_t, so only tokens with z_p >= zthr can reach the threshold
+                const bool filt = theta_u > 0x80000000u;  // threshold value > 0
+                float zthr = -INFINITY;
+                if (filt)
+                    zthr = round_down_storage<D>((lg2(value_of_ordered(theta_u)) + LT - 1e-3f) / c -
+                                                 1e-3f);
+                for (int v = tid; v < sl.nv; v += kThreads) {
+                    const uint4 wt = load_t(v);
+                    if (filt && ge_lanes<D>(wt, zthr) == 0) continue;
+                    float zt[VEC], zd[VEC];
+                    decode_vec<D>(wt, zt);
+                    decode_vec<D>(load_d(v), zd);
+                    const int e0 = sl.ebase + v * VEC;
+#pragma unroll
+                    for (int i = 0; i < VEC; ++i) {
+                        const int e = e0 + i;
+                        if (e < lo || e >= hi) continue;
+                        const uint64_t key = make_key(resid1(zt[i], zd[i], e), e);
+                        if (key >= theta) {
+                            const int idx = atomicAdd(&s_int[2], 1);
+                            if (idx < kCandCap) cand[idx] = key;
+                        }
+                    }
+                }
+            } else {
+                const float tval = value_of_ordered(theta_u);
+                const bool filt = theta_u >= 0x00800000u;  // a real value (not "none")
+                for (int v = tid; v < sl.nv; v += kThreads) {
+                    const uint4 wt = ld_vec(buf_t, 16 * v);
+                    if (filt && ge_lanes<D>(wt, tval) == 0) continue;
+                    float zt[VEC];
+                    decode_vec<D>(wt, zt);
+                    const int e0 = sl.ebase + v * VEC;
+#pragma unroll
+                    for (int i = 0; i < VEC; ++i) {
+                        const int e = e0 + i;
+                        if (e < lo || e >= hi) continue;
+                        const uint64_t key = (excl && e == xt) ? excluded_key(e) : make_key(zt[i], e);
+                        if (key >= theta) {
+                            const int idx = atomicAdd(&s_int[2], 1);
+                            if (idx < kCandCap) cand[idx] = key;
+                        }
                     }
                 }
             }
-        };
-        for (int v = tid; v < sl.nv; v += kThreads) {
-            const int e0 = sl.ebase + v * VEC;
-            if (e0 >= lo && e0 + VEC <= hi)
-                body(std::true_type{}, v);
-            else
-                body(std::false_type{}, v);
+            __syncthreads();
+            count = s_int[2];
+            if (count <= kCandCap) break;
+            // overflow: every stored key is >= theta; the F-th largest of them is a
+            // strictly higher bound, and the qualifying set shrinks every round
+            block_sort_desc(cand, kCandCap);
+            theta = cand[Fk - 1];
+            theta_u = static_cast<uint32_t>(theta >> 32);
+            __syncthreads();
+            if (tid == 0) s_int[2] = 0;
+            __syncthreads();
         }
-        zsum = acc[0] + acc[1];
-        if (bs >= 0.f) tbest = make_key(bs, bid);
-    }
-    if (want_resid) zsum = block_sum(zsum, red_f);
-
-    // ---- pass 2b: block top-F_k of the cache scores --------------------------
-    int nlist = 0;
-    if (active && Fk > 0) {
-        if (pair) {
-            nlist = block_topf(
-                Fk, tbest,
-                [&](uint64_t theta, auto emit) {
-                    const float ts = key_value(theta);
-                    // w_t <= p_t: skip tokens whose p is below the threshold score
-                    const float xmin =
-                        (theta >> 32) > 0x80000000ull && ts > 0.f ? lg2(ts) + lg2(gT.S) - 1e-3f
-                                                                  : -INFINITY;
-                    for (int v = tid; v < sl.nv; v += kThreads) {
-                        const int e0 = sl.ebase + v * VEC;
-                        float zt[VEC];
-                        load_vec<D>(buf_t, v, zt);
-                        bool any = false;
-#pragma unroll
-                        for (int i = 0; i < VEC; ++i) any |= (zt[i] * c - gT.m) >= xmin;
-                        if (!any) continue;
-                        float zd[VEC];
-                        load_d(v, zd);
-#pragma unroll
-                        for (int i = 0; i < VEC; ++i) {
-                            const int e = e0 + i;
-                            if (e >= lo && e < hi && (zt[i] * c - gT.m) >= xmin) {
-                                const uint64_t key = make_key(resid(zt[i], zd[i], e), e);
-                                if (key >= theta) emit(key);
-                            }
-                        }
-                    }
-                },
-                cand, &s_cnt);
-        } else {
-            // raw target logits: greedy rows (drafted token last) and row K (p_K ranks as z)
-            const uint64_t tb = my_best;
-            nlist = block_topf(
-                Fk, tb,
-                [&](uint64_t theta, auto emit) {
-                    const uint32_t tv = static_cast<uint32_t>(theta >> 32);
-                    for (int v = tid; v < sl.nv; v += kThreads) {
-                        const int e0 = sl.ebase + v * VEC;
-                        float zt[VEC];
-                        load_vec<D>(buf_t, v, zt);
-#pragma unroll
-                        for (int i = 0; i < VEC; ++i) {
-                            const int e = e0 + i;
-                            if (e >= lo && e < hi) {
-                                const uint64_t key =
-                                    (excl && e == xt) ? excluded_key(e) : make_key(zt[i], e);
-                                if ((key >> 32) >= tv && key >= theta) emit(key);
-                            }
-                        }
-                    }
-                },
-                cand, &s_cnt);
-        }
+        if (count > kCandCap) count = kCandCap;
+        list_at = sort_candidates(cand, count);
+        nlist = count < Fk ? count : Fk;
     }
 
     // ---- exchange 2 -----------------------------------------------------------
     if (tid == 0) {
         xc.zsum = zsum;
         xc.nlist = nlist;
+        xc.list_at = list_at;
     }
     cluster.sync();
-
-    // Cache placement: each CTA ranks its own list entries against every peer list.
-    if (active && Fk > 0) {
-        int32_t *seg = P.cache_tok + static_cast<int64_t>(b) * P.budget + P.off[k];
-        for (int i = tid; i < nlist; i += kThreads) {
-            const uint64_t key = cand[i];
-            int pos = i;  // entries of my own list above this one
-            for (int j = 0; j < CL; ++j) {
-                if (j == rank) continue;
-                const Xchg *px = cluster.map_shared_rank(&xc, j);
-                const uint64_t *pl = cluster.map_shared_rank(cand, j);
-                int l = 0, h = px->nlist;  // count entries > key (lists are descending)
-                while (l < h) {
-                    const int mid = (l + h) >> 1;
-                    if (pl[mid] > key)
-                        l = mid + 1;
-                    else
-                        h = mid;
-                }
-                pos += l;
-            }
-            if (pos < Fk) seg[pos] = key_id(key);
+    if (warp == 0) {
+        float zj = 0.f;
+        int nl = 0, la = 0;
+        if (lane < CL) {
+            const Xchg *px = cluster.map_shared_rank(&xc, lane);
+            zj = px->zsum;
+            nl = px->nlist;
+            la = px->list_at;
         }
-    }
-
-    // Bonus candidate t_k: inverse CDF at u_K over ascending token id.
-    if (active && sampled && do_verify) {
-        // weights: residual (pair with positive mass) or p itself (row K, or Z == 0)
-        if (tid == 0) {
-            double tot_res = 0.0;
-            for (int j = 0; j < CL; ++j) {
-                const Xchg *px = cluster.map_shared_rank(&xc, j);
-                dscan[j] = static_cast<double>(px->zsum);
-                tot_res += dscan[j];
-            }
-            const int use_res = (pair && tot_res > 0.0) ? 1 : 0;
+        if (active && sampled && do_verify) {
+            // crossing of u_K * total over the slices, accumulated in rank order in fp64
+            double tr = 0.0;
+            for (int j = 0; j < CL; ++j) tr += static_cast<double>(__shfl_sync(kFull, zj, j));
+            const bool use_res = pair && tr > 0.0;
+            const double part = (lane < CL) ? (use_res ? static_cast<double>(zj) : pm[lane]) : 0.0;
             double tot = 0.0;
-            for (int j = 0; j < CL; ++j) {
-                if (!use_res) dscan[j] = pm[j];
-                tot += dscan[j];
-            }
+            for (int j = 0; j < CL; ++j) tot += __shfl_sync(kFull, part, j);
             const double T = static_cast<double>(P.uniforms[static_cast<int64_t>(b) * (K + 1) + K]) * tot;
-            int cstar = -1, lastpos = -1;
             double below = 0.0, cut = 0.0;
+            int cstar = -1, lastpos = -1;
             for (int j = 0; j < CL; ++j) {
-                if (dscan[j] > 0.0) lastpos = j;
-                if (cstar < 0 && below + dscan[j] > T) {
+                const double pj = __shfl_sync(kFull, part, j);
+                if (pj > 0.0) lastpos = j;
+                if (cstar < 0 && below + pj > T) {
                     cstar = j;
                     cut = T - below;
                 }
-                below += dscan[j];
+                below += pj;
             }
             if (cstar < 0) {  // T reached the total only through rounding
                 cstar = lastpos;
-                cut = (lastpos >= 0) ? dscan[lastpos] : 0.0;
+                cut = lastpos >= 0 ? __shfl_sync(kFull, part, lastpos < 0 ? 0 : lastpos) : 0.0;
             }
-            s_int[0] = cstar;
-            s_int[1] = use_res;
-            s_cut = cut;
+            if (lane == 0) {
+                s_int[3] = cstar;
+                s_int[4] = use_res ? 1 : 0;
+                s_cut = cut;
+            }
         }
-        __syncthreads();
-        const int cstar = s_int[0];
-        const bool use_res = s_int[1] != 0;
-        if (rank == cstar) {
-            const double cut = s_cut;
-            auto weight = [&](float zt, float zd, int e) -> float {
-                return use_res ? resid(zt, zd, e) : ex2(zt * c - gT.m);
-            };
-            // contiguous vector runs per thread so that a prefix over threads is a prefix over ids
-            const int G = (sl.nv + kThreads - 1) / kThreads;
-            const int v0 = min(sl.nv, tid * G), v1 = min(sl.nv, v0 + G);
-            float run = 0.f;
-            int lastp = -1;
-            for (int v = v0; v < v1; ++v) {
-                const int e0 = sl.ebase + v * VEC;
-                float zt[VEC], zd[VEC];
-                load_vec<D>(buf_t, v, zt);
-                if (use_res) load_d(v, zd);
+        if (rank == 0 && active && Fk > 0) {
+            // exclusive prefix of list sizes over ranks
+            int incl = nl;
 #pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(kFull, incl, o);
+                if (lane >= o) incl += y;
+            }
+            if (lane < CL) {
+                s_base[lane] = incl - nl;
+                s_at[lane] = la;
+            }
+            if (lane == 31) s_int[6] = incl;  // total entries
+        }
+    }
+    __syncthreads();
+    // rank 0 gathers every peer list into local memory, then ranks by counting
+    if (rank == 0 && active && Fk > 0) {
+        const int total = s_int[6];
+        int32_t *seg = P.cache_tok + static_cast<int64_t>(b) * P.budget + P.off[k];
+        if (total <= kCandCap) {
+            for (int i = tid; i < total; i += kThreads) {
+                int j = 0;
+                while (j + 1 < CL && s_base[j + 1] <= i) ++j;
+                const uint64_t *pl = cluster.map_shared_rank(cand, j);
+                mergebuf[i] = pl[s_at[j] + (i - s_base[j])];
+            }
+            __syncthreads();
+            for (int i = tid; i < total; i += kThreads) {
+                const uint64_t key = mergebuf[i];
+                int r = 0;
+                for (int j = 0; j < total; ++j) r += mergebuf[j] > key ? 1 : 0;
+                if (r < Fk) seg[r] = key_id(key);
+            }
+        } else {
+            // long lists: rank each entry by binary search in every peer list
+            for (int j0 = 0; j0 < CL; ++j0) {
+                const Xchg *p0 = cluster.map_shared_rank(&xc, j0);
+                const uint64_t *l0 = cluster.map_shared_rank(cand, j0) + p0->list_at;
+                const int n0 = p0->nlist;
+                for (int i = tid; i < n0; i += kThreads) {
+                    const uint64_t key = l0[i];
+                    int r = i;
+                    for (int j = 0; j < CL; ++j) {
+                        if (j == j0) continue;
+                        const Xchg *pj = cluster.map_shared_rank(&xc, j);
+                        const uint64_t *lj = cluster.map_shared_rank(cand, j) + pj->list_at;
+                        int l = 0, h = pj->nlist;
+                        while (l < h) {
+                            const int mid = (l + h) >> 1;
+                            if (lj[mid] > key)
+                                l = mid + 1;
+                            else
+                                h = mid;
+                        }
+                        r += l;
+                    }
+                    if (r < Fk) seg[r] = key_id(key);
+                }
+            }
+        }
+    }
+    __syncthreads();
+    cluster_arrive();  // this CTA's reads of peer shared memory are complete
+
+    // ---- bonus candidate t_k: inverse CDF at u_K over ascending token id ----
+    if (active && sampled && do_verify && rank == s_int[3]) {
+        const bool use_res = s_int[4] != 0;
+        const double cut = s_cut;
+        auto weight = [&](float zt, float zd, int e) -> float {
+            return use_res ? resid1(zt, zd, e) : ex2(zt * c - gT.m);
+        };
+        // contiguous vector runs per thread: a prefix over threads is a prefix over ids
+        const int G = (sl.nv + kThreads - 1) / kThreads;
+        const int v0 = min(sl.nv, tid * G), v1 = min(sl.nv, v0 + G);
+        float run = 0.f;
+        int lastp = -1;
+        for (int v = v0; v < v1; ++v) {
+            float zt[VEC], zd[VEC];
+            decode_vec<D>(load_t(v), zt);
+            if (use_res) decode_vec<D>(load_d(v), zd);
+            const int e0 = sl.ebase + v * VEC;
+#pragma unroll
+            for (int i = 0; i < VEC; ++i) {
+                const int e = e0 + i;
+                if (e >= lo && e < hi) {
+                    const float w = weight(zt[i], use_res ? zd[i] : 0.f, e);
+                    run += w;
+                    if (w > 0.f) lastp = e;
+                }
+            }
+        }
+        // block exclusive prefix of the runs (fp64)
+        double incl = static_cast<double>(run);
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const double y = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += y;
+        }
+        int lp = lastp;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(kFull, lp, o));
+        if (lane == 31) w_d[warp] = incl;
+        if (lane == 0) w_i[warp] = lp;
+        if (tid == 0) s_int[5] = kThreads;
+        __syncthreads();
+        double wbase = 0.0;
+        for (int w = 0; w < warp; ++w) wbase += w_d[w];
+        int lastmax = -1;
+        for (int w = 0; w < kWarps; ++w) lastmax = max(lastmax, w_i[w]);
+        const double before = wbase + incl - static_cast<double>(run);
+        if (before + static_cast<double>(run) > cut) atomicMin(&s_int[5], tid);
+        __syncthreads();
+        const int jstar = s_int[5];
+        if (tid == jstar) {
+            double acc = before;
+            int pick = -1;
+            for (int v = v0; v < v1 && pick < 0; ++v) {
+                float zt[VEC], zd[VEC];
+                decode_vec<D>(load_t(v), zt);
+                if (use_res) decode_vec<D>(load_d(v), zd);
+                const int e0 = sl.ebase + v * VEC;
                 for (int i = 0; i < VEC; ++i) {
                     const int e = e0 + i;
                     if (e >= lo && e < hi) {
-                        const float w = weight(zt[i], use_res ? zd[i] : 0.f, e);
-                        run += w;
-                        if (w > 0.f) lastp = e;
-                    }
-                }
-            }
-            __syncthreads();  // dscan[] reuse
-            dscan[tid] = static_cast<double>(run);
-            if (tid == 0) s_int[2] = -1;
-            __syncthreads();
-            int lastmax = static_cast<int>(block_max_u64(static_cast<uint64_t>(lastp + 1), red_u)) - 1;
-            if (tid == 0) {
-                double acc = 0.0;
-                int jstar = -1;
-                for (int j = 0; j < kThreads; ++j) {
-                    if (acc + dscan[j] > cut) {
-                        jstar = j;
-                        break;
-                    }
-                    acc += dscan[j];
-                }
-                s_int[2] = jstar;
-                dscan[0] = acc;  // prefix before jstar
-            }
-            __syncthreads();
-            if (tid == s_int[2]) {
-                double acc = dscan[0];
-                int pick = -1;
-                for (int v = v0; v < v1 && pick < 0; ++v) {
-                    const int e0 = sl.ebase + v * VEC;
-                    float zt[VEC], zd[VEC];
-                    load_vec<D>(buf_t, v, zt);
-                    if (use_res) load_d(v, zd);
-                    for (int i = 0; i < VEC; ++i) {
-                        const int e = e0 + i;
-                        if (e >= lo && e < hi) {
-                            acc += static_cast<double>(weight(zt[i], use_res ? zd[i] : 0.f, e));
-                            if (acc > cut) {
-                                pick = e;
-                                break;
-                            }
+                        acc += static_cast<double>(weight(zt[i], use_res ? zd[i] : 0.f, e));
+                        if (acc > cut) {
+                            pick = e;
+                            break;
                         }
                     }
                 }
-                rec->tk = pick >= 0 ? pick : lastmax;
             }
-            if (s_int[2] < 0 && tid == 0) rec->tk = lastmax;
+            rec->tk = pick >= 0 ? pick : lastmax;
         }
+        if (jstar >= kThreads && tid == 0) rec->tk = lastmax;
     }
 
     // ---- completion ---------------------------------------------------------
-    cluster.sync();  // peers finished reading this CTA's shared memory
     __threadfence();
     __syncthreads();
     if (tid == 0) {
         const uint32_t done = atomicAdd(P.seq_count + b, 1u);
-        s_int[3] = (done == static_cast<uint32_t>((K + 1) * CL - 1)) ? 1 : 0;
+        s_int[7] = (done == static_cast<uint32_t>((K + 1) * CL - 1)) ? 1 : 0;
     }
     __syncthreads();
-    if (s_int[3] == 0 || tid != 0) return;
+    const bool last = s_int[7] != 0;
+    cluster_wait();  // peers finished reading this CTA's shared memory
+    if (!last || tid != 0) return;
     __threadfence();
 
     // ---- epilogue: last CTA of sequence b ------------------------------------

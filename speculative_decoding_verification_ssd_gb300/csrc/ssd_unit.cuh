@@ -55,6 +55,10 @@ struct UnitParams {
     uint32_t *seq_count;   // [B] finished CTAs of the sequence (reset by the epilogue)
     uint32_t *seq_reject;  // [B] bit k set when position k rejected (reset by the epilogue)
     int32_t *dev_status;
+    // persistent streaming kernel only
+    uint32_t *unit_counter;  // next unit to hand out (reset by the last CTA to exit)
+    uint32_t *exit_counter;  // CTAs that have exited
+    int perm_mul;            // unit u -> sequence ((u % B) * perm_mul) % B (coprime to B)
 };
 
 // Workspace layout (each region 256-byte aligned).
@@ -64,7 +68,7 @@ inline size_t ws_rec_bytes(int B, int K) {
 }
 inline size_t ws_count_bytes(int B) { return align256(static_cast<size_t>(B) * sizeof(uint32_t)); }
 inline size_t ws_total_bytes(int B, int K) {
-    return ws_rec_bytes(B, K) + 2 * ws_count_bytes(B);
+    return ws_rec_bytes(B, K) + 2 * ws_count_bytes(B) + 256;  // + scheduler counters
 }
 
 }  // namespace ssd
