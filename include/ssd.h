@@ -200,6 +200,33 @@ int ssd_round(const void *tgt, const void *drf, int dtype, int B, int K, int V, 
               int32_t *cache_tok, uint8_t *hit, int32_t *slot, void *workspace,
               size_t workspace_bytes, int32_t *dev_status, void *stream);
 
+/*
+ * ssd_round_noalloc -- ssd_round for callers that cannot allocate device
+ * memory (no counterpart on the pages: this is plumbing of this library).
+ * Some hosts own every device buffer and forbid allocation while they enqueue
+ * work -- for example a plugin inside an inference server, where cudaMalloc
+ * could block the device or fail under memory pressure while serving.  This
+ * entry point takes no workspace: it keeps the round's scratch in a
+ * file-scope device array of ssd_noalloc_max_scratch() bytes (1 MiB) that
+ * every GPU loading the library holds until the process exits, and it calls
+ * no allocating routine.
+ * Arguments and outputs are those of ssd_round without the workspace.
+ * Errors: SSD_ERR_UNSUPPORTED when ssd_workspace_size(B, K) exceeds the
+ * array; otherwise as ssd_round.
+ * The first call on a device looks up that device's address of the array
+ * (with the device current); make that first call before any stream capture.
+ * Each call clears the counters it needs on `stream` before the kernel.  All
+ * calls share the one array per device: calls that overlap on the GPU (two
+ * streams, or two host threads) race and must be serialised by the caller.
+ */
+size_t ssd_noalloc_max_scratch(void);
+int ssd_round_noalloc(const void *tgt, const void *drf, int dtype, int B, int K, int V,
+                      int drf_rows, const int32_t *tokens, const float *uniforms,
+                      const float *temperature, const ssd_reshape_desc *reshape,
+                      const int32_t *F_host, int budget, int32_t *accept_len, int32_t *bonus,
+                      float *p_tok, float *q_tok, int32_t *cache_tok, uint8_t *hit,
+                      int32_t *slot, int32_t *dev_status, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

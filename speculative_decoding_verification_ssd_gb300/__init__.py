@@ -40,7 +40,8 @@ LIB_PATH = _build.LIB
 
 # Symbols declared in include/ssd.h.
 ABI_SYMBOLS = ("ssd_strerror", "ssd_version", "ssd_workspace_size", "ssd_verify", "ssd_fanout",
-               "ssd_reshape_draft", "ssd_build_cache", "ssd_cache_lookup", "ssd_round")
+               "ssd_reshape_draft", "ssd_build_cache", "ssd_cache_lookup", "ssd_round",
+               "ssd_noalloc_max_scratch", "ssd_round_noalloc")
 
 
 class SSDError(RuntimeError):
@@ -81,6 +82,11 @@ def lib() -> ctypes.CDLL:
         L.ssd_round.argtypes = [P, P, i, i, i, i, i, P, P, P, P, P, i, P, P, P, P, P, P, P, P, z,
                                 P, P]
         L.ssd_round.restype = i
+        L.ssd_noalloc_max_scratch.argtypes = []
+        L.ssd_noalloc_max_scratch.restype = z
+        L.ssd_round_noalloc.argtypes = [P, P, i, i, i, i, i, P, P, P, P, P, i, P, P, P, P, P, P, P, P,
+                                        P]
+        L.ssd_round_noalloc.restype = i
         _lib = L
     return _lib
 

@@ -331,3 +331,79 @@ int ssd_reshape_draft(const void *drf, int dtype, int rows, int V, const float *
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Workspace-free round.  Some callers cannot allocate device memory on their
+// own: an inference-server plugin whose host framework owns every device
+// buffer and forbids allocation while it enqueues work (cudaMalloc can block
+// the device and can fail under memory pressure mid-serving), or a runtime
+// that fixes its memory footprint at start-up.  For them ssd_round_noalloc
+// keeps the per-round scratch (unit records, per-sequence counters) in the
+// array below, which every GPU that loads the library holds until the
+// process exits.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(1) << 20;  // 1 MiB per device
+__device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+struct NoAllocSlot {
+    bool ready = false;
+    void *ptr = nullptr;
+};
+NoAllocSlot g_noalloc[kMaxDevices];
+std::mutex g_noalloc_mu;
+
+// Device address of this device's scratch array.  In host code the array's
+// name stands for a host-side shadow, not a device address, so the address is
+// looked up once per device, with that device current.
+int noalloc_scratch(void **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SSD_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    NoAllocSlot &slot = g_noalloc[dev];
+    if (!slot.ready) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) {
+            cudaGetLastError();
+            return SSD_ERR_CUDA;
+        }
+        slot.ptr = p;
+        slot.ready = true;
+    }
+    *out = slot.ptr;
+    return SSD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t ssd_noalloc_max_scratch(void) { return kNoAllocScratchBytes; }
+
+int ssd_round_noalloc(const void *tgt, const void *drf, int dtype, int B, int K, int V,
+                      int drf_rows, const int32_t *tokens, const float *uniforms,
+                      const float *temperature, const ssd_reshape_desc *reshape,
+                      const int32_t *F_host, int budget, int32_t *accept_len, int32_t *bonus,
+                      float *p_tok, float *q_tok, int32_t *cache_tok, uint8_t *hit,
+                      int32_t *slot, int32_t *dev_status, void *stream) {
+    if (B < 1 || K < 1 || K > SSD_MAX_K) return SSD_ERR_INVALID_ARG;
+    const size_t need = ssd::ws_total_bytes(B, K);
+    if (need > kNoAllocScratchBytes) return SSD_ERR_UNSUPPORTED;
+    void *scratch = nullptr;
+    const int st = noalloc_scratch(&scratch);
+    if (st != SSD_OK) return st;
+    // The array keeps the previous call's contents: the per-sequence counters
+    // and the scheduler counters must start at zero.
+    unsigned char *base = static_cast<unsigned char *>(scratch);
+    const size_t rec = ssd::ws_rec_bytes(B, K);
+    if (cudaMemsetAsync(base + rec, 0, need - rec, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return SSD_ERR_CUDA;
+    }
+    return ssd_round(tgt, drf, dtype, B, K, V, drf_rows, tokens, uniforms, temperature, reshape,
+                     F_host, budget, accept_len, bonus, p_tok, q_tok, cache_tok, hit, slot, scratch,
+                     need, dev_status, stream);
+}
+
+}  // extern "C"
