@@ -1,31 +1,30 @@
 // ssd_stream.cu -- persistent, warp-specialised streaming form of the fused
 // verify / cache-build / lookup kernel (sm_103a).
 //
-// One CTA per SM.  Warp 16 is the producer: it takes units (sequence b,
-// position k) from a global counter and streams their logit rows into an
-// 8-stage shared-memory ring with cp.async.bulk, each stage guarded by a
-// full/empty mbarrier pair.  Warps 0..15 consume the ring one unit at a time:
-//
-//  pass 1 (HBM)  per 32-token group: the raw maximum (packed, NaN-propagating)
-//                and, for sampled rows, the base-2 mass 2^(z c - gmax c) summed
-//                over the group (c = log2 e / tau); stored per group in shared
-//                memory.  Greedy rows keep only the group maxima (drafted token
-//                excluded).  The draft row of a pair folds into running stats.
-//  pass 2 (L2)   pair units only (sampled, k < K): the rows are streamed again
-//                (the unit was just read, so they hit L2) and each group stores
-//                its residual mass sum of max(0, p - q) and its largest residual.
-//  tail          from the per-group arrays: row normalisers, the accept test
-//                ([SD] step 3), the greedy argmax, the cache top-F_k (groups whose
-//                maximum reaches the F-th largest per-thread maximum are
-//                expanded into (value, id) keys), and the inverse-CDF bonus
-//                t_k at u_K (group prefix in fp64, then one warp re-reads the
-//                crossing group).  The last unit of a sequence runs the
-//                epilogue (scan -> a, bonus t_a, outputs, cache lookup).
-//
-// While the consumers work on a unit's tail, the producer is already streaming
-// the next unit, so the HBM stream does not stop for the per-unit reductions.
-// Used when every row starts on a 16-byte boundary; other layouts go to the
-// cluster kernel in ssd_unit.cu.
+// One CTA per SM, three roles:
+//   * a producer warp (one elected lane) takes units (sequence b, position k)
+//     from a global counter and streams their logit rows with cp.async.bulk
+//     into two 4-stage shared-memory rings, one per consumer group, each stage
+//     guarded by a full/empty mbarrier pair; it serves whichever ring has a
+//     free stage, so one group's per-unit tail never stalls the HBM stream;
+//   * two consumer groups of 8 warps each, every group working through its
+//     own units:
+//       pass 1 (HBM)  per 32-token group: the raw maximum and, for sampled
+//                     rows, the base-2 mass sum 2^(z c - gmax c) (c = log2 e / tau);
+//                     greedy rows keep only group maxima (drafted token
+//                     excluded); the draft row of a pair folds into running
+//                     statistics;
+//       pass 2 (L2)   pair units (sampled, k < K) stream both rows again (they
+//                     were just read, so they hit L2): per group the residual
+//                     mass sum max(0, p - q) and the largest residual;
+//       tail          normalisers, accept test ([SD] step 3), greedy argmax,
+//                     cache top-F_k (groups whose maximum reaches the F-th
+//                     largest per-thread maximum are expanded into (value, id)
+//                     keys), inverse-CDF bonus t_k at u_K; the last unit of a
+//                     sequence runs the epilogue (scan -> a, bonus t_a, outputs,
+//                     cache lookup).
+// A thread owns whole 32-token groups (bf16) or halves/quarters of them (fp32,
+// second pass), so group reductions need at most two shuffles.
 //
 // Operation sources: [SD] "Speculative decoding" (brentwoodlivery.com), "The
 // Algorithm (Step-by-Step)" and "Temperature and Sampling"; [WHY] "Why does
@@ -40,11 +39,14 @@
 namespace ssd {
 namespace {
 
-constexpr int kCW = kStreamConsumerWarps;  // consumer warps
-constexpr int kCT = kCW * 32;              // consumer threads
+constexpr int kGW = kStreamGroupWarps;  // warps per consumer group
+constexpr int kGT = kGW * 32;           // threads per consumer group
+constexpr int kNG = kStreamGroups;      // consumer groups
+constexpr int kRS = kStreamRingStages;  // stages per ring
+constexpr int kSB = kStreamStageBytes;  // bytes per stage
 constexpr unsigned kFull = 0xFFFFFFFFu;
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kCandGroupsCap = 2048;
+constexpr int kCandGroupsCap = 512;
 
 enum : int { kPassStats = 1, kPassResid = 2, kPassSkip = 3, kPassStop = 4 };
 
@@ -67,10 +69,13 @@ __device__ __forceinline__ float draft_bias(const DraftShape &r, float z, int e)
     return (r.on && (z > r.thr || (z == r.thr && e <= r.thr_id))) ? r.l2C : 0.f;
 }
 
-__device__ __forceinline__ void cbar() { asm volatile("bar.sync 1, %0;" ::"r"(kCT) : "memory"); }
-
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+// Residual max(0, p - q) of one token: p = 2^(z_p c - L_T), q = 2^(z_q c + b - L_D)
+// with nLT = -L_T and nLDb = b - L_D.  The stage code computes the same
+// operations two tokens at a time, so both give identical bits.
+__device__ __forceinline__ float resid_of(float zp, float zq, float c, float nLT, float nLDb) {
+    const float ep = ex2(fmaf(zp, c, nLT));
+    const float eq = ex2(fmaf(zq, c, nLDb));
+    return fmaxf(ep - eq, 0.f);
 }
 
 __device__ __forceinline__ uint64_t policy_evict_first() {
@@ -94,127 +99,181 @@ __device__ __forceinline__ uint4 neg_inf_vec() {
     return make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
 }
 
-// Reductions over the GV lanes that hold one 32-token group (GV divides 32).
-template <int GV>
-__device__ __forceinline__ float group_max_nan(float v) {
+// Loads the VPT vectors [vbase, vbase + VPT) of a staged row (vectors at or
+// past nvec read as -inf), rotated by `rot` so that neighbouring threads hit
+// different shared-memory banks.
+template <class D, int VPT>
+__device__ __forceinline__ void load_vecs(const unsigned char *row, int vbase, int nvec, int rot,
+                                          uint4 (&w)[VPT]) {
 #pragma unroll
-    for (int o = 1; o < GV; o <<= 1) v = fmax_nan(v, __shfl_xor_sync(kFull, v, o));
+    for (int k = 0; k < VPT; ++k) {
+        const int v = vbase + ((k + rot) & (VPT - 1));
+        w[k] = v < nvec ? *reinterpret_cast<const uint4 *>(row + 16 * v) : neg_inf_vec<D>();
+    }
+}
+
+template <class D, int VPT>
+__device__ __forceinline__ float vecs_max(const uint4 (&w)[VPT]) {
+    RawMax<D> rm;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) rm.add(w[k]);
+    return rm.get();
+}
+
+template <class D, int VPT>
+__device__ __forceinline__ float vecs_expsum(const uint4 (&w)[VPT], float c, float mc) {
+    float2 a = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) a = exp_sum<D>(w[k], c, mc, a);
+    return a.x + a.y;
+}
+
+template <int TPG>
+__device__ __forceinline__ float tpg_max_nan(float v) {
+#pragma unroll
+    for (int o = 1; o < TPG; o <<= 1) v = fmax_nan(v, __shfl_xor_sync(kFull, v, o));
     return v;
 }
-template <int GV>
-__device__ __forceinline__ float group_sum(float v) {
+template <int TPG>
+__device__ __forceinline__ float tpg_max(float v) {
 #pragma unroll
-    for (int o = 1; o < GV; o <<= 1) v += __shfl_xor_sync(kFull, v, o);
+    for (int o = 1; o < TPG; o <<= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
+    return v;
+}
+template <int TPG>
+__device__ __forceinline__ float tpg_sum(float v) {
+#pragma unroll
+    for (int o = 1; o < TPG; o <<= 1) v += __shfl_xor_sync(kFull, v, o);
     return v;
 }
 
-// ---- consumer-wide reductions (512 threads, named barrier 1) ----------------
+// ---- group-wide reductions (one consumer group, named barrier 1 + group) ----
 struct Scratch {
-    uint32_t u[kCW];
-    float f[kCW];
-    double d[kCW];
-    uint64_t k[kCW];
-    Stat st[kCW];
+    uint32_t u[kGW];
+    float f[kGW];
+    double d[kGW];
+    uint64_t k[kGW];
+    Stat st[kGW];
     int i[4];
     double cut;
-    uint64_t bkey;  // greedy argmax key (outside the reductions' slots)
+    uint64_t bkey;
     int bid;
 };
 
-__device__ uint32_t c_max_u32(uint32_t v, Scratch &s) {
+struct GroupCtx {
+    int bar_id;  // named barrier of the group
+    int t;       // thread index within the group
+    int lane, warp;
+};
+
+__device__ __forceinline__ void gbar(const GroupCtx &g) {
+    asm volatile("bar.sync %0, %1;" ::"r"(g.bar_id), "r"(kGT) : "memory");
+}
+
+__device__ uint32_t g_max_u32(const GroupCtx &g, uint32_t v, Scratch &s) {
     v = __reduce_max_sync(kFull, v);
-    cbar();
-    if ((threadIdx.x & 31) == 0) s.u[threadIdx.x >> 5] = v;
-    cbar();
+    gbar(g);
+    if (g.lane == 0) s.u[g.warp] = v;
+    gbar(g);
     uint32_t r = s.u[0];
-    for (int w = 1; w < kCW; ++w) r = s.u[w] > r ? s.u[w] : r;
+    for (int w = 1; w < kGW; ++w) r = s.u[w] > r ? s.u[w] : r;
     return r;
 }
 
-__device__ uint64_t c_max_u64(uint64_t v, Scratch &s) {
+__device__ uint64_t g_max_u64(const GroupCtx &g, uint64_t v, Scratch &s) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         const uint64_t x = __shfl_xor_sync(kFull, v, o);
         v = x > v ? x : v;
     }
-    cbar();
-    if ((threadIdx.x & 31) == 0) s.k[threadIdx.x >> 5] = v;
-    cbar();
+    gbar(g);
+    if (g.lane == 0) s.k[g.warp] = v;
+    gbar(g);
     uint64_t r = s.k[0];
-    for (int w = 1; w < kCW; ++w) r = s.k[w] > r ? s.k[w] : r;
+    for (int w = 1; w < kGW; ++w) r = s.k[w] > r ? s.k[w] : r;
     return r;
 }
 
-__device__ float c_sum_f32(float v, Scratch &s) {
+__device__ float g_sum_f32(const GroupCtx &g, float v, Scratch &s) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
-    cbar();
-    if ((threadIdx.x & 31) == 0) s.f[threadIdx.x >> 5] = v;
-    cbar();
+    gbar(g);
+    if (g.lane == 0) s.f[g.warp] = v;
+    gbar(g);
     float r = s.f[0];
-    for (int w = 1; w < kCW; ++w) r += s.f[w];
+    for (int w = 1; w < kGW; ++w) r += s.f[w];
     return r;
 }
 
-__device__ Stat c_stat(Stat st, Scratch &s) {
+__device__ Stat g_stat(const GroupCtx &g, Stat st, Scratch &s) {
     const uint32_t mo = __reduce_max_sync(kFull, ordered_bits(st.m));
     const float M = value_of_ordered(mo);
     float S = (st.m == -INFINITY) ? 0.f : st.S * ex2(st.m - M);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(kFull, S, o);
-    cbar();
-    if ((threadIdx.x & 31) == 0) s.st[threadIdx.x >> 5] = {M, M == -INFINITY ? 0.f : S};
-    cbar();
+    gbar(g);
+    if (g.lane == 0) s.st[g.warp] = {M, M == -INFINITY ? 0.f : S};
+    gbar(g);
     Stat r = s.st[0];
-    for (int w = 1; w < kCW; ++w) r = stat_merge(r, s.st[w]);
+    for (int w = 1; w < kGW; ++w) r = stat_merge(r, s.st[w]);
     return r;
 }
 
-// F-th largest (with multiplicity) of the per-thread values v over all
-// consumer threads (ordered bits; 0 = none).  tops: kCW * 32 words.
-__device__ uint32_t c_fth_largest(uint32_t v, int F, uint32_t *tops, Scratch &s) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+// F-th largest (with multiplicity) of the per-thread values v of the group
+// (ordered bits; 0 = none).  tops: kGW * 32 words.
+__device__ uint32_t g_fth_largest(const GroupCtx &g, uint32_t v, int F, uint32_t *tops, Scratch &s) {
     const int Fw = F < 32 ? F : 32;
-    cbar();
+    gbar(g);
     for (int it = 0; it < Fw; ++it) {
         const uint32_t mx = __reduce_max_sync(kFull, v);
         const uint32_t who = __ballot_sync(kFull, v == mx);
-        if (lane == __ffs(who) - 1) v = 0;
-        if (lane == 0) tops[warp * 32 + it] = mx;
+        if (g.lane == __ffs(who) - 1) v = 0;
+        if (g.lane == 0) tops[g.warp * 32 + it] = mx;
     }
-    cbar();
-    if (warp == 0) {
-        uint32_t vals[kCW];
-        const int nq = kCW * Fw;
+    gbar(g);
+    if (g.warp == 0) {
+        uint32_t vals[kGW];
+        const int nq = kGW * Fw;
 #pragma unroll
-        for (int i = 0; i < kCW; ++i) {
-            const int q = lane + 32 * i;
+        for (int i = 0; i < kGW; ++i) {
+            const int q = g.lane + 32 * i;
             vals[i] = q < nq ? tops[(q / Fw) * 32 + (q % Fw)] : 0u;
         }
         uint32_t mx = 0;
         for (int it = 0; it < F; ++it) {
             uint32_t lm = vals[0];
 #pragma unroll
-            for (int i = 1; i < kCW; ++i) lm = vals[i] > lm ? vals[i] : lm;
+            for (int i = 1; i < kGW; ++i) lm = vals[i] > lm ? vals[i] : lm;
             mx = __reduce_max_sync(kFull, lm);
             const uint32_t who = __ballot_sync(kFull, lm == mx);
-            if (lane == __ffs(who) - 1) {
+            if (g.lane == __ffs(who) - 1) {
                 bool done = false;
 #pragma unroll
-                for (int i = 0; i < kCW; ++i)
+                for (int i = 0; i < kGW; ++i)
                     if (!done && vals[i] == mx) {
                         vals[i] = 0;
                         done = true;
                     }
             }
         }
-        if (lane == 0) s.u[0] = mx;
+        if (g.lane == 0) s.u[0] = mx;
     }
-    cbar();
+    gbar(g);
     const uint32_t r = s.u[0];
-    cbar();
+    gbar(g);
     return r;
 }
+
+// Per consumer group shared state.
+struct GroupShared {
+    uint64_t full_bar[kRS];
+    uint64_t empty_bar[kRS];
+    Hdr hdr[kRS];
+    Scratch sc;
+    uint64_t cand[kCandCap];
+    int cgroups[kCandGroupsCap];
+    uint32_t tops[kGW * 32];
+};
 
 }  // namespace
 
@@ -222,107 +281,173 @@ template <class D>
 __global__ void __launch_bounds__(kStreamThreads, 1)
     ssd_stream_kernel(const __grid_constant__ UnitParams P) {
     constexpr int VEC = D::kVec, S = D::kBytes;
-    constexpr int GV = kGroupTokens / VEC;                 // vectors per group
-    constexpr int kHalfBytes = kStreamStageBytes / 2;
-    constexpr int GPC_PAIR = kHalfBytes / S / kGroupTokens;          // groups per pair chunk
-    constexpr int GPC_ONE = kStreamStageBytes / S / kGroupTokens;    // groups per single chunk
+    constexpr int GV = kGroupTokens / VEC;        // vectors per 32-token group
+    constexpr int HALF = kSB / 2;                 // bytes per row in a pair stage
+    constexpr int GPR = HALF / 16 / GV;           // groups per row in a pair stage
+    constexpr int GPS = kSB / 16 / GV;            // groups in a single-row stage
+    constexpr int TPG1 = (kGT / 2) / GPR;         // pass 1 pair: threads per group (per row)
+    constexpr int TPGS = kGT / GPS;               // pass 1 single: threads per group
+    constexpr int TPG2 = kGT / GPR;               // pass 2: threads per group
+    constexpr int VPT1 = GV / TPG1, VPTS = GV / TPGS, VPT2 = GV / TPG2;
+    static_assert(VPT1 == 4 && VPTS == 4 && VPT2 == 2, "stage geometry");
+
     extern __shared__ __align__(128) unsigned char dyn_smem[];
-    __shared__ __align__(8) uint64_t full_bar[kStreamStages], empty_bar[kStreamStages];
-    __shared__ Hdr hdr[kStreamStages];
-    __shared__ __align__(16) uint64_t cand[kCandCap];
-    __shared__ int cgroups[kCandGroupsCap];
-    __shared__ uint32_t tops[kCW * 32];
-    __shared__ Scratch sc;
+    __shared__ GroupShared gsh[kNG];
     __shared__ int s_abort;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int B = P.B, K = P.K, V = P.V;
     const int G = (V + kGroupTokens - 1) / kGroupTokens;
-    unsigned char *ring = dyn_smem;
-    float *gmax = reinterpret_cast<float *>(dyn_smem + kStreamStages * kStreamStageBytes);
-    float *gsum = gmax + ((G + 31) & ~31);
+    const int Gp = (G + 31) & ~31;
     const bool do_verify = (P.mode & kModeVerify) != 0;
     const bool do_cache = (P.mode & kModeCache) != 0;
     const int nunits = B * (K + 1);
     const int64_t row_bytes = static_cast<int64_t>(V) * S;
 
     if (tid == 0) {
-        for (int i = 0; i < kStreamStages; ++i) {
-            mbar_init(&full_bar[i], 1);
-            mbar_init(&empty_bar[i], kCW);
-        }
+        for (int g = 0; g < kNG; ++g)
+            for (int i = 0; i < kRS; ++i) {
+                mbar_init(&gsh[g].full_bar[i], 1);
+                mbar_init(&gsh[g].empty_bar[i], kGW);
+            }
         s_abort = 0;
         fence_mbar_init();
     }
     __syncthreads();
 
     // =========================== producer ===================================
-    if (warp == kCW) {
+    if (warp == kNG * kGW) {
         if (lane != 0) return;
         const uint64_t pol = policy_evict_first();
-        int64_t n = 0;  // stages produced
-        auto push = [&](const Hdr &h, const unsigned char *src_t, const unsigned char *src_d,
-                        uint32_t bytes, bool evict_first) -> bool {
-            const int s = static_cast<int>(n % kStreamStages);
-            const uint32_t par = static_cast<uint32_t>(((n / kStreamStages) & 1) ^ 1);
-            if (!mbar_wait_bounded(&empty_bar[s], par)) return false;
-            hdr[s] = h;
-            unsigned char *dst = ring + s * kStreamStageBytes;
-            const uint32_t tx = bytes * (src_d ? 2u : 1u);
-            mbar_arrive_expect_tx(&full_bar[s], tx);
-            if (bytes) {
-                if (evict_first) {
-                    bulk_copy_hint(dst, src_t, bytes, &full_bar[s], pol);
-                    if (src_d) bulk_copy_hint(dst + kHalfBytes, src_d, bytes, &full_bar[s], pol);
-                } else {
-                    bulk_copy_g2s(dst, src_t, bytes, &full_bar[s]);
-                    if (src_d) bulk_copy_g2s(dst + kHalfBytes, src_d, bytes, &full_bar[s]);
-                }
-            }
-            ++n;
-            return true;
+        struct Ring {
+            int64_t n;   // stages pushed
+            int unit;    // unit being streamed (-1: start the claimed one)
+            int pass, chunk, nch;
+            bool pair, p2, skip, stopped;
+            const unsigned char *trow, *drow;
+            // the next unit, claimed ahead: pf 0 = not claimed, 1 = claimed,
+            // 2 = its temperature and reject bits are loaded
+            int pf;
+            int next_u;
+            float next_tau;
+            uint32_t next_rej;
         };
-        bool ok = true;
-        while (ok) {
-            if (atomicAdd(&s_abort, 0)) break;
-            const int u = static_cast<int>(atomicAdd(P.unit_counter, 1u));
-            if (u >= nunits) break;
-            const int k = u / B;
-            const int b = static_cast<int>((static_cast<int64_t>(u - k * B) * P.perm_mul) % B);
-            const float tau = P.temperature[b];
-            const bool sampled = (tau > 0.f) && (tau < INFINITY);
-            const bool pair = sampled && k < K;
-            const bool p2 = pair && (do_verify || (do_cache && P.F[k] > 0));
-            bool skip = false;
-            if ((P.mode & kModeEarlyExit) && k > 0) {
-                const uint32_t mask = (k >= 32) ? 0xFFFFFFFFu : ((1u << k) - 1u);
-                skip = (__ldcg(P.seq_reject + b) & mask) != 0;
-            }
-            const unsigned char *trow = static_cast<const unsigned char *>(P.tgt) +
-                                        (static_cast<int64_t>(b) * P.tgt_seq_stride +
-                                         static_cast<int64_t>(k) * V) * S;
-            const unsigned char *drow =
-                pair ? static_cast<const unsigned char *>(P.drf) +
-                           (static_cast<int64_t>(b) * P.drf_seq_stride + static_cast<int64_t>(k) * V) * S
-                     : nullptr;
-            if (skip) {
-                ok = push(Hdr{u, kPassSkip, 0, 0, 1}, nullptr, nullptr, 0, false);
-                continue;
-            }
-            const int cb = pair ? kHalfBytes : kStreamStageBytes;
-            const int nch = static_cast<int>((row_bytes + cb - 1) / cb);
-            for (int pass = kPassStats; pass <= (p2 ? kPassResid : kPassStats) && ok; ++pass) {
-                for (int c = 0; c < nch && ok; ++c) {
-                    const int64_t off = static_cast<int64_t>(c) * cb;
-                    const uint32_t bytes = static_cast<uint32_t>(row_bytes - off < cb ? row_bytes - off : cb);
-                    const bool ef = !pair || pass == kPassResid;  // data not read again
-                    ok = push(Hdr{u, pass, c, static_cast<int>(bytes / 16), c == nch - 1},
-                              trow + off, pair ? drow + off : nullptr, bytes, ef);
+        Ring r[kNG];
+        // One prefetch step: claim a unit, or load the claimed unit's metadata.
+        // Steps are taken right after a stage is issued, so their latency
+        // overlaps the copies in flight.
+        auto prefetch_step = [&](Ring &q) {
+            if (q.pf == 0) {
+                q.next_u = static_cast<int>(atomicAdd(P.unit_counter, 1u));
+                q.pf = 1;
+            } else if (q.pf == 1) {
+                const int u = q.next_u;
+                if (u < nunits) {
+                    const int k = u / B;
+                    const int b = static_cast<int>((static_cast<int64_t>(u - k * B) * P.perm_mul) % B);
+                    q.next_tau = P.temperature[b];
+                    q.next_rej = (P.mode & kModeEarlyExit) ? __ldcg(P.seq_reject + b) : 0u;
                 }
+                q.pf = 2;
+            }
+        };
+#pragma unroll
+        for (int g = 0; g < kNG; ++g) {
+            r[g].n = 0;
+            r[g].unit = -1;
+            r[g].stopped = false;
+            r[g].pf = 0;
+            r[g].next_u = 0;
+            r[g].next_tau = 0.f;
+            r[g].next_rej = 0;
+            prefetch_step(r[g]);
+        }
+        int idle_rounds = 0;
+        bool ok = true;
+        for (;;) {
+            bool all_stopped = true, progress = false;
+#pragma unroll
+            for (int g = 0; g < kNG; ++g) {
+                Ring &q = r[g];
+                if (q.stopped) continue;
+                all_stopped = false;
+                const int s = static_cast<int>(q.n % kRS);
+                const uint32_t par = static_cast<uint32_t>(((q.n / kRS) & 1) ^ 1);
+                if (!mbar_test_wait(&gsh[g].empty_bar[s], par)) continue;
+                progress = true;
+                if (q.unit < 0) {
+                    while (q.pf < 2) prefetch_step(q);
+                    q.pf = 0;
+                    const int u = q.next_u;
+                    if (u >= nunits) {
+                        gsh[g].hdr[s] = Hdr{-1, kPassStop, 0, 0, 1};
+                        mbar_arrive_expect_tx(&gsh[g].full_bar[s], 0);
+                        ++q.n;
+                        q.stopped = true;
+                        continue;
+                    }
+                    const int k = u / B;
+                    const int b = static_cast<int>((static_cast<int64_t>(u - k * B) * P.perm_mul) % B);
+                    const bool sampled = (q.next_tau > 0.f) && (q.next_tau < INFINITY);
+                    q.unit = u;
+                    q.pair = sampled && k < K;
+                    q.p2 = q.pair && (do_verify || (do_cache && P.F[k] > 0));
+                    const uint32_t mask = (k >= 32) ? 0xFFFFFFFFu : ((1u << k) - 1u);
+                    q.skip = (P.mode & kModeEarlyExit) && k > 0 && (q.next_rej & mask) != 0;
+                    q.trow = static_cast<const unsigned char *>(P.tgt) +
+                             (static_cast<int64_t>(b) * P.tgt_seq_stride + static_cast<int64_t>(k) * V) * S;
+                    q.drow = q.pair ? static_cast<const unsigned char *>(P.drf) +
+                                          (static_cast<int64_t>(b) * P.drf_seq_stride +
+                                           static_cast<int64_t>(k) * V) * S
+                                    : nullptr;
+                    q.pass = kPassStats;
+                    q.chunk = 0;
+                    const int cb = q.pair ? HALF : kSB;
+                    q.nch = static_cast<int>((row_bytes + cb - 1) / cb);
+                }
+                if (q.skip) {
+                    gsh[g].hdr[s] = Hdr{q.unit, kPassSkip, 0, 0, 1};
+                    mbar_arrive_expect_tx(&gsh[g].full_bar[s], 0);
+                    ++q.n;
+                    q.unit = -1;
+                    prefetch_step(q);
+                    continue;
+                }
+                const int cb = q.pair ? HALF : kSB;
+                const int64_t off = static_cast<int64_t>(q.chunk) * cb;
+                const uint32_t bytes = static_cast<uint32_t>(row_bytes - off < cb ? row_bytes - off : cb);
+                gsh[g].hdr[s] = Hdr{q.unit, q.pass, q.chunk, static_cast<int>(bytes / 16), q.chunk == q.nch - 1};
+                unsigned char *dst = dyn_smem + (g * kRS + s) * kSB;
+                mbar_arrive_expect_tx(&gsh[g].full_bar[s], bytes * (q.pair ? 2u : 1u));
+                if (!q.pair || q.pass == kPassResid) {  // not read again
+                    bulk_copy_hint(dst, q.trow + off, bytes, &gsh[g].full_bar[s], pol);
+                    if (q.pair) bulk_copy_hint(dst + HALF, q.drow + off, bytes, &gsh[g].full_bar[s], pol);
+                } else {
+                    bulk_copy_g2s(dst, q.trow + off, bytes, &gsh[g].full_bar[s]);
+                    bulk_copy_g2s(dst + HALF, q.drow + off, bytes, &gsh[g].full_bar[s]);
+                }
+                ++q.n;
+                if (++q.chunk == q.nch) {
+                    q.chunk = 0;
+                    if (q.pass == kPassStats && q.p2)
+                        q.pass = kPassResid;
+                    else
+                        q.unit = -1;
+                }
+                prefetch_step(q);
+            }
+            if (all_stopped) break;
+            if (progress) {
+                idle_rounds = 0;
+            } else {
+                if (++idle_rounds > (1 << 24) || *reinterpret_cast<volatile int *>(&s_abort)) {
+                    ok = false;
+                    break;
+                }
+                __nanosleep(32);
             }
         }
-        if (ok) push(Hdr{-1, kPassStop, 0, 0, 1}, nullptr, nullptr, 0, false);
-        else {
+        if (!ok) {
             atomicOr(&s_abort, 1);
             if (P.dev_status) atomicOr(P.dev_status, SSD_DEV_TIMEOUT);
         }
@@ -330,172 +455,173 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     }
 
     // =========================== consumers ==================================
+    const int grp = warp / kGW;
+    GroupShared &gs = gsh[grp];
+    Scratch &sc = gs.sc;
+    GroupCtx gc{1 + grp, tid - grp * kGT, lane, warp - grp * kGW};
+    const int t = gc.t;
+    unsigned char *ring = dyn_smem + grp * kRS * kSB;
+    float *gmax = reinterpret_cast<float *>(dyn_smem + kNG * kRS * kSB) + grp * 2 * Gp;
+    float *gsum = gmax + Gp;
+
     int64_t n = 0;  // stages consumed
-    int cur = -1;   // current unit
-    // per-unit state (uniform over consumers)
+    int cur = -1;
     int b = 0, k = 0, xt = -1, flags = 0, Fk = 0, xmask = -1;
-    bool greedy = false, sampled = false, pair = false, rowK = false, active = false, excl = false;
+    bool greedy = false, sampled = false, pair = false, rowK = false, active = false;
     float c = 0.f;
     DraftShape shape{false, 0.f, 0, 0.f};
     const unsigned char *trow = nullptr, *drow = nullptr;
-    Stat st_d{-INFINITY, 0.f};   // running draft statistics (group-leader lanes)
+    Stat st_d{-INFINITY, 0.f};
     Stat gT{-INFINITY, 0.f}, gD{-INFINITY, 0.f};
     float LT = 0.f, LD = 0.f;
-    float ztx = 0.f, zdx = 0.f, u_k = 0.f;  // gathers (consumer thread 0)
+    float ztx = 0.f, zdx = 0.f, u_k = 0.f;
     UnitRecord rec{};
 
-    auto resid1 = [&](float zp, float zq, int e) -> float {
-        const float xp = zp * c - LT;
-        const float xq = zq * c + draft_bias(shape, zq, e) - LD;
-        return xp > xq ? fmaxf(ex2(xp) - ex2(xq), 0.f) : 0.f;
+    auto resid_e = [&](float zp, float zq, int e) -> float {
+        return resid_of(zp, zq, c, -LT, draft_bias(shape, zq, e) - LD);
     };
 
-    // ---- unit tail helpers ----------------------------------------------------
-    // row normaliser of the target from the group arrays (sampled rows)
-    auto target_stats = [&]() {
+    // normaliser of the target row from the group arrays
+    auto target_stats = [&]() -> Stat {
         uint32_t mo = 0;
-        for (int g = tid; g < G; g += kCT) {
+        for (int g = t; g < G; g += kGT) {
             const uint32_t o = ordered_bits(gmax[g]);
             mo = o > mo ? o : mo;
         }
-        const float M = value_of_ordered(c_max_u32(mo, sc));
+        const float M = value_of_ordered(g_max_u32(gc, mo, sc));
         const float Mc = M * c;
         float s = 0.f;
         if (M == M && M != -INFINITY) {
-            for (int g = tid; g < G; g += kCT) {
+            for (int g = t; g < G; g += kGT) {
                 const float gm = gmax[g];
                 if (gm != -INFINITY) s += gsum[g] * ex2(gm * c - Mc);
             }
         }
-        const float Ssum = c_sum_f32(s, sc);
-        return Stat{Mc, Ssum};
+        return Stat{Mc, g_sum_f32(gc, s, sc)};
     };
 
-    // top-F_k of the unit into its cache segment (gmax holds per-group maxima of
-    // the scores: residuals for pairs, raw logits otherwise)
+    // top-F_k of the unit into its cache segment (gmax: per-group maxima of the
+    // scores -- residuals for pairs, raw logits otherwise)
     auto top_f = [&]() {
         uint32_t tv = 0;
-        for (int g = tid; g < G; g += kCT) {
+        for (int g = t; g < G; g += kGT) {
             const uint32_t o = ordered_bits(gmax[g]);
             tv = o > tv ? o : tv;
         }
-        const uint32_t theta_u0 = c_fth_largest(tv, Fk, tops, sc);
+        const uint32_t theta_u0 = g_fth_largest(gc, tv, Fk, gs.tops, sc);
         uint64_t theta = static_cast<uint64_t>(theta_u0) << 32;
-        if (tid == 0) {
+        if (t == 0) {
             sc.i[0] = 0;
             sc.i[1] = 0;
         }
-        cbar();
-        for (int g = tid; g < G; g += kCT) {
+        gbar(gc);
+        for (int g = t; g < G; g += kGT) {
             if (ordered_bits(gmax[g]) >= theta_u0) {
                 const int idx = atomicAdd(&sc.i[0], 1);
-                if (idx < kCandGroupsCap) cgroups[idx] = g;
+                if (idx < kCandGroupsCap) gs.cgroups[idx] = g;
             }
         }
-        cbar();
+        gbar(gc);
         const int ncg = sc.i[0];
         const bool all_groups = ncg > kCandGroupsCap;
         const int ngroups = all_groups ? G : ncg;
         int count = 0;
         for (int round = 0; round < 64; ++round) {
-            for (int q = warp; q < ngroups; q += kCW) {
-                const int g = all_groups ? q : cgroups[q];
+            for (int q = gc.warp; q < ngroups; q += kGW) {
+                const int g = all_groups ? q : gs.cgroups[q];
                 const int e = g * kGroupTokens + lane;
-                uint64_t key = 0;
                 bool has = false;
+                uint64_t key = 0;
                 if (e < V) {
                     const float zt = load_logit<D>(trow, e);
-                    if (pair) {
-                        key = make_key(resid1(zt, load_logit<D>(drow, e), e), e);
-                    } else {
+                    if (pair)
+                        key = make_key(resid_e(zt, load_logit<D>(drow, e), e), e);
+                    else
                         key = (e == xmask) ? excluded_key(e) : make_key(zt, e);
-                    }
                     has = key >= theta;
                 }
                 if (has) {
                     const int idx = atomicAdd(&sc.i[1], 1);
-                    if (idx < kCandCap) cand[idx] = key;
+                    if (idx < kCandCap) gs.cand[idx] = key;
                 }
             }
-            cbar();
+            gbar(gc);
             count = sc.i[1];
             if (count <= kCandCap) break;
             // overflow: raise theta to the F-th largest of the stored keys
             for (int kk = 2; kk <= kCandCap; kk <<= 1) {
                 for (int j = kk >> 1; j > 0; j >>= 1) {
-                    for (int i = tid; i < kCandCap; i += kCT) {
+                    for (int i = t; i < kCandCap; i += kGT) {
                         const int ixj = i ^ j;
                         if (ixj > i) {
-                            const uint64_t a = cand[i], cc = cand[ixj];
+                            const uint64_t a = gs.cand[i], cc2 = gs.cand[ixj];
                             const bool desc = (i & kk) == 0;
-                            if (desc ? (a < cc) : (a > cc)) {
-                                cand[i] = cc;
-                                cand[ixj] = a;
+                            if (desc ? (a < cc2) : (a > cc2)) {
+                                gs.cand[i] = cc2;
+                                gs.cand[ixj] = a;
                             }
                         }
                     }
-                    cbar();
+                    gbar(gc);
                 }
             }
-            theta = cand[Fk - 1];
-            cbar();
-            if (tid == 0) sc.i[1] = 0;
-            cbar();
+            theta = gs.cand[Fk - 1];
+            gbar(gc);
+            if (t == 0) sc.i[1] = 0;
+            gbar(gc);
         }
         if (count > kCandCap) count = kCandCap;
-        // rank by counting into cand[kCandCap ..]
-        uint64_t key = 0;
-        int r = 0;
-        if (tid < count) {
-            key = cand[tid];
-            for (int j = 0; j < count; ++j) r += cand[j] > key ? 1 : 0;
+        // rank by counting; ranks below F go straight to the cache row
+        for (int i = t; i < count; i += kGT) {
+            const uint64_t key = gs.cand[i];
+            int rr = 0;
+            for (int j = 0; j < count; ++j) rr += gs.cand[j] > key ? 1 : 0;
+            if (rr < Fk) {
+                P.cache_tok[static_cast<int64_t>(b) * P.budget + P.off[k] + rr] = key_id(key);
+                __threadfence();
+            }
         }
-        if (tid < count && r < Fk) {
-            P.cache_tok[static_cast<int64_t>(b) * P.budget + P.off[k] + r] = key_id(key);
-        }
-        cbar();
+        gbar(gc);
     };
 
-    // inverse-CDF bonus at u_K over ascending token id; weights per group in gsum
-    // (residual masses, or p-masses when `pmode`), element weights by `wfn`
+    // inverse-CDF bonus at u_K over ascending token id; per-group weights from
+    // gsum (residual masses) or, when `pmode`, p-masses gsum * 2^(gmax c - Mc)
     auto crossing = [&](bool pmode, float Mc) {
-        // group weights
-        const int R = (G + kCT - 1) / kCT;
-        const int g0 = min(G, tid * R), g1 = min(G, g0 + R);
-        float run = 0.f;
-        for (int g = g0; g < g1; ++g) {
+        const int R = (G + kGT - 1) / kGT;
+        const int g0 = min(G, t * R), g1 = min(G, g0 + R);
+        auto gweight = [&](int g) -> float {
+            if (!pmode) return gsum[g];
             const float gm = gmax[g];
-            run += pmode ? ((gm == -INFINITY) ? 0.f : gsum[g] * ex2(gm * c - Mc)) : gsum[g];
-        }
-        // block exclusive prefix (fp64), warps in order
+            return (gm == -INFINITY) ? 0.f : gsum[g] * ex2(gm * c - Mc);
+        };
+        float run = 0.f;
+        for (int g = g0; g < g1; ++g) run += gweight(g);
         double incl = static_cast<double>(run);
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const double y = __shfl_up_sync(kFull, incl, o);
             if (lane >= o) incl += y;
         }
-        cbar();
-        if (lane == 31) sc.d[warp] = incl;
-        if (tid == 0) sc.i[2] = kCT;
-        cbar();
+        gbar(gc);
+        if (lane == 31) sc.d[gc.warp] = incl;
+        if (t == 0) sc.i[2] = kGT;
+        gbar(gc);
         double base = 0.0, tot = 0.0;
-        for (int w = 0; w < kCW; ++w) {
-            if (w < warp) base += sc.d[w];
+        for (int w = 0; w < kGW; ++w) {
+            if (w < gc.warp) base += sc.d[w];
             tot += sc.d[w];
         }
         const double T = static_cast<double>(P.uniforms[static_cast<int64_t>(b) * (K + 1) + K]) * tot;
         const double before = base + incl - static_cast<double>(run);
-        if (run > 0.f && before + static_cast<double>(run) > T) atomicMin(&sc.i[2], tid);
-        cbar();
+        if (run > 0.f && before + static_cast<double>(run) > T) atomicMin(&sc.i[2], t);
+        gbar(gc);
         const int tstar = sc.i[2];
-        // the crossing group (or, past the total by rounding, the last group with mass)
-        if (tid == tstar) {
+        if (t == tstar) {
             double acc = before;
             int gstar = g1 - 1;
             double cut = 0.0;
             for (int g = g0; g < g1; ++g) {
-                const float gm = gmax[g];
-                const float wg = pmode ? ((gm == -INFINITY) ? 0.f : gsum[g] * ex2(gm * c - Mc)) : gsum[g];
+                const float wg = gweight(g);
                 if (acc + static_cast<double>(wg) > T) {
                     gstar = g;
                     cut = T - acc;
@@ -506,31 +632,25 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             sc.i[3] = gstar;
             sc.cut = cut;
         }
-        if (tstar == kCT) {  // no crossing: the last group with positive weight
+        if (tstar == kGT) {  // past the total only through rounding: last group with mass
             uint32_t lastg = 0;
-            for (int g = tid; g < G; g += kCT) {
-                const float gm = gmax[g];
-                const float wg = pmode ? ((gm == -INFINITY) ? 0.f : gsum[g] * ex2(gm * c - Mc)) : gsum[g];
-                if (wg > 0.f) lastg = static_cast<uint32_t>(g + 1);
-            }
-            const uint32_t lg = c_max_u32(lastg, sc);
-            if (tid == 0) {
+            for (int g = t; g < G; g += kGT)
+                if (gweight(g) > 0.f) lastg = static_cast<uint32_t>(g + 1);
+            const uint32_t lg = g_max_u32(gc, lastg, sc);
+            if (t == 0) {
                 sc.i[3] = lg > 0 ? static_cast<int>(lg) - 1 : 0;
-                sc.cut = 1e300;  // past every element: pick the last positive one
+                sc.cut = 1e300;
             }
         }
-        cbar();
-        if (warp == 0) {
+        gbar(gc);
+        if (gc.warp == 0) {
             const int g = sc.i[3];
             const double cut = sc.cut;
             const int e = g * kGroupTokens + lane;
             float w = 0.f;
             if (e < V) {
                 const float zt = load_logit<D>(trow, e);
-                if (pmode)
-                    w = ex2(zt * c - Mc);
-                else
-                    w = resid1(zt, load_logit<D>(drow, e), e);
+                w = pmode ? ex2(fmaf(zt, c, -Mc)) : resid_e(zt, load_logit<D>(drow, e), e);
             }
             double cum = static_cast<double>(w);
 #pragma unroll
@@ -538,7 +658,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                 const double y = __shfl_up_sync(kFull, cum, o);
                 if (lane >= o) cum += y;
             }
-            const uint32_t over = __ballot_sync(kFull, cum > cut && w >= 0.f && e < V);
+            const uint32_t over = __ballot_sync(kFull, cum > cut && e < V);
             const uint32_t pos = __ballot_sync(kFull, w > 0.f && e < V);
             int pick;
             if (over)
@@ -547,16 +667,15 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                 pick = g * kGroupTokens + 31 - __clz(pos);
             else
                 pick = g * kGroupTokens;
-            if (lane == 0) rec.tk = pick;
+            if (lane == 0) sc.bid = pick;
         }
-        cbar();
+        gbar(gc);
+        if (t == 0) rec.tk = sc.bid;
     };
 
     auto finish_unit = [&]() {
-        // record, then count the unit; the sequence's last unit runs the epilogue
-        __threadfence();
-        cbar();
-        if (tid == 0) {
+        gbar(gc);
+        if (t == 0) {
             UnitRecord *R = P.rec + static_cast<int64_t>(b) * (K + 1) + k;
             R->p_tok = rec.p_tok;
             R->q_tok = rec.q_tok;
@@ -612,21 +731,21 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                 P.seq_reject[b] = 0;
             }
         }
-        cbar();
+        gbar(gc);
     };
 
     for (;;) {
-        const int s = static_cast<int>(n % kStreamStages);
-        const uint32_t par = static_cast<uint32_t>((n / kStreamStages) & 1);
-        if (!mbar_wait_bounded(&full_bar[s], par)) {
+        const int s = static_cast<int>(n % kRS);
+        const uint32_t par = static_cast<uint32_t>((n / kRS) & 1);
+        if (!mbar_wait_bounded(&gs.full_bar[s], par)) {
             atomicOr(&s_abort, 1);
-            if (tid == 0 && P.dev_status) atomicOr(P.dev_status, SSD_DEV_TIMEOUT);
+            if (t == 0 && P.dev_status) atomicOr(P.dev_status, SSD_DEV_TIMEOUT);
             break;
         }
-        const Hdr h = hdr[s];
+        const Hdr h = gs.hdr[s];
         if (h.pass == kPassStop) break;
         if (h.unit != cur) {
-            // ---- a new unit: per-unit constants (identical in every consumer) --
+            // a new unit: per-unit constants (identical in every thread of the group)
             cur = h.unit;
             k = cur / B;
             b = static_cast<int>((static_cast<int64_t>(cur - k * B) * P.perm_mul) % B);
@@ -642,8 +761,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                 xt = P.tokens[static_cast<int64_t>(b) * K + k];
                 if (xt < 0 || xt >= V) flags |= SSD_DEV_BAD_TOKEN;
             }
-            excl = greedy && !rowK;
-            xmask = excl ? xt : -1;
+            xmask = (greedy && !rowK) ? xt : -1;
             Fk = do_cache ? P.F[k] : 0;
             active = flags == 0;
             c = sampled ? kLog2e / tau : 0.f;
@@ -666,7 +784,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             rec.p_tok = NAN;
             rec.q_tok = NAN;
             rec.state = 1;
-            if (tid == 0 && active && !rowK) {
+            if (t == 0 && active && !rowK) {
                 ztx = load_logit<D>(trow, xt);
                 if (pair) {
                     zdx = load_logit<D>(drow, xt);
@@ -674,10 +792,10 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                 }
             }
         }
-        const unsigned char *st = ring + s * kStreamStageBytes;
+        const unsigned char *st = ring + s * kSB;
         if (h.pass == kPassSkip) {
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty_bar[s]);
+            if (lane == 0) mbar_arrive(&gs.empty_bar[s]);
             ++n;
             rec.state = 2;
             rec.flags = flags;
@@ -688,137 +806,153 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         // ---- stage processing -----------------------------------------------
         if (active) {
             if (h.pass == kPassStats && pair) {
-                const int j = tid;
-                const bool ok = j < h.nvec;
-                const uint4 wt = ok ? *reinterpret_cast<const uint4 *>(st + 16 * j) : neg_inf_vec<D>();
-                const uint4 wd = ok ? *reinterpret_cast<const uint4 *>(st + kHalfBytes + 16 * j)
-                                    : neg_inf_vec<D>();
-                const int g = h.chunk * GPC_PAIR + j / GV;
-                // target: group maximum and mass
-                RawMax<D> rm;
-                rm.add(wt);
-                const float gm = group_max_nan<GV>(rm.get());
-                float vs = 0.f;
-                if (gm != -INFINITY) {
-                    const float2 a = exp_sum<D>(wt, c, gm * c, make_float2(0.f, 0.f));
-                    vs = a.x + a.y;
-                }
-                const float gs = group_sum<GV>(vs);
-                const bool leader = (j % GV) == 0;
-                if (leader && g < G) {
-                    gmax[g] = gm;
-                    gsum[g] = gs;
-                }
-                // draft: fold the group into the running statistics
-                if (!shape.on) {
-                    RawMax<D> rd;
-                    rd.add(wd);
-                    const float gmd = group_max_nan<GV>(rd.get());
-                    float vd = 0.f;
-                    if (gmd != -INFINITY) {
-                        const float2 a = exp_sum<D>(wd, c, gmd * c, make_float2(0.f, 0.f));
-                        vd = a.x + a.y;
+                // threads [0, kGT/2) take target groups, the rest draft groups
+                const int row = t / (kGT / 2);
+                const int tr = t - row * (kGT / 2);
+                const int gl = tr / TPG1, part = tr % TPG1;
+                uint4 w[VPT1];
+                load_vecs<D, VPT1>(st + row * HALF, gl * GV + part * VPT1, h.nvec, (tr >> 1) & 3, w);
+                const int g = h.chunk * GPR + gl;
+                if (row == 0 || !shape.on) {
+                    const float gm = tpg_max_nan<TPG1>(vecs_max<D, VPT1>(w));
+                    float vs = 0.f;
+                    if (gm != -INFINITY) vs = vecs_expsum<D, VPT1>(w, c, gm * c);
+                    const float gsv = tpg_sum<TPG1>(vs);
+                    if (part == 0) {
+                        if (row == 0) {
+                            if (g < G) {
+                                gmax[g] = gm;
+                                gsum[g] = gsv;
+                            }
+                        } else if (gm != -INFINITY) {
+                            st_d = (gm == gm) ? stat_merge(st_d, Stat{gm * c, gsv}) : Stat{NAN, NAN};
+                        }
                     }
-                    const float gsd = group_sum<GV>(vd);
-                    if (leader && gmd != -INFINITY) st_d = stat_merge(st_d, Stat{gmd * c, gsd});
-                    if (leader && gmd != gmd) st_d = Stat{NAN, NAN};
                 } else {
-                    float z[VEC];
-                    decode_vec<D>(wd, z);
-                    const int e0 = (h.chunk * GPC_PAIR) * kGroupTokens + j * VEC;
-                    float x[VEC];
+                    // reshaped draft: weights 2^(z c + log2 c_t), maximum over weighted values
+                    const int e0 = h.chunk * GPR * kGroupTokens + (gl * GV + part * VPT1) * VEC;
+                    float x[VPT1][VEC];
                     float xm = -INFINITY;
 #pragma unroll
-                    for (int i = 0; i < VEC; ++i) {
-                        x[i] = z[i] * c + draft_bias(shape, z[i], e0 + i);
-                        xm = fmax_nan(xm, x[i]);
+                    for (int kk = 0; kk < VPT1; ++kk) {
+                        float z[VEC];
+                        decode_vec<D>(w[kk], z);
+                        const int ev = e0 + ((kk + ((tr >> 1) & 3)) & (VPT1 - 1)) * VEC;
+#pragma unroll
+                        for (int i = 0; i < VEC; ++i) {
+                            x[kk][i] = z[i] * c + draft_bias(shape, z[i], ev + i);
+                            xm = fmax_nan(xm, x[kk][i]);
+                        }
                     }
-                    const float gxm = group_max_nan<GV>(xm);
-                    float vd = 0.f;
+                    const float gxm = tpg_max_nan<TPG1>(xm);
+                    float vs = 0.f;
                     if (gxm != -INFINITY) {
 #pragma unroll
-                        for (int i = 0; i < VEC; ++i) vd += ex2(x[i] - gxm);
+                        for (int kk = 0; kk < VPT1; ++kk)
+#pragma unroll
+                            for (int i = 0; i < VEC; ++i) vs += ex2(x[kk][i] - gxm);
                     }
-                    const float gsd = group_sum<GV>(vd);
-                    if (leader && gxm != -INFINITY) st_d = stat_merge(st_d, Stat{gxm, gsd});
-                    if (leader && gxm != gxm) st_d = Stat{NAN, NAN};
+                    const float gsv = tpg_sum<TPG1>(vs);
+                    if (part == 0 && gxm != -INFINITY)
+                        st_d = (gxm == gxm) ? stat_merge(st_d, Stat{gxm, gsv}) : Stat{NAN, NAN};
                 }
             } else if (h.pass == kPassStats) {
                 // one row: sampled row K (max + mass) or greedy (max, drafted token excluded)
+                const int gl = t / TPGS, part = t % TPGS;
+                const int vbase = gl * GV + part * VPTS;
+                uint4 w[VPTS];
+                load_vecs<D, VPTS>(st, vbase, h.nvec, (t >> 1) & 3, w);
+                const int e0 = h.chunk * GPS * kGroupTokens + vbase * VEC;
+                if (static_cast<unsigned>(xmask - e0) < static_cast<unsigned>(VPTS * VEC)) {
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    const int j = tid + half * kCT;
-                    const bool ok = j < h.nvec;
-                    uint4 w = ok ? *reinterpret_cast<const uint4 *>(st + 16 * j) : neg_inf_vec<D>();
-                    const int e0 = h.chunk * GPC_ONE * kGroupTokens + j * VEC;
-                    if (static_cast<unsigned>(xmask - e0) < static_cast<unsigned>(VEC))
-                        mask_vec<D>(w, e0, 0, V, xmask);
-                    const int g = h.chunk * GPC_ONE + j / GV;
-                    RawMax<D> rm;
-                    rm.add(w);
-                    const float gm = group_max_nan<GV>(rm.get());
-                    float gs = 0.f;
-                    if (sampled) {
-                        float vs = 0.f;
-                        if (gm != -INFINITY) {
-                            const float2 a = exp_sum<D>(w, c, gm * c, make_float2(0.f, 0.f));
-                            vs = a.x + a.y;
-                        }
-                        gs = group_sum<GV>(vs);
+                    for (int kk = 0; kk < VPTS; ++kk) {
+                        const int ev = e0 + ((kk + ((t >> 1) & 3)) & (VPTS - 1)) * VEC;
+                        if (static_cast<unsigned>(xmask - ev) < static_cast<unsigned>(VEC))
+                            mask_vec<D>(w[kk], ev, 0, V, xmask);
                     }
-                    if ((j % GV) == 0 && g < G) {
-                        gmax[g] = gm;
-                        gsum[g] = gs;
-                    }
+                }
+                const float gm = tpg_max_nan<TPGS>(vecs_max<D, VPTS>(w));
+                float gsv = 0.f;
+                if (sampled) {
+                    float vs = 0.f;
+                    if (gm != -INFINITY) vs = vecs_expsum<D, VPTS>(w, c, gm * c);
+                    gsv = tpg_sum<TPGS>(vs);
+                }
+                const int g = h.chunk * GPS + gl;
+                if (part == 0 && g < G) {
+                    gmax[g] = gm;
+                    gsum[g] = gsv;
                 }
             } else {
                 // pass 2 (pair): residual masses and maxima per group
-                const int j = tid;
-                const bool ok = j < h.nvec;
-                const uint4 wt = ok ? *reinterpret_cast<const uint4 *>(st + 16 * j) : neg_inf_vec<D>();
-                const uint4 wd = ok ? *reinterpret_cast<const uint4 *>(st + kHalfBytes + 16 * j)
-                                    : neg_inf_vec<D>();
-                float zt[VEC], zd[VEC];
-                decode_vec<D>(wt, zt);
-                decode_vec<D>(wd, zd);
-                const int e0 = (h.chunk * GPC_PAIR) * kGroupTokens + j * VEC;
+                const int gl = t / TPG2, part = t % TPG2;
+                const int vbase = gl * GV + part * VPT2;
+                const int rot = (t >> 2) & 1;
+                uint4 wt[VPT2], wd[VPT2];
+                load_vecs<D, VPT2>(st, vbase, h.nvec, rot, wt);
+                load_vecs<D, VPT2>(st + HALF, vbase, h.nvec, rot, wd);
                 float2 acc = make_float2(0.f, 0.f);
                 float mx = 0.f;
+                if (!shape.on) {
+                    const float2 cc = make_float2(c, c), nl = make_float2(-LT, -LD);
 #pragma unroll
-                for (int i = 0; i < VEC; i += 2) {
-                    const float w0 = resid1(zt[i], zd[i], e0 + i);
-                    const float w1 = resid1(zt[i + 1], zd[i + 1], e0 + i + 1);
-                    acc = __fadd2_rn(acc, make_float2(w0, w1));
-                    mx = fmaxf(mx, fmaxf(w0, w1));
+                    for (int kk = 0; kk < VPT2; ++kk) {
+                        float zt[VEC], zd[VEC];
+                        decode_vec<D>(wt[kk], zt);
+                        decode_vec<D>(wd[kk], zd);
+#pragma unroll
+                        for (int i = 0; i < VEC; i += 2) {
+                            const float2 x0 = __ffma2_rn(make_float2(zt[i], zd[i]), cc, nl);
+                            const float2 x1 = __ffma2_rn(make_float2(zt[i + 1], zd[i + 1]), cc, nl);
+                            const float2 d = __ffma2_rn(make_float2(ex2(x0.y), ex2(x1.y)),
+                                                        make_float2(-1.f, -1.f),
+                                                        make_float2(ex2(x0.x), ex2(x1.x)));
+                            const float w0 = fmaxf(d.x, 0.f), w1 = fmaxf(d.y, 0.f);
+                            acc = __fadd2_rn(acc, make_float2(w0, w1));
+                            mx = fmaxf(mx, fmaxf(w0, w1));
+                        }
+                    }
+                } else {
+                    const int e0 = h.chunk * GPR * kGroupTokens + vbase * VEC;
+#pragma unroll
+                    for (int kk = 0; kk < VPT2; ++kk) {
+                        float zt[VEC], zd[VEC];
+                        decode_vec<D>(wt[kk], zt);
+                        decode_vec<D>(wd[kk], zd);
+                        const int ev = e0 + ((kk + rot) & (VPT2 - 1)) * VEC;
+#pragma unroll
+                        for (int i = 0; i < VEC; ++i) {
+                            const float wv = resid_e(zt[i], zd[i], ev + i);
+                            acc.x += wv;
+                            mx = fmaxf(mx, wv);
+                        }
+                    }
                 }
-                const float gs = group_sum<GV>(acc.x + acc.y);
-                float gm = mx;
-#pragma unroll
-                for (int o = 1; o < GV; o <<= 1) gm = fmaxf(gm, __shfl_xor_sync(kFull, gm, o));
-                const int g = h.chunk * GPC_PAIR + j / GV;
-                if ((j % GV) == 0 && g < G) {
+                const float gsv = tpg_sum<TPG2>(acc.x + acc.y);
+                const float gm = tpg_max<TPG2>(mx);
+                const int g = h.chunk * GPR + gl;
+                if (part == 0 && g < G) {
                     gmax[g] = gm;
-                    gsum[g] = gs;
+                    gsum[g] = gsv;
                 }
             }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty_bar[s]);
+        if (lane == 0) mbar_arrive(&gs.empty_bar[s]);
         ++n;
         if (!h.last) continue;
 
         // ---- end of a pass: the unit's tail ----------------------------------
-        cbar();  // group arrays complete
+        gbar(gc);  // group arrays complete
         rec.flags = flags;
         const bool want_p2 = pair && (do_verify || Fk > 0);
         if (!active) {
-            // an inactive pair still receives its second pass; finish after it
             if (h.pass == kPassResid || !want_p2) finish_unit();
             continue;
         }
         if (h.pass == kPassStats && sampled) {
             gT = target_stats();
-            if (pair) gD = c_stat(st_d, sc);
+            if (pair) gD = g_stat(gc, st_d, sc);
             const bool okT = (gT.m < INFINITY) && (gT.S > 0.f) && (gT.S < INFINITY);
             const bool okD = !pair || ((gD.m < INFINITY) && (gD.S > 0.f) && (gD.S < INFINITY));
             if (!okT || !okD) {
@@ -826,11 +960,11 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                 rec.flags = flags;
                 active = false;
                 if (!want_p2) finish_unit();
-                continue;  // a pair's second pass is still streamed and consumed
+                continue;
             }
             LT = gT.m + lg2(gT.S);
             LD = pair ? gD.m + lg2(gD.S) : 0.f;
-            if (pair && tid == 0) {
+            if (pair && t == 0) {
                 const float p = ex2(ztx * c - gT.m) / gT.S;
                 const float q = ex2(zdx * c + draft_bias(shape, zdx, xt) - gD.m) / gD.S;
                 rec.p_tok = p;
@@ -839,23 +973,21 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             }
             if (pair) {
                 if (!want_p2) finish_unit();
-                continue;  // pass 2 follows
+                continue;
             }
-            // sampled row K: cache from raw maxima, bonus from p_K
             if (Fk > 0) top_f();
             if (do_verify) crossing(true, gT.m);
             finish_unit();
             continue;
         }
         if (h.pass == kPassStats && greedy) {
-            // argmax: the best group (lowest index on ties), then the lowest id in it
             uint64_t gk = 0;
-            for (int g = tid; g < G; g += kCT) {
+            for (int g = t; g < G; g += kGT) {
                 const uint64_t key = (static_cast<uint64_t>(ordered_bits(gmax[g])) << 32) |
                                      static_cast<uint64_t>(0xFFFFFFFFu - static_cast<uint32_t>(g));
                 gk = key > gk ? key : gk;
             }
-            const uint64_t best = c_max_u64(gk, sc);
+            const uint64_t best = g_max_u64(gc, gk, sc);
             const float M = value_of_ordered(static_cast<uint32_t>(best >> 32));
             const int gbest = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(best & 0xFFFFFFFFu));
             if (M != M) {
@@ -864,7 +996,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                 finish_unit();
                 continue;
             }
-            if (warp == 0) {
+            if (gc.warp == 0) {
                 const int e = gbest * kGroupTokens + lane;
                 bool m = false;
                 if (e < V && e != xmask) m = load_logit<D>(trow, e) == M;
@@ -875,17 +1007,15 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                     sc.bid = id;
                 }
             }
-            cbar();
-            const uint64_t gkey = sc.bkey;
-            if (tid == 0) {
+            gbar(gc);
+            if (t == 0) {
                 rec.tk = sc.bid;
                 if (!rowK) {
-                    rec.accept = make_key(ztx, xt) > gkey ? 1 : 0;
+                    rec.accept = make_key(ztx, xt) > sc.bkey ? 1 : 0;
                     rec.p_tok = rec.accept ? 1.f : 0.f;
                     rec.q_tok = 1.f;
                 }
             }
-            cbar();
             if (Fk > 0) top_f();
             finish_unit();
             continue;
@@ -893,15 +1023,15 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         // end of pass 2 (pair): residual mass, cache, bonus
         {
             float zs = 0.f;
-            for (int g = tid; g < G; g += kCT) zs += gsum[g];
-            const float Z = c_sum_f32(zs, sc);
+            for (int g = t; g < G; g += kGT) zs += gsum[g];
+            const float Z = g_sum_f32(gc, zs, sc);
             if (Fk > 0) top_f();
             if (do_verify) {
                 if (Z > 0.f) {
                     crossing(false, 0.f);
                 } else {
                     // no residual mass: draw from p at this row (group p-masses again)
-                    for (int g = tid; g < G; g += kCT) {
+                    for (int g = t; g < G; g += kGT) {
                         float m = -INFINITY;
                         for (int i = 0; i < kGroupTokens; ++i) {
                             const int e = g * kGroupTokens + i;
@@ -910,12 +1040,12 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                         float s2 = 0.f;
                         for (int i = 0; i < kGroupTokens; ++i) {
                             const int e = g * kGroupTokens + i;
-                            if (e < V) s2 += ex2(load_logit<D>(trow, e) * c - m * c);
+                            if (e < V) s2 += ex2(fmaf(load_logit<D>(trow, e), c, -m * c));
                         }
                         gmax[g] = m;
                         gsum[g] = s2;
                     }
-                    cbar();
+                    gbar(gc);
                     crossing(true, gT.m);
                 }
             }
@@ -923,12 +1053,12 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         }
     }
 
-    // consumers done: the last CTA to finish resets the unit scheduler
-    cbar();
-    if (tid == 0) {
+    // this group is done; the last group of the grid resets the unit scheduler
+    gbar(gc);
+    if (t == 0) {
         __threadfence();
         const uint32_t done = atomicAdd(P.exit_counter, 1u);
-        if (done == gridDim.x - 1) {
+        if (done == gridDim.x * kNG - 1) {
             *P.unit_counter = 0;
             *P.exit_counter = 0;
         }

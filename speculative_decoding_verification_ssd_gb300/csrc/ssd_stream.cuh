@@ -6,18 +6,21 @@
 
 namespace ssd {
 
-constexpr int kStreamConsumerWarps = 16;
-constexpr int kStreamThreads = kStreamConsumerWarps * 32 + 32;  // + one producer warp
-constexpr int kStreamStages = 8;
+constexpr int kStreamGroups = 2;       // consumer groups, each with its own ring
+constexpr int kStreamGroupWarps = 8;   // warps per consumer group
+constexpr int kStreamThreads = kStreamGroups * kStreamGroupWarps * 32 + 32;  // + one producer warp
+constexpr int kStreamRingStages = 4;   // stages per ring
 constexpr int kStreamStageBytes = 16384;
 constexpr int kGroupTokens = 32;
 
 // Dynamic shared memory of the streaming kernel for a vocabulary of V tokens:
-// the stage ring plus two float arrays with one entry per 32-token group.
+// the stage rings plus, per consumer group, two float arrays with one entry per
+// 32-token group.
 inline size_t stream_dyn_bytes(int V) {
     const size_t G = (static_cast<size_t>(V) + kGroupTokens - 1) / kGroupTokens;
     const size_t Gp = (G + 31) & ~static_cast<size_t>(31);
-    return static_cast<size_t>(kStreamStages) * kStreamStageBytes + 2 * Gp * sizeof(float);
+    return static_cast<size_t>(kStreamGroups) *
+           (static_cast<size_t>(kStreamRingStages) * kStreamStageBytes + 2 * Gp * sizeof(float));
 }
 
 struct UnitParams;
