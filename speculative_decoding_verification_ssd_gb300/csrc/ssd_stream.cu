@@ -1,12 +1,14 @@
 // ssd_stream.cu -- persistent, warp-specialised streaming form of the fused
 // verify / cache-build / lookup kernel (sm_103a).
 //
-// One CTA per SM, three roles:
-//   * a producer warp (one elected lane) takes units (sequence b, position k)
-//     from a global counter and streams their logit rows with cp.async.bulk
-//     into two 4-stage shared-memory rings, one per consumer group, each stage
-//     guarded by a full/empty mbarrier pair; it serves whichever ring has a
-//     free stage, so one group's per-unit tail never stalls the HBM stream;
+// One CTA per SM, four roles:
+//   * two producer warps (one elected lane each), one per consumer group: each
+//     takes units (sequence b, position k) from a global counter and streams
+//     their logit rows with cp.async.bulk into its group's 4-stage shared-memory
+//     ring, each stage guarded by a full/empty mbarrier pair.  Units whose
+//     sequence samples (temperature > 0) and whose position is below K -- the
+//     two-row, two-pass units -- are handed out first, single rows last, so the
+//     grid ends on short units;
 //   * two consumer groups of 8 warps each, every group working through its
 //     own units:
 //       pass 1 (HBM)  per 32-token group: the raw maximum and, for sampled
@@ -20,9 +22,12 @@
 //       tail          normalisers, accept test ([SD] step 3), greedy argmax,
 //                     cache top-F_k (groups whose maximum reaches the F-th
 //                     largest per-thread maximum are expanded into (value, id)
-//                     keys), inverse-CDF bonus t_k at u_K; the last unit of a
-//                     sequence runs the epilogue (scan -> a, bonus t_a, outputs,
-//                     cache lookup).
+//                     keys), inverse-CDF bonus t_k at u_K;
+//   * a finisher warp that takes each unit's record from the groups through a
+//     small shared-memory queue, publishes it, counts the sequence's finished
+//     units and, for the last unit of a sequence, runs the epilogue (scan -> a,
+//     bonus t_a, outputs, cache lookup) with its 32 lanes loading in parallel;
+//     the consumer groups never wait on global-memory round trips.
 // A thread owns whole 32-token groups (bf16) or halves/quarters of them (fp32,
 // second pass), so group reductions need at most two shuffles.
 //
@@ -50,13 +55,26 @@ constexpr int kCandGroupsCap = 512;
 
 enum : int { kPassStats = 1, kPassResid = 2, kPassSkip = 3, kPassStop = 4 };
 
-struct Hdr {
-    int unit;   // unit index
+struct __align__(16) Hdr {
+    int unit;   // unit index (changes at every unit)
     int pass;   // kPass*
     int chunk;  // chunk index within the pass
     int nvec;   // 16-byte vectors per row in this stage
     int last;   // last chunk of the pass
+    int b, k;   // sequence and position of the unit
+    int pair;   // stage layout: 1 = target and draft halves, 0 = one row
 };
+
+// A finished unit on its way from a consumer group to the finisher warp.
+struct FinEntry {
+    UnitRecord rec;
+    int b, k;
+    int stop;  // 1: the group has no more units
+    int pad;
+};
+
+constexpr int kFinQ = 4;          // finisher queue entries per consumer group
+constexpr int kSchedCap = 2048;   // largest batch ordered by unit kind
 
 struct DraftShape {
     bool on;
@@ -268,7 +286,10 @@ __device__ uint32_t g_fth_largest(const GroupCtx &g, uint32_t v, int F, uint32_t
 struct GroupShared {
     uint64_t full_bar[kRS];
     uint64_t empty_bar[kRS];
+    uint64_t fin_full[kFinQ];
+    uint64_t fin_empty[kFinQ];
     Hdr hdr[kRS];
+    FinEntry fin[kFinQ];
     Scratch sc;
     uint64_t cand[kCandCap];
     int cgroups[kCandGroupsCap];
@@ -294,6 +315,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     extern __shared__ __align__(128) unsigned char dyn_smem[];
     __shared__ GroupShared gsh[kNG];
     __shared__ int s_abort;
+    __shared__ int s_nS;
+    __shared__ int s_cnt[kSchedCap / 32];
+    __shared__ uint16_t sched[kSchedCap];  // sampled sequences, then the others
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int B = P.B, K = P.K, V = P.V;
@@ -305,151 +329,306 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     const int64_t row_bytes = static_cast<int64_t>(V) * S;
 
     if (tid == 0) {
-        for (int g = 0; g < kNG; ++g)
+        for (int g = 0; g < kNG; ++g) {
             for (int i = 0; i < kRS; ++i) {
                 mbar_init(&gsh[g].full_bar[i], 1);
                 mbar_init(&gsh[g].empty_bar[i], kGW);
             }
+            for (int i = 0; i < kFinQ; ++i) {
+                mbar_init(&gsh[g].fin_full[i], 1);
+                mbar_init(&gsh[g].fin_empty[i], 1);
+            }
+        }
         s_abort = 0;
+        s_nS = 0;
         fence_mbar_init();
     }
     __syncthreads();
-
-    // =========================== producer ===================================
-    if (warp == kNG * kGW) {
-        if (lane != 0) return;
-        const uint64_t pol = policy_evict_first();
-        struct Ring {
-            int64_t n;   // stages pushed
-            int unit;    // unit being streamed (-1: start the claimed one)
-            int pass, chunk, nch;
-            bool pair, p2, skip, stopped;
-            const unsigned char *trow, *drow;
-            // the next unit, claimed ahead: pf 0 = not claimed, 1 = claimed,
-            // 2 = its temperature and reject bits are loaded
-            int pf;
-            int next_u;
-            float next_tau;
-            uint32_t next_rej;
-        };
-        Ring r[kNG];
-        // One prefetch step: claim a unit, or load the claimed unit's metadata.
-        // Steps are taken right after a stage is issued, so their latency
-        // overlaps the copies in flight.
-        auto prefetch_step = [&](Ring &q) {
-            if (q.pf == 0) {
-                q.next_u = static_cast<int>(atomicAdd(P.unit_counter, 1u));
-                q.pf = 1;
-            } else if (q.pf == 1) {
-                const int u = q.next_u;
-                if (u < nunits) {
-                    const int k = u / B;
-                    const int b = static_cast<int>((static_cast<int64_t>(u - k * B) * P.perm_mul) % B);
-                    q.next_tau = P.temperature[b];
-                    q.next_rej = (P.mode & kModeEarlyExit) ? __ldcg(P.seq_reject + b) : 0u;
+    // Unit order: pair units (sampled sequence, k < K) first, then the sampled
+    // rows K, then the other sequences' rows.  Every CTA maps the shared unit
+    // counter through this list, so it is built the same way everywhere: a
+    // stable compaction in ascending b (per-32 ballots, then chunk prefixes).
+    const bool use_list = B <= kSchedCap;
+    if (use_list) {
+        constexpr int kWarps = kStreamThreads / 32;
+        constexpr int kMaxIt = (kSchedCap / 32 + kWarps - 1) / kWarps;
+        const int nchunks = (B + 31) / 32;
+        uint32_t masks[kMaxIt];
+#pragma unroll
+        for (int i = 0; i < kMaxIt; ++i) {
+            const int c = warp + i * kWarps;
+            masks[i] = 0;
+            if (c < nchunks) {
+                const int b = c * 32 + lane;
+                bool smp = false;
+                if (b < B) {
+                    const float tau = P.temperature[b];
+                    smp = tau > 0.f && tau < INFINITY;
                 }
-                q.pf = 2;
+                masks[i] = __ballot_sync(kFull, smp);
+                if (lane == 0) s_cnt[c] = __popc(masks[i]);
+            }
+        }
+        __syncthreads();
+        int tot = 0;
+        for (int j = lane; j < nchunks; j += 32) tot += s_cnt[j];
+        tot = __reduce_add_sync(kFull, tot);
+        if (tid == 0) s_nS = tot;
+#pragma unroll
+        for (int i = 0; i < kMaxIt; ++i) {
+            const int c = warp + i * kWarps;
+            if (c < nchunks) {
+                int pre = 0;
+                for (int j = lane; j < c; j += 32) pre += s_cnt[j];
+                pre = __reduce_add_sync(kFull, pre);
+                const int b = c * 32 + lane;
+                if (b < B) {
+                    const int below = __popc(masks[i] & ((1u << lane) - 1u));
+                    if ((masks[i] >> lane) & 1u)
+                        sched[pre + below] = static_cast<uint16_t>(b);
+                    else
+                        sched[tot + (c * 32 - pre) + (lane - below)] = static_cast<uint16_t>(b);
+                }
+            }
+        }
+    }
+    __syncthreads();
+
+    // =========================== producers ==================================
+    if (warp >= kNG * kGW && warp < kNG * kGW + kNG) {
+        if (lane != 0) return;
+        const int rg = warp - kNG * kGW;  // ring served by this producer
+        GroupShared &gq = gsh[rg];
+        unsigned char *ring = dyn_smem + rg * kRS * kSB;
+        const uint64_t pol = policy_evict_first();
+        const int nS = s_nS;
+        const int nG = B - nS;
+        auto unit_bk = [&](int u, int &b, int &k) {
+            if (use_list) {
+                const int np = nS * K;
+                if (u < np) {
+                    k = u / nS;
+                    b = sched[u - k * nS];
+                    return;
+                }
+                int v = u - np;
+                if (v < nS) {
+                    k = K;
+                    b = sched[v];
+                    return;
+                }
+                v -= nS;
+                k = v / nG;
+                b = sched[nS + v - k * nG];
+            } else {
+                k = u / B;
+                b = static_cast<int>((static_cast<int64_t>(u - k * B) * P.perm_mul) % B);
             }
         };
-#pragma unroll
-        for (int g = 0; g < kNG; ++g) {
-            r[g].n = 0;
-            r[g].unit = -1;
-            r[g].stopped = false;
-            r[g].pf = 0;
-            r[g].next_u = 0;
-            r[g].next_tau = 0.f;
-            r[g].next_rej = 0;
-            prefetch_step(r[g]);
-        }
-        int idle_rounds = 0;
+        // The next unit is claimed and its metadata loaded while the current
+        // unit's last stages are issued, so neither round trip stalls the ring.
+        int pf_state = 0, pf_u = 0, pf_b = 0, pf_k = 0;
+        float pf_tau = 0.f;
+        uint32_t pf_rej = 0;
+        auto pf_step = [&]() {
+            if (pf_state == 0) {
+                pf_u = static_cast<int>(atomicAdd(P.unit_counter, 1u));
+                pf_state = 1;
+            } else if (pf_state == 1) {
+                if (pf_u < nunits) {
+                    unit_bk(pf_u, pf_b, pf_k);
+                    pf_tau = P.temperature[pf_b];
+                    pf_rej = (P.mode & kModeEarlyExit) ? __ldcg(P.seq_reject + pf_b) : 0u;
+                }
+                pf_state = 2;
+            }
+        };
+        uint32_t n = 0;  // stages pushed
         bool ok = true;
         for (;;) {
-            bool all_stopped = true, progress = false;
-#pragma unroll
-            for (int g = 0; g < kNG; ++g) {
-                Ring &q = r[g];
-                if (q.stopped) continue;
-                all_stopped = false;
-                const int s = static_cast<int>(q.n % kRS);
-                const uint32_t par = static_cast<uint32_t>(((q.n / kRS) & 1) ^ 1);
-                if (!mbar_test_wait(&gsh[g].empty_bar[s], par)) continue;
-                progress = true;
-                if (q.unit < 0) {
-                    while (q.pf < 2) prefetch_step(q);
-                    q.pf = 0;
-                    const int u = q.next_u;
-                    if (u >= nunits) {
-                        gsh[g].hdr[s] = Hdr{-1, kPassStop, 0, 0, 1};
-                        mbar_arrive_expect_tx(&gsh[g].full_bar[s], 0);
-                        ++q.n;
-                        q.stopped = true;
-                        continue;
-                    }
-                    const int k = u / B;
-                    const int b = static_cast<int>((static_cast<int64_t>(u - k * B) * P.perm_mul) % B);
-                    const bool sampled = (q.next_tau > 0.f) && (q.next_tau < INFINITY);
-                    q.unit = u;
-                    q.pair = sampled && k < K;
-                    q.p2 = q.pair && (do_verify || (do_cache && P.F[k] > 0));
-                    const uint32_t mask = (k >= 32) ? 0xFFFFFFFFu : ((1u << k) - 1u);
-                    q.skip = (P.mode & kModeEarlyExit) && k > 0 && (q.next_rej & mask) != 0;
-                    q.trow = static_cast<const unsigned char *>(P.tgt) +
-                             (static_cast<int64_t>(b) * P.tgt_seq_stride + static_cast<int64_t>(k) * V) * S;
-                    q.drow = q.pair ? static_cast<const unsigned char *>(P.drf) +
-                                          (static_cast<int64_t>(b) * P.drf_seq_stride +
-                                           static_cast<int64_t>(k) * V) * S
-                                    : nullptr;
-                    q.pass = kPassStats;
-                    q.chunk = 0;
-                    const int cb = q.pair ? HALF : kSB;
-                    q.nch = static_cast<int>((row_bytes + cb - 1) / cb);
-                }
-                if (q.skip) {
-                    gsh[g].hdr[s] = Hdr{q.unit, kPassSkip, 0, 0, 1};
-                    mbar_arrive_expect_tx(&gsh[g].full_bar[s], 0);
-                    ++q.n;
-                    q.unit = -1;
-                    prefetch_step(q);
-                    continue;
-                }
-                const int cb = q.pair ? HALF : kSB;
-                const int64_t off = static_cast<int64_t>(q.chunk) * cb;
-                const uint32_t bytes = static_cast<uint32_t>(row_bytes - off < cb ? row_bytes - off : cb);
-                gsh[g].hdr[s] = Hdr{q.unit, q.pass, q.chunk, static_cast<int>(bytes / 16), q.chunk == q.nch - 1};
-                unsigned char *dst = dyn_smem + (g * kRS + s) * kSB;
-                mbar_arrive_expect_tx(&gsh[g].full_bar[s], bytes * (q.pair ? 2u : 1u));
-                if (!q.pair || q.pass == kPassResid) {  // not read again
-                    bulk_copy_hint(dst, q.trow + off, bytes, &gsh[g].full_bar[s], pol);
-                    if (q.pair) bulk_copy_hint(dst + HALF, q.drow + off, bytes, &gsh[g].full_bar[s], pol);
-                } else {
-                    bulk_copy_g2s(dst, q.trow + off, bytes, &gsh[g].full_bar[s]);
-                    bulk_copy_g2s(dst + HALF, q.drow + off, bytes, &gsh[g].full_bar[s]);
-                }
-                ++q.n;
-                if (++q.chunk == q.nch) {
-                    q.chunk = 0;
-                    if (q.pass == kPassStats && q.p2)
-                        q.pass = kPassResid;
-                    else
-                        q.unit = -1;
-                }
-                prefetch_step(q);
-            }
-            if (all_stopped) break;
-            if (progress) {
-                idle_rounds = 0;
-            } else {
-                if (++idle_rounds > (1 << 24) || *reinterpret_cast<volatile int *>(&s_abort)) {
+            while (pf_state < 2) pf_step();
+            pf_state = 0;
+            const int u = pf_u;
+            if (u >= nunits) {
+                const int s = static_cast<int>(n % kRS);
+                if (!mbar_wait_bounded(&gq.empty_bar[s], ((n / kRS) & 1) ^ 1)) {
                     ok = false;
                     break;
                 }
-                __nanosleep(32);
+                gq.hdr[s] = Hdr{-1, kPassStop, 0, 0, 1, 0, 0, 0};
+                mbar_arrive_expect_tx(&gq.full_bar[s], 0);
+                break;
             }
+            const int b = pf_b, k = pf_k;
+            const float tau = pf_tau;
+            const bool sampled = (tau > 0.f) && (tau < INFINITY);
+            const bool pair = sampled && k < K;
+            const bool p2 = pair && (do_verify || (do_cache && P.F[k] > 0));
+            const uint32_t mask = (k >= 32) ? 0xFFFFFFFFu : ((1u << k) - 1u);
+            const bool skip = (P.mode & kModeEarlyExit) && k > 0 && (pf_rej & mask) != 0;
+            const unsigned char *trow = static_cast<const unsigned char *>(P.tgt) +
+                                        (static_cast<int64_t>(b) * P.tgt_seq_stride + static_cast<int64_t>(k) * V) * S;
+            const unsigned char *drow =
+                pair ? static_cast<const unsigned char *>(P.drf) +
+                           (static_cast<int64_t>(b) * P.drf_seq_stride + static_cast<int64_t>(k) * V) * S
+                     : nullptr;
+            const int cb = pair ? HALF : kSB;
+            const int nch = static_cast<int>((row_bytes + cb - 1) / cb);
+            const int total = skip ? 1 : nch * (p2 ? 2 : 1);
+            for (int i = 0; i < total; ++i) {
+                const int s = static_cast<int>(n % kRS);
+                if (!mbar_wait_bounded(&gq.empty_bar[s], ((n / kRS) & 1) ^ 1)) {
+                    ok = false;
+                    break;
+                }
+                if (skip) {
+                    gq.hdr[s] = Hdr{u, kPassSkip, 0, 0, 1, b, k, 0};
+                    mbar_arrive_expect_tx(&gq.full_bar[s], 0);
+                } else {
+                    const bool second = i >= nch;
+                    const int chunk = second ? i - nch : i;
+                    const int64_t off = static_cast<int64_t>(chunk) * cb;
+                    const uint32_t bytes = static_cast<uint32_t>(row_bytes - off < cb ? row_bytes - off : cb);
+                    gq.hdr[s] = Hdr{u, second ? kPassResid : kPassStats, chunk, static_cast<int>(bytes / 16),
+                                    chunk == nch - 1, b, k, pair ? 1 : 0};
+                    unsigned char *dst = ring + s * kSB;
+                    mbar_arrive_expect_tx(&gq.full_bar[s], bytes * (pair ? 2u : 1u));
+                    if (!pair || second) {  // not read again
+                        bulk_copy_hint(dst, trow + off, bytes, &gq.full_bar[s], pol);
+                        if (pair) bulk_copy_hint(dst + HALF, drow + off, bytes, &gq.full_bar[s], pol);
+                    } else {
+                        bulk_copy_g2s(dst, trow + off, bytes, &gq.full_bar[s]);
+                        bulk_copy_g2s(dst + HALF, drow + off, bytes, &gq.full_bar[s]);
+                    }
+                }
+                ++n;
+                if (total - i <= 3) pf_step();
+            }
+            if (!ok) break;
         }
         if (!ok) {
             atomicOr(&s_abort, 1);
             if (P.dev_status) atomicOr(P.dev_status, SSD_DEV_TIMEOUT);
+        }
+        return;
+    }
+
+    // =========================== finisher ===================================
+    if (warp == kNG * kGW + kNG) {
+        uint32_t nf[kNG];
+        bool stopped[kNG];
+#pragma unroll
+        for (int g = 0; g < kNG; ++g) {
+            nf[g] = 0;
+            stopped[g] = false;
+        }
+        int idle = 0;
+        for (;;) {
+            bool all = true, progress = false;
+#pragma unroll
+            for (int g = 0; g < kNG; ++g) {
+                if (stopped[g]) continue;
+                all = false;
+                const uint32_t qi = nf[g] % kFinQ;
+                const uint32_t par = (nf[g] / kFinQ) & 1;
+                const bool ready = __all_sync(kFull, mbar_test_wait(&gsh[g].fin_full[qi], par));
+                if (!ready) continue;
+                progress = true;
+                const FinEntry E = gsh[g].fin[qi];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&gsh[g].fin_empty[qi]);
+                ++nf[g];
+                if (E.stop) {
+                    stopped[g] = true;
+                    continue;
+                }
+                const int b = E.b, k = E.k;
+                if (lane == 0) {
+                    UnitRecord *R = P.rec + static_cast<int64_t>(b) * (K + 1) + k;
+                    *R = E.rec;
+                    if (E.rec.flags == 0 && E.rec.state == 1 && k < K && !E.rec.accept &&
+                        (P.mode & kModeEarlyExit))
+                        atomicOr(P.seq_reject + b, 1u << k);
+                }
+                // The record and the group's cache writes (ordered before the
+                // queue entry) become visible before the unit is counted.
+                __threadfence();
+                uint32_t done = 0;
+                if (lane == 0) done = atomicAdd(P.seq_count + b, 1u);
+                done = __shfl_sync(kFull, done, 0);
+                if (done != static_cast<uint32_t>(K)) continue;
+                // last unit of sequence b: the epilogue, lanes loading in parallel
+                __threadfence();
+                const UnitRecord *RR = P.rec + static_cast<int64_t>(b) * (K + 1);
+                int fl = 0, acc = 1, tk = -1;
+                float pt = NAN, qt = NAN;
+                if (lane < K) {
+                    fl = __ldcg(&RR[lane].flags);
+                    acc = __ldcg(&RR[lane].accept);
+                    tk = __ldcg(&RR[lane].tk);
+                    pt = __ldcg(&RR[lane].p_tok);
+                    qt = __ldcg(&RR[lane].q_tok);
+                }
+                const int flK = __ldcg(&RR[K].flags);
+                const int tkK = __ldcg(&RR[K].tk);
+                fl = static_cast<int>(__reduce_or_sync(kFull, static_cast<unsigned>(fl))) | flK;
+                const uint32_t rej = __ballot_sync(kFull, lane < K && acc == 0);
+                const int a = rej ? __ffs(rej) - 1 : K;
+                const int tsh = __shfl_sync(kFull, tk, a & 31);
+                const int tstar = a == K ? tkK : tsh;
+                const bool bad = fl != 0 || tstar < 0;
+                if (do_verify) {
+                    if (lane == 0) {
+                        P.accept_len[b] = bad ? -1 : a;
+                        P.bonus[b] = bad ? -1 : tstar;
+                    }
+                    if (P.p_tok && lane < K) {
+                        const bool keep = !bad && lane <= a;
+                        P.p_tok[static_cast<int64_t>(b) * K + lane] = keep ? pt : NAN;
+                        P.q_tok[static_cast<int64_t>(b) * K + lane] = keep ? qt : NAN;
+                    }
+                    if (P.mode & kModeLookup) {
+                        int slot = -1;
+                        if (!bad) {
+                            const int32_t *row = P.cache_tok + static_cast<int64_t>(b) * P.budget;
+                            for (int j0 = P.off[a]; j0 < P.off[a + 1] && slot < 0; j0 += 32) {
+                                const int j = j0 + lane;
+                                const bool m = j < P.off[a + 1] && __ldcg(row + j) == tstar;
+                                const uint32_t mm = __ballot_sync(kFull, m);
+                                if (mm) slot = j0 + __ffs(mm) - 1;
+                            }
+                        }
+                        if (lane == 0) {
+                            P.hit[b] = slot >= 0 ? 1 : 0;
+                            P.slot[b] = slot;
+                        }
+                    }
+                }
+                if (lane == 0) {
+                    if (fl && P.dev_status) atomicOr(P.dev_status, fl);
+                    P.seq_count[b] = 0;
+                    P.seq_reject[b] = 0;
+                }
+            }
+            if (all) break;
+            if (progress) {
+                idle = 0;
+            } else {
+                if (++idle > (1 << 24)) {
+                    if (lane == 0 && P.dev_status) atomicOr(P.dev_status, SSD_DEV_TIMEOUT);
+                    break;
+                }
+                __nanosleep(64);
+            }
+        }
+        // this CTA is done; the last CTA of the grid resets the unit scheduler
+        if (lane == 0) {
+            __threadfence();
+            const uint32_t done = atomicAdd(P.exit_counter, 1u);
+            if (done == gridDim.x - 1) {
+                *P.unit_counter = 0;
+                *P.exit_counter = 0;
+            }
         }
         return;
     }
@@ -578,7 +757,6 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             for (int j = 0; j < count; ++j) rr += gs.cand[j] > key ? 1 : 0;
             if (rr < Fk) {
                 P.cache_tok[static_cast<int64_t>(b) * P.budget + P.off[k] + rr] = key_id(key);
-                __threadfence();
             }
         }
         gbar(gc);
@@ -673,65 +851,29 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         if (t == 0) rec.tk = sc.bid;
     };
 
-    auto finish_unit = [&]() {
-        gbar(gc);
+    uint32_t nfin = 0;  // entries handed to the finisher (uniform in the group)
+    auto push_fin = [&](int stop) {
         if (t == 0) {
-            UnitRecord *R = P.rec + static_cast<int64_t>(b) * (K + 1) + k;
-            R->p_tok = rec.p_tok;
-            R->q_tok = rec.q_tok;
-            R->accept = rec.accept;
-            R->tk = rec.tk;
-            R->flags = rec.flags;
-            R->state = rec.state;
-            if (rec.flags == 0 && rec.state == 1 && !rowK && !rec.accept && (P.mode & kModeEarlyExit))
-                atomicOr(P.seq_reject + b, 1u << k);
-            __threadfence();
-            const uint32_t done = atomicAdd(P.seq_count + b, 1u);
-            if (done == static_cast<uint32_t>(K)) {
-                __threadfence();
-                const UnitRecord *RR = P.rec + static_cast<int64_t>(b) * (K + 1);
-                int fl = 0;
-                for (int i = 0; i <= K; ++i) fl |= __ldcg(&RR[i].flags);
-                int a = K;
-                for (int i = 0; i < K; ++i) {
-                    if (__ldcg(&RR[i].accept) == 0) {
-                        a = i;
-                        break;
-                    }
-                }
-                const int tstar = __ldcg(&RR[a].tk);
-                const bool bad = fl != 0 || tstar < 0;
-                if (do_verify) {
-                    P.accept_len[b] = bad ? -1 : a;
-                    P.bonus[b] = bad ? -1 : tstar;
-                    if (P.p_tok) {
-                        for (int i = 0; i < K; ++i) {
-                            const bool keep = !bad && i <= a;
-                            P.p_tok[static_cast<int64_t>(b) * K + i] = keep ? __ldcg(&RR[i].p_tok) : NAN;
-                            P.q_tok[static_cast<int64_t>(b) * K + i] = keep ? __ldcg(&RR[i].q_tok) : NAN;
-                        }
-                    }
-                    if (P.mode & kModeLookup) {
-                        int s = -1;
-                        if (!bad) {
-                            const int32_t *row = P.cache_tok + static_cast<int64_t>(b) * P.budget;
-                            for (int j = P.off[a]; j < P.off[a + 1]; ++j) {
-                                if (__ldcg(row + j) == tstar) {
-                                    s = j;
-                                    break;
-                                }
-                            }
-                        }
-                        P.hit[b] = s >= 0 ? 1 : 0;
-                        P.slot[b] = s;
-                    }
-                }
-                if (fl && P.dev_status) atomicOr(P.dev_status, fl);
-                P.seq_count[b] = 0;
-                P.seq_reject[b] = 0;
+            const uint32_t qi = nfin % kFinQ;
+            if (mbar_wait_bounded(&gs.fin_empty[qi], ((nfin / kFinQ) & 1) ^ 1)) {
+                FinEntry &E = gs.fin[qi];
+                E.rec = rec;
+                E.b = b;
+                E.k = k;
+                E.stop = stop;
+                mbar_arrive(&gs.fin_full[qi]);
+            } else {
+                atomicOr(&s_abort, 1);
+                if (P.dev_status) atomicOr(P.dev_status, SSD_DEV_TIMEOUT);
             }
         }
+        ++nfin;
+    };
+    // the unit is complete: hand its record to the finisher (the barrier orders
+    // every thread's cache writes before the hand-off)
+    auto finish_unit = [&]() {
         gbar(gc);
+        push_fin(0);
     };
 
     for (;;) {
@@ -747,8 +889,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         if (h.unit != cur) {
             // a new unit: per-unit constants (identical in every thread of the group)
             cur = h.unit;
-            k = cur / B;
-            b = static_cast<int>((static_cast<int64_t>(cur - k * B) * P.perm_mul) % B);
+            k = h.k;
+            b = h.b;
             const float tau = P.temperature[b];
             const bool tau_ok = (tau >= 0.f) && (tau < INFINITY);
             greedy = tau_ok && tau == 0.f;
@@ -805,7 +947,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
 
         // ---- stage processing -----------------------------------------------
         if (active) {
-            if (h.pass == kPassStats && pair) {
+            if (h.pass == kPassStats && h.pair) {
                 // threads [0, kGT/2) take target groups, the rest draft groups
                 const int row = t / (kGT / 2);
                 const int tr = t - row * (kGT / 2);
@@ -1053,16 +1195,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         }
     }
 
-    // this group is done; the last group of the grid resets the unit scheduler
+    // this group is done
     gbar(gc);
-    if (t == 0) {
-        __threadfence();
-        const uint32_t done = atomicAdd(P.exit_counter, 1u);
-        if (done == gridDim.x * kNG - 1) {
-            *P.unit_counter = 0;
-            *P.exit_counter = 0;
-        }
-    }
+    push_fin(1);
 }
 
 int stream_setup(int dtype, size_t optin, size_t *max_dyn) {

@@ -8,7 +8,8 @@ namespace ssd {
 
 constexpr int kStreamGroups = 2;       // consumer groups, each with its own ring
 constexpr int kStreamGroupWarps = 8;   // warps per consumer group
-constexpr int kStreamThreads = kStreamGroups * kStreamGroupWarps * 32 + 32;  // + one producer warp
+// consumer warps, then one producer warp per ring, then one finisher warp
+constexpr int kStreamThreads = kStreamGroups * kStreamGroupWarps * 32 + kStreamGroups * 32 + 32;
 constexpr int kStreamRingStages = 4;   // stages per ring
 constexpr int kStreamStageBytes = 16384;
 constexpr int kGroupTokens = 32;
