@@ -1,35 +1,34 @@
 // ssd_stream.cu -- persistent, warp-specialised streaming form of the fused
 // verify / cache-build / lookup kernel (sm_103a).
 //
-// One CTA per SM, four roles:
-//   * two producer warps (one elected lane each), one per consumer group: each
-//     takes units (sequence b, position k) from a global counter and streams
-//     their logit rows with cp.async.bulk into its group's 4-stage shared-memory
-//     ring, each stage guarded by a full/empty mbarrier pair.  Units whose
-//     sequence samples (temperature > 0) and whose position is below K -- the
-//     two-row, two-pass units -- are handed out first, single rows last, so the
-//     grid ends on short units;
-//   * two consumer groups of 8 warps each, every group working through its
-//     own units:
-//       pass 1 (HBM)  per 32-token group: the raw maximum and, for sampled
-//                     rows, the base-2 mass sum 2^(z c - gmax c) (c = log2 e / tau);
-//                     greedy rows keep only group maxima (drafted token
-//                     excluded); the draft row of a pair folds into running
-//                     statistics;
-//       pass 2 (L2)   pair units (sampled, k < K) stream both rows again (they
-//                     were just read, so they hit L2): per group the residual
-//                     mass sum max(0, p - q) and the largest residual;
-//       tail          normalisers, accept test ([SD] step 3), greedy argmax,
-//                     cache top-F_k (groups whose maximum reaches the F-th
-//                     largest per-thread maximum are expanded into (value, id)
-//                     keys), inverse-CDF bonus t_k at u_K;
-//   * a finisher warp that takes each unit's record from the groups through a
-//     small shared-memory queue, publishes it, counts the sequence's finished
-//     units and, for the last unit of a sequence, runs the epilogue (scan -> a,
-//     bonus t_a, outputs, cache lookup) with its 32 lanes loading in parallel;
-//     the consumer groups never wait on global-memory round trips.
-// A thread owns whole 32-token groups (bf16) or halves/quarters of them (fp32,
-// second pass), so group reductions need at most two shuffles.
+// One CTA per SM, three roles, each present once per work lane g = 0, 1:
+//   * producer warp g (one elected lane) takes units (sequence b, position k)
+//     from a global counter and streams their logit rows with cp.async.bulk
+//     into ring g (4 stages of 16 KB, each guarded by a full/empty mbarrier
+//     pair).  Units whose sequence samples (temperature > 0) and whose
+//     position is below K -- the two-row, two-pass units -- are handed out
+//     first, single rows last, so the grid ends on short units;
+//   * consumer group g (8 warps) only streams:
+//       pass 1 (HBM)  sampled rows fold every element into per-thread online
+//                     softmax statistics (base 2: m = max z c, S = sum 2^(z c - m),
+//                     c = log2 e / tau); single rows also store per 64-token
+//                     group the raw maximum (greedy rows: drafted token
+//                     excluded) and, when sampled, the mass 2^(z c - gmax c);
+//       between       a pair unit (sampled, k < K) reduces its two statistics
+//                     to the normalisers L_T, L_D and takes the accept test
+//                     ([SD] step 3);
+//       pass 2 (L2)   the pair's rows stream again (just read, so they hit L2):
+//                     per group the residual mass sum max(0, p - q) and the
+//                     largest residual;
+//     then hands the unit's group arrays (double-buffered) to
+//   * tail warp g, which, without block barriers: selects the cache top-F_k
+//     (groups whose maximum reaches the F-th largest lane maximum are
+//     re-read and ranked as (value, id) keys), draws the bonus t_k at u_K by
+//     inverse CDF over ascending token id (group prefix, then the crossing
+//     group re-read), takes the greedy argmax, publishes the unit's record,
+//     counts the sequence's finished units and, for the last one, runs the
+//     epilogue (scan -> a, bonus t_a, outputs, cache lookup).
+// The consumer groups never wait on a global-memory round trip.
 //
 // Operation sources: [SD] "Speculative decoding" (brentwoodlivery.com), "The
 // Algorithm (Step-by-Step)" and "Temperature and Sampling"; [WHY] "Why does
@@ -46,38 +45,35 @@ namespace {
 
 constexpr int kGW = kStreamGroupWarps;  // warps per consumer group
 constexpr int kGT = kGW * 32;           // threads per consumer group
-constexpr int kNG = kStreamGroups;      // consumer groups
+constexpr int kNG = kStreamGroups;      // consumer groups (= rings = tail warps)
 constexpr int kRS = kStreamRingStages;  // stages per ring
 constexpr int kSB = kStreamStageBytes;  // bytes per stage
+constexpr int kGTok = kGroupTokens;     // tokens per group of the group arrays
+constexpr int kNBuf = 2;                // group-array buffers per consumer group
+constexpr int kProducerWarp0 = kNG * kGW;
+constexpr int kTailWarp0 = kProducerWarp0 + kNG;
 constexpr unsigned kFull = 0xFFFFFFFFu;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kCandGroupsCap = 512;
+constexpr int kSchedCap = 2048;  // largest batch ordered by unit kind
+
+static_assert(kTailWarp0 + kNG == kStreamThreads / 32, "warp roles");
 
 enum : int { kPassStats = 1, kPassResid = 2, kPassSkip = 3, kPassStop = 4 };
+enum : int { kKindStop = 0, kKindPair = 1, kKindGreedy = 2, kKindSampled = 3, kKindPass = 4 };
 
+// Stage header written by the producer: code = pass | last << 4 | pair << 5.
 struct __align__(16) Hdr {
-    int unit;   // unit index (changes at every unit)
-    int pass;   // kPass*
+    int unit;
+    int code;
     int chunk;  // chunk index within the pass
     int nvec;   // 16-byte vectors per row in this stage
-    int last;   // last chunk of the pass
     int b, k;   // sequence and position of the unit
-    int pair;   // stage layout: 1 = target and draft halves, 0 = one row
+    int pad0, pad1;
 };
-
-// A finished unit on its way from a consumer group to the finisher warp.
-struct FinEntry {
-    UnitRecord rec;
-    int b, k;
-    int stop;  // 1: the group has no more units
-    int pad;
-};
-
-constexpr int kFinQ = 4;          // finisher queue entries per consumer group
-constexpr int kSchedCap = 2048;   // largest batch ordered by unit kind
 
 struct DraftShape {
-    bool on;
+    int on;
     float thr;
     int thr_id;
     float l2C;
@@ -95,6 +91,31 @@ __device__ __forceinline__ float resid_of(float zp, float zq, float c, float nLT
     const float eq = ex2(fmaf(zq, c, nLDb));
     return fmaxf(ep - eq, 0.f);
 }
+
+// A finished unit's hand-off from a consumer group to its tail warp.
+struct TailDesc {
+    int kind, b, k, flags;
+    int state, accept, xt, pad0;
+    float c;       // log2 e / tau
+    float M, S;    // sampled single row: target statistics (base 2)
+    float LT, LD;  // pair: normalisers (base 2)
+    float p_tok, q_tok, pad1;
+    DraftShape shape;
+};
+
+struct GroupShared {
+    uint64_t full_bar[kRS];
+    uint64_t empty_bar[kRS];
+    uint64_t tail_full[kNBuf];
+    uint64_t tail_empty[kNBuf];
+    Hdr hdr[kRS];
+    TailDesc desc[kNBuf];
+    Stat red[kGW];
+    // tail-warp scratch
+    uint64_t cand[kCandCap];
+    int cgroups[kCandGroupsCap];
+    int cnt[2];
+};
 
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;
@@ -117,16 +138,20 @@ __device__ __forceinline__ uint4 neg_inf_vec() {
     return make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
 }
 
-// Loads the VPT vectors [vbase, vbase + VPT) of a staged row (vectors at or
-// past nvec read as -inf), rotated by `rot` so that neighbouring threads hit
-// different shared-memory banks.
+// Loads the VPT vectors [vbase, vbase + VPT) of a staged row, rotated by `rot`
+// so that neighbouring threads hit different shared-memory banks.  With
+// `full` every vector is in the stage; otherwise vectors at or past nvec read
+// as -inf.
 template <class D, int VPT>
 __device__ __forceinline__ void load_vecs(const unsigned char *row, int vbase, int nvec, int rot,
-                                          uint4 (&w)[VPT]) {
+                                          bool full, uint4 (&w)[VPT]) {
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
         const int v = vbase + ((k + rot) & (VPT - 1));
-        w[k] = v < nvec ? *reinterpret_cast<const uint4 *>(row + 16 * v) : neg_inf_vec<D>();
+        if (full)
+            w[k] = *reinterpret_cast<const uint4 *>(row + 16 * v);
+        else
+            w[k] = v < nvec ? *reinterpret_cast<const uint4 *>(row + 16 * v) : neg_inf_vec<D>();
     }
 }
 
@@ -138,12 +163,16 @@ __device__ __forceinline__ float vecs_max(const uint4 (&w)[VPT]) {
     return rm.get();
 }
 
+// sum over the vectors of 2^(z c - mc), two independent accumulators
 template <class D, int VPT>
 __device__ __forceinline__ float vecs_expsum(const uint4 (&w)[VPT], float c, float mc) {
-    float2 a = make_float2(0.f, 0.f);
+    float2 a = make_float2(0.f, 0.f), b = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int k = 0; k < VPT; ++k) a = exp_sum<D>(w[k], c, mc, a);
-    return a.x + a.y;
+    for (int k = 0; k < VPT; k += 2) {
+        a = exp_sum<D>(w[k], c, mc, a);
+        if (k + 1 < VPT) b = exp_sum<D>(w[k + 1], c, mc, b);
+    }
+    return (a.x + a.y) + (b.x + b.y);
 }
 
 template <int TPG>
@@ -165,136 +194,64 @@ __device__ __forceinline__ float tpg_sum(float v) {
     return v;
 }
 
-// ---- group-wide reductions (one consumer group, named barrier 1 + group) ----
-struct Scratch {
-    uint32_t u[kGW];
-    float f[kGW];
-    double d[kGW];
-    uint64_t k[kGW];
-    Stat st[kGW];
-    int i[4];
-    double cut;
-    uint64_t bkey;
-    int bid;
-};
-
-struct GroupCtx {
-    int bar_id;  // named barrier of the group
-    int t;       // thread index within the group
-    int lane, warp;
-};
-
-__device__ __forceinline__ void gbar(const GroupCtx &g) {
-    asm volatile("bar.sync %0, %1;" ::"r"(g.bar_id), "r"(kGT) : "memory");
+// NaN-propagating merge of two online statistics.
+__device__ __forceinline__ Stat stat_merge_nan(Stat a, Stat b) {
+    const float m = fmax_nan(a.m, b.m);
+    if (m == -INFINITY) return {m, 0.f};
+    const float sa = (a.m == -INFINITY) ? 0.f : a.S * ex2(a.m - m);
+    const float sb = (b.m == -INFINITY) ? 0.f : b.S * ex2(b.m - m);
+    return {m, sa + sb};
 }
 
-__device__ uint32_t g_max_u32(const GroupCtx &g, uint32_t v, Scratch &s) {
-    v = __reduce_max_sync(kFull, v);
-    gbar(g);
-    if (g.lane == 0) s.u[g.warp] = v;
-    gbar(g);
-    uint32_t r = s.u[0];
-    for (int w = 1; w < kGW; ++w) r = s.u[w] > r ? s.u[w] : r;
-    return r;
+// Folds a block whose largest base-2 value is xm into st; mass(mn) returns the
+// block's sum of 2^(x - mn) for the new maximum mn.
+template <class F>
+__device__ __forceinline__ void stat_fold(Stat &st, float xm, F mass) {
+    const float mn = fmax_nan(st.m, xm);
+    if (mn == -INFINITY) return;
+    const float keep = (st.m == -INFINITY) ? 0.f : st.S * ex2(st.m - mn);
+    st.S = keep + mass(mn);
+    st.m = mn;
 }
 
-__device__ uint64_t g_max_u64(const GroupCtx &g, uint64_t v, Scratch &s) {
+__device__ __forceinline__ Stat warp_stat(Stat s) {
+    const uint32_t mo = __reduce_max_sync(kFull, ordered_bits(s.m));
+    const float M = value_of_ordered(mo);
+    float S = (s.m == -INFINITY) ? 0.f : s.S * ex2(s.m - M);
+    if (M == -INFINITY) S = 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(kFull, S, o);
+    return {M, S};
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+    return v;
+}
+
+__device__ __forceinline__ uint64_t warp_max_u64(uint64_t v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         const uint64_t x = __shfl_xor_sync(kFull, v, o);
         v = x > v ? x : v;
     }
-    gbar(g);
-    if (g.lane == 0) s.k[g.warp] = v;
-    gbar(g);
-    uint64_t r = s.k[0];
-    for (int w = 1; w < kGW; ++w) r = s.k[w] > r ? s.k[w] : r;
-    return r;
+    return v;
 }
 
-__device__ float g_sum_f32(const GroupCtx &g, float v, Scratch &s) {
+// Inclusive prefix sum over the warp (fp64).
+__device__ __forceinline__ double warp_incl_scan(double v, int lane) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
-    gbar(g);
-    if (g.lane == 0) s.f[g.warp] = v;
-    gbar(g);
-    float r = s.f[0];
-    for (int w = 1; w < kGW; ++w) r += s.f[w];
-    return r;
-}
-
-__device__ Stat g_stat(const GroupCtx &g, Stat st, Scratch &s) {
-    const uint32_t mo = __reduce_max_sync(kFull, ordered_bits(st.m));
-    const float M = value_of_ordered(mo);
-    float S = (st.m == -INFINITY) ? 0.f : st.S * ex2(st.m - M);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(kFull, S, o);
-    gbar(g);
-    if (g.lane == 0) s.st[g.warp] = {M, M == -INFINITY ? 0.f : S};
-    gbar(g);
-    Stat r = s.st[0];
-    for (int w = 1; w < kGW; ++w) r = stat_merge(r, s.st[w]);
-    return r;
-}
-
-// F-th largest (with multiplicity) of the per-thread values v of the group
-// (ordered bits; 0 = none).  tops: kGW * 32 words.
-__device__ uint32_t g_fth_largest(const GroupCtx &g, uint32_t v, int F, uint32_t *tops, Scratch &s) {
-    const int Fw = F < 32 ? F : 32;
-    gbar(g);
-    for (int it = 0; it < Fw; ++it) {
-        const uint32_t mx = __reduce_max_sync(kFull, v);
-        const uint32_t who = __ballot_sync(kFull, v == mx);
-        if (g.lane == __ffs(who) - 1) v = 0;
-        if (g.lane == 0) tops[g.warp * 32 + it] = mx;
+    for (int o = 1; o < 32; o <<= 1) {
+        const double y = __shfl_up_sync(kFull, v, o);
+        if (lane >= o) v += y;
     }
-    gbar(g);
-    if (g.warp == 0) {
-        uint32_t vals[kGW];
-        const int nq = kGW * Fw;
-#pragma unroll
-        for (int i = 0; i < kGW; ++i) {
-            const int q = g.lane + 32 * i;
-            vals[i] = q < nq ? tops[(q / Fw) * 32 + (q % Fw)] : 0u;
-        }
-        uint32_t mx = 0;
-        for (int it = 0; it < F; ++it) {
-            uint32_t lm = vals[0];
-#pragma unroll
-            for (int i = 1; i < kGW; ++i) lm = vals[i] > lm ? vals[i] : lm;
-            mx = __reduce_max_sync(kFull, lm);
-            const uint32_t who = __ballot_sync(kFull, lm == mx);
-            if (g.lane == __ffs(who) - 1) {
-                bool done = false;
-#pragma unroll
-                for (int i = 0; i < kGW; ++i)
-                    if (!done && vals[i] == mx) {
-                        vals[i] = 0;
-                        done = true;
-                    }
-            }
-        }
-        if (g.lane == 0) s.u[0] = mx;
-    }
-    gbar(g);
-    const uint32_t r = s.u[0];
-    gbar(g);
-    return r;
+    return v;
 }
 
-// Per consumer group shared state.
-struct GroupShared {
-    uint64_t full_bar[kRS];
-    uint64_t empty_bar[kRS];
-    uint64_t fin_full[kFinQ];
-    uint64_t fin_empty[kFinQ];
-    Hdr hdr[kRS];
-    FinEntry fin[kFinQ];
-    Scratch sc;
-    uint64_t cand[kCandCap];
-    int cgroups[kCandGroupsCap];
-    uint32_t tops[kGW * 32];
-};
+__device__ __forceinline__ bool stat_ok(Stat s) {
+    return (s.m < INFINITY) && (s.S > 0.f) && (s.S < INFINITY);
+}
 
 }  // namespace
 
@@ -302,15 +259,19 @@ template <class D>
 __global__ void __launch_bounds__(kStreamThreads, 1)
     ssd_stream_kernel(const __grid_constant__ UnitParams P) {
     constexpr int VEC = D::kVec, S = D::kBytes;
-    constexpr int GV = kGroupTokens / VEC;        // vectors per 32-token group
-    constexpr int HALF = kSB / 2;                 // bytes per row in a pair stage
-    constexpr int GPR = HALF / 16 / GV;           // groups per row in a pair stage
-    constexpr int GPS = kSB / 16 / GV;            // groups in a single-row stage
-    constexpr int TPG1 = (kGT / 2) / GPR;         // pass 1 pair: threads per group (per row)
-    constexpr int TPGS = kGT / GPS;               // pass 1 single: threads per group
-    constexpr int TPG2 = kGT / GPR;               // pass 2: threads per group
-    constexpr int VPT1 = GV / TPG1, VPTS = GV / TPGS, VPT2 = GV / TPG2;
+    constexpr int GV = kGTok / VEC;        // vectors per group
+    constexpr int HALF = kSB / 2;          // bytes per row in a pair stage
+    constexpr int FULL_PAIR = HALF / 16;   // vectors per row in a full pair stage
+    constexpr int FULL_ONE = kSB / 16;     // vectors in a full single-row stage
+    constexpr int GPR = FULL_PAIR / GV;    // groups per row in a pair stage
+    constexpr int GPS = FULL_ONE / GV;     // groups in a single-row stage
+    constexpr int TPGS = kGT / GPS;        // single rows: threads per group
+    constexpr int TPG2 = kGT / GPR;        // pass 2: threads per group
+    constexpr int VPT1 = FULL_PAIR / (kGT / 2), VPTS = GV / TPGS, VPT2 = GV / TPG2;
     static_assert(VPT1 == 4 && VPTS == 4 && VPT2 == 2, "stage geometry");
+    constexpr int LPG = GV;        // tail: lanes per group (one vector each)
+    constexpr int GPI = 32 / LPG;  // tail: groups per warp iteration
+    static_assert(32 % LPG == 0, "tail geometry");
 
     extern __shared__ __align__(128) unsigned char dyn_smem[];
     __shared__ GroupShared gsh[kNG];
@@ -321,7 +282,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int B = P.B, K = P.K, V = P.V;
-    const int G = (V + kGroupTokens - 1) / kGroupTokens;
+    const int G = (V + kGTok - 1) / kGTok;
     const int Gp = (G + 31) & ~31;
     const bool do_verify = (P.mode & kModeVerify) != 0;
     const bool do_cache = (P.mode & kModeCache) != 0;
@@ -334,9 +295,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                 mbar_init(&gsh[g].full_bar[i], 1);
                 mbar_init(&gsh[g].empty_bar[i], kGW);
             }
-            for (int i = 0; i < kFinQ; ++i) {
-                mbar_init(&gsh[g].fin_full[i], 1);
-                mbar_init(&gsh[g].fin_empty[i], 1);
+            for (int i = 0; i < kNBuf; ++i) {
+                mbar_init(&gsh[g].tail_full[i], 1);
+                mbar_init(&gsh[g].tail_empty[i], 1);
             }
         }
         s_abort = 0;
@@ -395,9 +356,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     __syncthreads();
 
     // =========================== producers ==================================
-    if (warp >= kNG * kGW && warp < kNG * kGW + kNG) {
+    if (warp >= kProducerWarp0 && warp < kTailWarp0) {
         if (lane != 0) return;
-        const int rg = warp - kNG * kGW;  // ring served by this producer
+        const int rg = warp - kProducerWarp0;  // ring served by this producer
         GroupShared &gq = gsh[rg];
         unsigned char *ring = dyn_smem + rg * kRS * kSB;
         const uint64_t pol = policy_evict_first();
@@ -455,7 +416,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                     ok = false;
                     break;
                 }
-                gq.hdr[s] = Hdr{-1, kPassStop, 0, 0, 1, 0, 0, 0};
+                gq.hdr[s] = Hdr{-1, kPassStop | (1 << 4), 0, 0, 0, 0, 0, 0};
                 mbar_arrive_expect_tx(&gq.full_bar[s], 0);
                 break;
             }
@@ -482,15 +443,16 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                     break;
                 }
                 if (skip) {
-                    gq.hdr[s] = Hdr{u, kPassSkip, 0, 0, 1, b, k, 0};
+                    gq.hdr[s] = Hdr{u, kPassSkip | (1 << 4), 0, 0, b, k, 0, 0};
                     mbar_arrive_expect_tx(&gq.full_bar[s], 0);
                 } else {
                     const bool second = i >= nch;
                     const int chunk = second ? i - nch : i;
                     const int64_t off = static_cast<int64_t>(chunk) * cb;
                     const uint32_t bytes = static_cast<uint32_t>(row_bytes - off < cb ? row_bytes - off : cb);
-                    gq.hdr[s] = Hdr{u, second ? kPassResid : kPassStats, chunk, static_cast<int>(bytes / 16),
-                                    chunk == nch - 1, b, k, pair ? 1 : 0};
+                    const int code = (second ? kPassResid : kPassStats) | ((chunk == nch - 1) << 4) |
+                                     ((pair ? 1 : 0) << 5);
+                    gq.hdr[s] = Hdr{u, code, chunk, static_cast<int>(bytes / 16), b, k, 0, 0};
                     unsigned char *dst = ring + s * kSB;
                     mbar_arrive_expect_tx(&gq.full_bar[s], bytes * (pair ? 2u : 1u));
                     if (!pair || second) {  // not read again
@@ -513,119 +475,419 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         return;
     }
 
-    // =========================== finisher ===================================
-    if (warp == kNG * kGW + kNG) {
-        uint32_t nf[kNG];
-        bool stopped[kNG];
-#pragma unroll
-        for (int g = 0; g < kNG; ++g) {
-            nf[g] = 0;
-            stopped[g] = false;
-        }
-        int idle = 0;
-        for (;;) {
-            bool all = true, progress = false;
-#pragma unroll
-            for (int g = 0; g < kNG; ++g) {
-                if (stopped[g]) continue;
-                all = false;
-                const uint32_t qi = nf[g] % kFinQ;
-                const uint32_t par = (nf[g] / kFinQ) & 1;
-                const bool ready = __all_sync(kFull, mbar_test_wait(&gsh[g].fin_full[qi], par));
-                if (!ready) continue;
-                progress = true;
-                const FinEntry E = gsh[g].fin[qi];
+    // =========================== tail warps =================================
+    if (warp >= kTailWarp0) {
+        const int team = warp - kTailWarp0;
+        GroupShared &gs = gsh[team];
+        float *const arrays = reinterpret_cast<float *>(dyn_smem + kNG * kRS * kSB) + team * kNBuf * 2 * Gp;
+        const int R = (G + 31) / 32;  // groups per lane, contiguous
+        const int g0 = min(G, lane * R), g1 = min(G, g0 + R);
+
+        for (uint32_t j = 0;; ++j) {
+            const int buf = static_cast<int>(j & 1);
+            if (!mbar_wait_bounded(&gs.tail_full[buf], (j >> 1) & 1)) {
+                if (lane == 0 && P.dev_status) atomicOr(P.dev_status, SSD_DEV_TIMEOUT);
+                break;
+            }
+            const TailDesc d = gs.desc[buf];
+            if (d.kind == kKindStop) {
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&gsh[g].fin_empty[qi]);
-                ++nf[g];
-                if (E.stop) {
-                    stopped[g] = true;
-                    continue;
+                if (lane == 0) mbar_arrive(&gs.tail_empty[buf]);
+                break;
+            }
+            float *gmax = arrays + buf * 2 * Gp;
+            float *gsum = gmax + Gp;
+            const int b = d.b, k = d.k;
+            const int Fk = do_cache ? P.F[k] : 0;
+            const float c = d.c;
+            const unsigned char *trow = static_cast<const unsigned char *>(P.tgt) +
+                                        (static_cast<int64_t>(b) * P.tgt_seq_stride + static_cast<int64_t>(k) * V) * S;
+            const unsigned char *drow = static_cast<const unsigned char *>(P.drf) +
+                                        (static_cast<int64_t>(b) * P.drf_seq_stride + static_cast<int64_t>(k) * V) * S;
+            const int xt = d.xt;
+            const int xmask = (d.kind == kKindGreedy && k < K) ? xt : -1;
+            const float nLT = -d.LT;
+            const DraftShape shape = d.shape;
+            UnitRecord rec{};
+            rec.p_tok = d.p_tok;
+            rec.q_tok = d.q_tok;
+            rec.accept = d.accept;
+            rec.tk = -1;
+            rec.flags = d.flags;
+            rec.state = d.state;
+
+            auto resid_e = [&](float zp, float zq, int e) -> float {
+                return resid_of(zp, zq, c, nLT, draft_bias(shape, zq, e) - d.LD);
+            };
+
+            // ---- cache top-F_k (gmax holds the scores' group maxima) --------
+            auto top_f = [&](bool resid) {
+                uint32_t tv = 0;
+                for (int g = g0; g < g1; ++g) {
+                    const uint32_t o = ordered_bits(gmax[g]);
+                    tv = o > tv ? o : tv;
                 }
-                const int b = E.b, k = E.k;
+                uint32_t th = 0;
+                if (Fk <= 32) {
+                    // F-th largest (with multiplicity) of the 32 lane maxima
+                    uint32_t v = tv;
+                    for (int it = 0; it < Fk; ++it) {
+                        th = __reduce_max_sync(kFull, v);
+                        const uint32_t who = __ballot_sync(kFull, v == th);
+                        if (lane == __ffs(who) - 1) v = 0;
+                    }
+                } else {
+                    // largest th with at least F groups whose maximum reaches it
+                    uint32_t lo = 0, hi = 0xFFFFFFFFu;
+                    while (lo < hi) {
+                        const uint32_t mid = lo + ((hi - lo) >> 1) + 1;
+                        int cnt = 0;
+                        for (int g = g0; g < g1; ++g) cnt += ordered_bits(gmax[g]) >= mid ? 1 : 0;
+                        cnt = __reduce_add_sync(kFull, cnt);
+                        if (cnt >= Fk)
+                            lo = mid;
+                        else
+                            hi = mid - 1;
+                    }
+                    th = lo;
+                }
                 if (lane == 0) {
-                    UnitRecord *R = P.rec + static_cast<int64_t>(b) * (K + 1) + k;
-                    *R = E.rec;
-                    if (E.rec.flags == 0 && E.rec.state == 1 && k < K && !E.rec.accept &&
-                        (P.mode & kModeEarlyExit))
-                        atomicOr(P.seq_reject + b, 1u << k);
+                    gs.cnt[0] = 0;
+                    gs.cnt[1] = 0;
                 }
-                // The record and the group's cache writes (ordered before the
-                // queue entry) become visible before the unit is counted.
-                __threadfence();
-                uint32_t done = 0;
-                if (lane == 0) done = atomicAdd(P.seq_count + b, 1u);
-                done = __shfl_sync(kFull, done, 0);
-                if (done != static_cast<uint32_t>(K)) continue;
-                // last unit of sequence b: the epilogue, lanes loading in parallel
-                __threadfence();
-                const UnitRecord *RR = P.rec + static_cast<int64_t>(b) * (K + 1);
-                int fl = 0, acc = 1, tk = -1;
-                float pt = NAN, qt = NAN;
-                if (lane < K) {
-                    fl = __ldcg(&RR[lane].flags);
-                    acc = __ldcg(&RR[lane].accept);
-                    tk = __ldcg(&RR[lane].tk);
-                    pt = __ldcg(&RR[lane].p_tok);
-                    qt = __ldcg(&RR[lane].q_tok);
+                __syncwarp();
+                for (int g = g0; g < g1; ++g) {
+                    if (ordered_bits(gmax[g]) >= th) {
+                        const int idx = atomicAdd(&gs.cnt[0], 1);
+                        if (idx < kCandGroupsCap) gs.cgroups[idx] = g;
+                    }
                 }
-                const int flK = __ldcg(&RR[K].flags);
-                const int tkK = __ldcg(&RR[K].tk);
-                fl = static_cast<int>(__reduce_or_sync(kFull, static_cast<unsigned>(fl))) | flK;
-                const uint32_t rej = __ballot_sync(kFull, lane < K && acc == 0);
-                const int a = rej ? __ffs(rej) - 1 : K;
-                const int tsh = __shfl_sync(kFull, tk, a & 31);
-                const int tstar = a == K ? tkK : tsh;
-                const bool bad = fl != 0 || tstar < 0;
-                if (do_verify) {
-                    if (lane == 0) {
-                        P.accept_len[b] = bad ? -1 : a;
-                        P.bonus[b] = bad ? -1 : tstar;
-                    }
-                    if (P.p_tok && lane < K) {
-                        const bool keep = !bad && lane <= a;
-                        P.p_tok[static_cast<int64_t>(b) * K + lane] = keep ? pt : NAN;
-                        P.q_tok[static_cast<int64_t>(b) * K + lane] = keep ? qt : NAN;
-                    }
-                    if (P.mode & kModeLookup) {
-                        int slot = -1;
-                        if (!bad) {
-                            const int32_t *row = P.cache_tok + static_cast<int64_t>(b) * P.budget;
-                            for (int j0 = P.off[a]; j0 < P.off[a + 1] && slot < 0; j0 += 32) {
-                                const int j = j0 + lane;
-                                const bool m = j < P.off[a + 1] && __ldcg(row + j) == tstar;
-                                const uint32_t mm = __ballot_sync(kFull, m);
-                                if (mm) slot = j0 + __ffs(mm) - 1;
+                __syncwarp();
+                const int ncg = gs.cnt[0];
+                const bool all_groups = ncg > kCandGroupsCap;
+                const int ngroups = all_groups ? G : ncg;
+                uint64_t theta = static_cast<uint64_t>(th) << 32;
+                const int sub = lane / LPG, li = lane % LPG;
+                int count = 0;
+                for (int round = 0; round < 64; ++round) {
+                    for (int q0 = 0; q0 < ngroups; q0 += 2 * GPI) {
+                        uint4 wt[2], wd[2];
+                        int e0[2];
+#pragma unroll
+                        for (int x = 0; x < 2; ++x) {
+                            const int q = q0 + x * GPI + sub;
+                            e0[x] = V;
+                            if (q < ngroups) {
+                                const int g = all_groups ? q : gs.cgroups[q];
+                                e0[x] = g * kGTok + li * VEC;
+                            }
+                            if (e0[x] < V) {
+                                wt[x] = __ldg(reinterpret_cast<const uint4 *>(trow + static_cast<int64_t>(e0[x]) * S));
+                                if (resid)
+                                    wd[x] = __ldg(reinterpret_cast<const uint4 *>(drow + static_cast<int64_t>(e0[x]) * S));
                             }
                         }
-                        if (lane == 0) {
-                            P.hit[b] = slot >= 0 ? 1 : 0;
-                            P.slot[b] = slot;
+#pragma unroll
+                        for (int x = 0; x < 2; ++x) {
+                            if (e0[x] >= V) continue;
+                            float zt[VEC], zd[VEC];
+                            decode_vec<D>(wt[x], zt);
+                            if (resid) decode_vec<D>(wd[x], zd);
+#pragma unroll
+                            for (int i = 0; i < VEC; ++i) {
+                                const int e = e0[x] + i;
+                                uint64_t key;
+                                if (resid)
+                                    key = make_key(resid_e(zt[i], zd[i], e), e);
+                                else
+                                    key = (e == xmask) ? excluded_key(e) : make_key(zt[i], e);
+                                if (key >= theta) {
+                                    const int idx = atomicAdd(&gs.cnt[1], 1);
+                                    if (idx < kCandCap) gs.cand[idx] = key;
+                                }
+                            }
                         }
                     }
+                    __syncwarp();
+                    count = gs.cnt[1];
+                    if (count <= kCandCap) break;
+                    // overflow: raise theta to the F-th largest of the stored keys
+                    for (int kk = 2; kk <= kCandCap; kk <<= 1) {
+                        for (int jj = kk >> 1; jj > 0; jj >>= 1) {
+                            for (int i = lane; i < kCandCap; i += 32) {
+                                const int ixj = i ^ jj;
+                                if (ixj > i) {
+                                    const uint64_t a = gs.cand[i], cc2 = gs.cand[ixj];
+                                    const bool desc = (i & kk) == 0;
+                                    if (desc ? (a < cc2) : (a > cc2)) {
+                                        gs.cand[i] = cc2;
+                                        gs.cand[ixj] = a;
+                                    }
+                                }
+                            }
+                            __syncwarp();
+                        }
+                    }
+                    theta = gs.cand[Fk - 1];
+                    __syncwarp();
+                    if (lane == 0) gs.cnt[1] = 0;
+                    __syncwarp();
                 }
+                if (count > kCandCap) count = kCandCap;
+                // rank by counting; ranks below F go straight to the cache row
+                for (int i = lane; i < count; i += 32) {
+                    const uint64_t key = gs.cand[i];
+                    int rr = 0;
+                    for (int jx = 0; jx < count; ++jx) rr += gs.cand[jx] > key ? 1 : 0;
+                    if (rr < Fk) P.cache_tok[static_cast<int64_t>(b) * P.budget + P.off[k] + rr] = key_id(key);
+                }
+                __syncwarp();
+            };
+
+            // ---- inverse-CDF bonus at u_K over ascending token id -----------
+            // Group weights: residual masses (gsum), or, with pmode, p-masses
+            // gsum * 2^(gmax c - Mc).
+            auto crossing = [&](bool pmode, float Mc) {
+                auto gweight = [&](int g) -> float {
+                    if (!pmode) return gsum[g];
+                    const float gm = gmax[g];
+                    return (gm == -INFINITY) ? 0.f : gsum[g] * ex2(fmaf(gm, c, -Mc));
+                };
+                float run = 0.f;
+                int lastpos = -1;
+                for (int g = g0; g < g1; ++g) {
+                    const float wg = gweight(g);
+                    run += wg;
+                    if (wg > 0.f) lastpos = g;
+                }
+                const double incl = warp_incl_scan(static_cast<double>(run), lane);
+                const double tot = __shfl_sync(kFull, incl, 31);
+                const double T = static_cast<double>(P.uniforms[static_cast<int64_t>(b) * (K + 1) + K]) * tot;
+                const double before = incl - static_cast<double>(run);
+                const uint32_t hit = __ballot_sync(kFull, run > 0.f && before + static_cast<double>(run) > T);
+                int gstar;
+                double cut;
+                if (hit) {
+                    // the crossing lane's groups, scanned by the whole warp
+                    const int ls = __ffs(hit) - 1;
+                    const double base = __shfl_sync(kFull, before, ls);
+                    const int a0 = min(G, ls * R), a1 = min(G, a0 + R);
+                    const int per = (a1 - a0 + 31) / 32;
+                    const int h0 = min(a1, a0 + lane * per), h1 = min(a1, h0 + per);
+                    float r2 = 0.f;
+                    for (int g = h0; g < h1; ++g) r2 += gweight(g);
+                    const double i2 = warp_incl_scan(static_cast<double>(r2), lane);
+                    const double b2 = base + i2 - static_cast<double>(r2);
+                    const uint32_t hit2 = __ballot_sync(kFull, r2 > 0.f && b2 + static_cast<double>(r2) > T);
+                    const int l2 = hit2 ? __ffs(hit2) - 1 : 31 - __clz(__ballot_sync(kFull, r2 > 0.f) | 1u);
+                    int gs2 = -1;
+                    double cut2 = 1e300;
+                    if (lane == l2) {
+                        double acc = b2;
+                        for (int g = h0; g < h1; ++g) {
+                            const float wg = gweight(g);
+                            if (hit2 && acc + static_cast<double>(wg) > T) {
+                                gs2 = g;
+                                cut2 = T - acc;
+                                break;
+                            }
+                            acc += static_cast<double>(wg);
+                        }
+                        if (gs2 < 0) {  // rounding: last group of the lane with mass
+                            for (int g = h1 - 1; g >= h0; --g)
+                                if (gweight(g) > 0.f) {
+                                    gs2 = g;
+                                    break;
+                                }
+                            cut2 = 1e300;
+                        }
+                    }
+                    gstar = __shfl_sync(kFull, gs2, l2);
+                    cut = __shfl_sync(kFull, cut2, l2);
+                    if (gstar < 0) {
+                        gstar = a0;
+                        cut = 1e300;
+                    }
+                } else {
+                    // past the total only through rounding: last group with mass
+                    const int lp = static_cast<int>(__reduce_max_sync(kFull, static_cast<unsigned>(lastpos + 1)));
+                    gstar = lp > 0 ? lp - 1 : 0;
+                    cut = 1e300;
+                }
+                // element level: two tokens per lane, ascending
+                const int e0 = gstar * kGTok + 2 * lane;
+                float w[2] = {0.f, 0.f};
+#pragma unroll
+                for (int x = 0; x < 2; ++x) {
+                    const int e = e0 + x;
+                    if (e < V) {
+                        const float zt = load_logit<D>(trow, e);
+                        w[x] = pmode ? ex2(fmaf(zt, c, -Mc)) : resid_e(zt, load_logit<D>(drow, e), e);
+                    }
+                }
+                const double pairsum = static_cast<double>(w[0]) + static_cast<double>(w[1]);
+                const double ex = warp_incl_scan(pairsum, lane) - pairsum;
+                const double c0 = ex + static_cast<double>(w[0]);
+                const double c1 = c0 + static_cast<double>(w[1]);
+                const bool o0 = c0 > cut && e0 < V, o1 = c1 > cut && e0 + 1 < V;
+                const uint32_t over = __ballot_sync(kFull, o0 || o1);
+                const bool q0 = w[0] > 0.f && e0 < V, q1 = w[1] > 0.f && e0 + 1 < V;
+                const uint32_t pos = __ballot_sync(kFull, q0 || q1);
+                int pick;
+                if (over) {
+                    const int l = __ffs(over) - 1;
+                    const int first = __shfl_sync(kFull, o0 ? 0 : 1, l);
+                    pick = gstar * kGTok + 2 * l + first;
+                } else if (pos) {
+                    const int l = 31 - __clz(pos);
+                    const int last = __shfl_sync(kFull, q1 ? 1 : 0, l);
+                    pick = gstar * kGTok + 2 * l + last;
+                } else {
+                    pick = gstar * kGTok;
+                }
+                rec.tk = pick;
+            };
+
+            if (d.kind == kKindPair) {
+                float zs = 0.f;
+                for (int g = g0; g < g1; ++g) zs += gsum[g];
+                const float Z = warp_sum(zs);
+                if (Fk > 0) top_f(true);
+                if (do_verify) {
+                    if (Z > 0.f) {
+                        crossing(false, 0.f);
+                    } else {
+                        // no residual mass: draw from p at this row (group p-masses again)
+                        for (int g = g0; g < g1; ++g) {
+                            float m = -INFINITY;
+                            for (int i = 0; i < kGTok; ++i) {
+                                const int e = g * kGTok + i;
+                                if (e < V) m = fmaxf(m, load_logit<D>(trow, e));
+                            }
+                            float s2 = 0.f;
+                            if (m != -INFINITY) {
+                                for (int i = 0; i < kGTok; ++i) {
+                                    const int e = g * kGTok + i;
+                                    if (e < V) s2 += ex2(fmaf(load_logit<D>(trow, e), c, -m * c));
+                                }
+                            }
+                            gmax[g] = m;
+                            gsum[g] = s2;
+                        }
+                        __syncwarp();
+                        crossing(true, d.LT);
+                    }
+                }
+            } else if (d.kind == kKindGreedy) {
+                // argmax: the best group (lowest index on ties), then the lowest id in it
+                uint64_t gk = 0;
+                for (int g = g0; g < g1; ++g) {
+                    const uint64_t key = (static_cast<uint64_t>(ordered_bits(gmax[g])) << 32) |
+                                         static_cast<uint64_t>(0xFFFFFFFFu - static_cast<uint32_t>(g));
+                    gk = key > gk ? key : gk;
+                }
+                const uint64_t best = warp_max_u64(gk);
+                const float M = value_of_ordered(static_cast<uint32_t>(best >> 32));
+                const int gbest = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(best & 0xFFFFFFFFu));
+                if (M != M) {
+                    rec.flags |= SSD_DEV_NONFINITE;
+                } else {
+                    const int e0 = gbest * kGTok + 2 * lane;
+                    bool m0 = false, m1 = false;
+                    if (e0 < V && e0 != xmask) m0 = load_logit<D>(trow, e0) == M;
+                    if (e0 + 1 < V && e0 + 1 != xmask) m1 = load_logit<D>(trow, e0 + 1) == M;
+                    const uint32_t who = __ballot_sync(kFull, m0 || m1);
+                    int id = gbest * kGTok;
+                    if (who) {
+                        const int l = __ffs(who) - 1;
+                        id = gbest * kGTok + 2 * l + __shfl_sync(kFull, m0 ? 0 : 1, l);
+                    }
+                    rec.tk = id;
+                    if (k < K) {
+                        const float ztx = load_logit<D>(trow, xt);
+                        rec.accept = make_key(ztx, xt) > make_key(M, id) ? 1 : 0;
+                        rec.p_tok = rec.accept ? 1.f : 0.f;
+                        rec.q_tok = 1.f;
+                    }
+                    if (Fk > 0) top_f(false);
+                }
+            } else if (d.kind == kKindSampled) {
+                if (Fk > 0) top_f(false);
+                if (do_verify) crossing(true, d.M);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&gs.tail_empty[buf]);
+
+            // ---- publish the record; the last unit of b runs the epilogue ----
+            if (lane == 0) {
+                UnitRecord *Rr = P.rec + static_cast<int64_t>(b) * (K + 1) + k;
+                *Rr = rec;
+                if (rec.flags == 0 && rec.state == 1 && k < K && !rec.accept && (P.mode & kModeEarlyExit))
+                    atomicOr(P.seq_reject + b, 1u << k);
+            }
+            // the record and this warp's cache writes are visible before the unit is counted
+            __threadfence();
+            uint32_t done = 0;
+            if (lane == 0) done = atomicAdd(P.seq_count + b, 1u);
+            done = __shfl_sync(kFull, done, 0);
+            if (done != static_cast<uint32_t>(K)) continue;
+            __threadfence();
+            const UnitRecord *RR = P.rec + static_cast<int64_t>(b) * (K + 1);
+            int fl = 0, acc = 1, tk = -1;
+            float pt = NAN, qt = NAN;
+            if (lane < K) {
+                fl = __ldcg(&RR[lane].flags);
+                acc = __ldcg(&RR[lane].accept);
+                tk = __ldcg(&RR[lane].tk);
+                pt = __ldcg(&RR[lane].p_tok);
+                qt = __ldcg(&RR[lane].q_tok);
+            }
+            const int flK = __ldcg(&RR[K].flags);
+            const int tkK = __ldcg(&RR[K].tk);
+            fl = static_cast<int>(__reduce_or_sync(kFull, static_cast<unsigned>(fl))) | flK;
+            const uint32_t rej = __ballot_sync(kFull, lane < K && acc == 0);
+            const int a = rej ? __ffs(rej) - 1 : K;
+            const int tsh = __shfl_sync(kFull, tk, a & 31);
+            const int tstar = a == K ? tkK : tsh;
+            const bool bad = fl != 0 || tstar < 0;
+            if (do_verify) {
                 if (lane == 0) {
-                    if (fl && P.dev_status) atomicOr(P.dev_status, fl);
-                    P.seq_count[b] = 0;
-                    P.seq_reject[b] = 0;
+                    P.accept_len[b] = bad ? -1 : a;
+                    P.bonus[b] = bad ? -1 : tstar;
+                }
+                if (P.p_tok && lane < K) {
+                    const bool keep = !bad && lane <= a;
+                    P.p_tok[static_cast<int64_t>(b) * K + lane] = keep ? pt : NAN;
+                    P.q_tok[static_cast<int64_t>(b) * K + lane] = keep ? qt : NAN;
+                }
+                if (P.mode & kModeLookup) {
+                    int slot = -1;
+                    if (!bad) {
+                        const int32_t *row = P.cache_tok + static_cast<int64_t>(b) * P.budget;
+                        for (int j0 = P.off[a]; j0 < P.off[a + 1] && slot < 0; j0 += 32) {
+                            const int jj = j0 + lane;
+                            const bool m = jj < P.off[a + 1] && __ldcg(row + jj) == tstar;
+                            const uint32_t mm = __ballot_sync(kFull, m);
+                            if (mm) slot = j0 + __ffs(mm) - 1;
+                        }
+                    }
+                    if (lane == 0) {
+                        P.hit[b] = slot >= 0 ? 1 : 0;
+                        P.slot[b] = slot;
+                    }
                 }
             }
-            if (all) break;
-            if (progress) {
-                idle = 0;
-            } else {
-                if (++idle > (1 << 24)) {
-                    if (lane == 0 && P.dev_status) atomicOr(P.dev_status, SSD_DEV_TIMEOUT);
-                    break;
-                }
-                __nanosleep(64);
+            if (lane == 0) {
+                if (fl && P.dev_status) atomicOr(P.dev_status, fl);
+                P.seq_count[b] = 0;
+                P.seq_reject[b] = 0;
             }
         }
-        // this CTA is done; the last CTA of the grid resets the unit scheduler
+        // this tail warp is done; the last one of the grid resets the unit scheduler
         if (lane == 0) {
             __threadfence();
             const uint32_t done = atomicAdd(P.exit_counter, 1u);
-            if (done == gridDim.x - 1) {
+            if (done == gridDim.x * kNG - 1) {
                 *P.unit_counter = 0;
                 *P.exit_counter = 0;
             }
@@ -636,403 +898,199 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     // =========================== consumers ==================================
     const int grp = warp / kGW;
     GroupShared &gs = gsh[grp];
-    Scratch &sc = gs.sc;
-    GroupCtx gc{1 + grp, tid - grp * kGT, lane, warp - grp * kGW};
-    const int t = gc.t;
-    unsigned char *ring = dyn_smem + grp * kRS * kSB;
-    float *gmax = reinterpret_cast<float *>(dyn_smem + kNG * kRS * kSB) + grp * 2 * Gp;
-    float *gsum = gmax + Gp;
+    const int t = tid - grp * kGT;
+    const int gw = warp - grp * kGW;
+    const int bar_id = 1 + grp;
+    auto gbar = [&]() { asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "r"(kGT) : "memory"); };
+    unsigned char *const ring = dyn_smem + grp * kRS * kSB;
+    float *const arrays = reinterpret_cast<float *>(dyn_smem + kNG * kRS * kSB) + grp * kNBuf * 2 * Gp;
 
-    int64_t n = 0;  // stages consumed
+    // per-thread stage geometry (fixed for the whole launch)
+    const int p1_row = t / (kGT / 2), p1_tr = t % (kGT / 2);
+    const int p1_vbase = p1_tr * VPT1, p1_rot = (p1_tr >> 1) & 3;
+    const int s_gl = t / TPGS, s_part = t % TPGS;
+    const int s_vbase = s_gl * GV + s_part * VPTS, s_rot = (t >> 1) & 3;
+    const int r_gl = t / TPG2, r_part = t % TPG2;
+    const int r_vbase = r_gl * GV + r_part * VPT2, r_rot = (t >> 2) & 1;
+
+    uint32_t n = 0;    // stages consumed
+    uint32_t nho = 0;  // hand-offs to the tail warp
     int cur = -1;
-    int b = 0, k = 0, xt = -1, flags = 0, Fk = 0, xmask = -1;
-    bool greedy = false, sampled = false, pair = false, rowK = false, active = false;
-    float c = 0.f;
-    DraftShape shape{false, 0.f, 0, 0.f};
-    const unsigned char *trow = nullptr, *drow = nullptr;
-    Stat st_d{-INFINITY, 0.f};
-    Stat gT{-INFINITY, 0.f}, gD{-INFINITY, 0.f};
-    float LT = 0.f, LD = 0.f;
-    float ztx = 0.f, zdx = 0.f, u_k = 0.f;
-    UnitRecord rec{};
+    int b = 0, k = 0, flags = 0, xt = -1, xmask = -1;
+    bool sampled = false, pair = false, active = false, want_p2 = false;
+    float c = 0.f, LT = 0.f, LD = 0.f;
+    DraftShape shape{0, 0.f, 0, 0.f};
+    Stat st{-INFINITY, 0.f};
+    float *gmax = arrays, *gsum = arrays + Gp;
+    // thread 0: the accept test's gathers and results
+    float ztx = 0.f, zdx = 0.f, u_k = 0.f, p_tok = NAN, q_tok = NAN;
+    int accept = 0;
 
-    auto resid_e = [&](float zp, float zq, int e) -> float {
-        return resid_of(zp, zq, c, -LT, draft_bias(shape, zq, e) - LD);
-    };
-
-    // normaliser of the target row from the group arrays
-    auto target_stats = [&]() -> Stat {
-        uint32_t mo = 0;
-        for (int g = t; g < G; g += kGT) {
-            const uint32_t o = ordered_bits(gmax[g]);
-            mo = o > mo ? o : mo;
-        }
-        const float M = value_of_ordered(g_max_u32(gc, mo, sc));
-        const float Mc = M * c;
-        float s = 0.f;
-        if (M == M && M != -INFINITY) {
-            for (int g = t; g < G; g += kGT) {
-                const float gm = gmax[g];
-                if (gm != -INFINITY) s += gsum[g] * ex2(gm * c - Mc);
-            }
-        }
-        return Stat{Mc, g_sum_f32(gc, s, sc)};
-    };
-
-    // top-F_k of the unit into its cache segment (gmax: per-group maxima of the
-    // scores -- residuals for pairs, raw logits otherwise)
-    auto top_f = [&]() {
-        uint32_t tv = 0;
-        for (int g = t; g < G; g += kGT) {
-            const uint32_t o = ordered_bits(gmax[g]);
-            tv = o > tv ? o : tv;
-        }
-        const uint32_t theta_u0 = g_fth_largest(gc, tv, Fk, gs.tops, sc);
-        uint64_t theta = static_cast<uint64_t>(theta_u0) << 32;
+    // hands the unit to the tail warp (the barrier orders every thread's array writes first)
+    auto handoff = [&](int hk, int state, float M, float Ssum) {
+        gbar();
         if (t == 0) {
-            sc.i[0] = 0;
-            sc.i[1] = 0;
+            TailDesc &D0 = gs.desc[nho & 1];
+            D0.kind = hk;
+            D0.b = b;
+            D0.k = k;
+            D0.flags = flags;
+            D0.state = state;
+            D0.accept = accept;
+            D0.xt = xt;
+            D0.c = c;
+            D0.M = M;
+            D0.S = Ssum;
+            D0.LT = LT;
+            D0.LD = LD;
+            D0.p_tok = p_tok;
+            D0.q_tok = q_tok;
+            D0.shape = shape;
+            mbar_arrive(&gs.tail_full[nho & 1]);
         }
-        gbar(gc);
-        for (int g = t; g < G; g += kGT) {
-            if (ordered_bits(gmax[g]) >= theta_u0) {
-                const int idx = atomicAdd(&sc.i[0], 1);
-                if (idx < kCandGroupsCap) gs.cgroups[idx] = g;
-            }
-        }
-        gbar(gc);
-        const int ncg = sc.i[0];
-        const bool all_groups = ncg > kCandGroupsCap;
-        const int ngroups = all_groups ? G : ncg;
-        int count = 0;
-        for (int round = 0; round < 64; ++round) {
-            for (int q = gc.warp; q < ngroups; q += kGW) {
-                const int g = all_groups ? q : gs.cgroups[q];
-                const int e = g * kGroupTokens + lane;
-                bool has = false;
-                uint64_t key = 0;
-                if (e < V) {
-                    const float zt = load_logit<D>(trow, e);
-                    if (pair)
-                        key = make_key(resid_e(zt, load_logit<D>(drow, e), e), e);
-                    else
-                        key = (e == xmask) ? excluded_key(e) : make_key(zt, e);
-                    has = key >= theta;
-                }
-                if (has) {
-                    const int idx = atomicAdd(&sc.i[1], 1);
-                    if (idx < kCandCap) gs.cand[idx] = key;
-                }
-            }
-            gbar(gc);
-            count = sc.i[1];
-            if (count <= kCandCap) break;
-            // overflow: raise theta to the F-th largest of the stored keys
-            for (int kk = 2; kk <= kCandCap; kk <<= 1) {
-                for (int j = kk >> 1; j > 0; j >>= 1) {
-                    for (int i = t; i < kCandCap; i += kGT) {
-                        const int ixj = i ^ j;
-                        if (ixj > i) {
-                            const uint64_t a = gs.cand[i], cc2 = gs.cand[ixj];
-                            const bool desc = (i & kk) == 0;
-                            if (desc ? (a < cc2) : (a > cc2)) {
-                                gs.cand[i] = cc2;
-                                gs.cand[ixj] = a;
-                            }
-                        }
-                    }
-                    gbar(gc);
-                }
-            }
-            theta = gs.cand[Fk - 1];
-            gbar(gc);
-            if (t == 0) sc.i[1] = 0;
-            gbar(gc);
-        }
-        if (count > kCandCap) count = kCandCap;
-        // rank by counting; ranks below F go straight to the cache row
-        for (int i = t; i < count; i += kGT) {
-            const uint64_t key = gs.cand[i];
-            int rr = 0;
-            for (int j = 0; j < count; ++j) rr += gs.cand[j] > key ? 1 : 0;
-            if (rr < Fk) {
-                P.cache_tok[static_cast<int64_t>(b) * P.budget + P.off[k] + rr] = key_id(key);
-            }
-        }
-        gbar(gc);
-    };
-
-    // inverse-CDF bonus at u_K over ascending token id; per-group weights from
-    // gsum (residual masses) or, when `pmode`, p-masses gsum * 2^(gmax c - Mc)
-    auto crossing = [&](bool pmode, float Mc) {
-        const int R = (G + kGT - 1) / kGT;
-        const int g0 = min(G, t * R), g1 = min(G, g0 + R);
-        auto gweight = [&](int g) -> float {
-            if (!pmode) return gsum[g];
-            const float gm = gmax[g];
-            return (gm == -INFINITY) ? 0.f : gsum[g] * ex2(gm * c - Mc);
-        };
-        float run = 0.f;
-        for (int g = g0; g < g1; ++g) run += gweight(g);
-        double incl = static_cast<double>(run);
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const double y = __shfl_up_sync(kFull, incl, o);
-            if (lane >= o) incl += y;
-        }
-        gbar(gc);
-        if (lane == 31) sc.d[gc.warp] = incl;
-        if (t == 0) sc.i[2] = kGT;
-        gbar(gc);
-        double base = 0.0, tot = 0.0;
-        for (int w = 0; w < kGW; ++w) {
-            if (w < gc.warp) base += sc.d[w];
-            tot += sc.d[w];
-        }
-        const double T = static_cast<double>(P.uniforms[static_cast<int64_t>(b) * (K + 1) + K]) * tot;
-        const double before = base + incl - static_cast<double>(run);
-        if (run > 0.f && before + static_cast<double>(run) > T) atomicMin(&sc.i[2], t);
-        gbar(gc);
-        const int tstar = sc.i[2];
-        if (t == tstar) {
-            double acc = before;
-            int gstar = g1 - 1;
-            double cut = 0.0;
-            for (int g = g0; g < g1; ++g) {
-                const float wg = gweight(g);
-                if (acc + static_cast<double>(wg) > T) {
-                    gstar = g;
-                    cut = T - acc;
-                    break;
-                }
-                acc += static_cast<double>(wg);
-            }
-            sc.i[3] = gstar;
-            sc.cut = cut;
-        }
-        if (tstar == kGT) {  // past the total only through rounding: last group with mass
-            uint32_t lastg = 0;
-            for (int g = t; g < G; g += kGT)
-                if (gweight(g) > 0.f) lastg = static_cast<uint32_t>(g + 1);
-            const uint32_t lg = g_max_u32(gc, lastg, sc);
-            if (t == 0) {
-                sc.i[3] = lg > 0 ? static_cast<int>(lg) - 1 : 0;
-                sc.cut = 1e300;
-            }
-        }
-        gbar(gc);
-        if (gc.warp == 0) {
-            const int g = sc.i[3];
-            const double cut = sc.cut;
-            const int e = g * kGroupTokens + lane;
-            float w = 0.f;
-            if (e < V) {
-                const float zt = load_logit<D>(trow, e);
-                w = pmode ? ex2(fmaf(zt, c, -Mc)) : resid_e(zt, load_logit<D>(drow, e), e);
-            }
-            double cum = static_cast<double>(w);
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const double y = __shfl_up_sync(kFull, cum, o);
-                if (lane >= o) cum += y;
-            }
-            const uint32_t over = __ballot_sync(kFull, cum > cut && e < V);
-            const uint32_t pos = __ballot_sync(kFull, w > 0.f && e < V);
-            int pick;
-            if (over)
-                pick = g * kGroupTokens + __ffs(over) - 1;
-            else if (pos)
-                pick = g * kGroupTokens + 31 - __clz(pos);
-            else
-                pick = g * kGroupTokens;
-            if (lane == 0) sc.bid = pick;
-        }
-        gbar(gc);
-        if (t == 0) rec.tk = sc.bid;
-    };
-
-    uint32_t nfin = 0;  // entries handed to the finisher (uniform in the group)
-    auto push_fin = [&](int stop) {
-        if (t == 0) {
-            const uint32_t qi = nfin % kFinQ;
-            if (mbar_wait_bounded(&gs.fin_empty[qi], ((nfin / kFinQ) & 1) ^ 1)) {
-                FinEntry &E = gs.fin[qi];
-                E.rec = rec;
-                E.b = b;
-                E.k = k;
-                E.stop = stop;
-                mbar_arrive(&gs.fin_full[qi]);
-            } else {
-                atomicOr(&s_abort, 1);
-                if (P.dev_status) atomicOr(P.dev_status, SSD_DEV_TIMEOUT);
-            }
-        }
-        ++nfin;
-    };
-    // the unit is complete: hand its record to the finisher (the barrier orders
-    // every thread's cache writes before the hand-off)
-    auto finish_unit = [&]() {
-        gbar(gc);
-        push_fin(0);
+        ++nho;
     };
 
     for (;;) {
-        const int s = static_cast<int>(n % kRS);
-        const uint32_t par = static_cast<uint32_t>((n / kRS) & 1);
-        if (!mbar_wait_bounded(&gs.full_bar[s], par)) {
+        const int s = static_cast<int>(n & (kRS - 1));
+        if (!mbar_wait_bounded(&gs.full_bar[s], (n / kRS) & 1)) {
             atomicOr(&s_abort, 1);
             if (t == 0 && P.dev_status) atomicOr(P.dev_status, SSD_DEV_TIMEOUT);
             break;
         }
         const Hdr h = gs.hdr[s];
-        if (h.pass == kPassStop) break;
+        const int pass = h.code & 15;
+        if (pass == kPassStop) break;
         if (h.unit != cur) {
-            // a new unit: per-unit constants (identical in every thread of the group)
+            // a new unit: wait for its group-array buffer, then per-unit constants
+            if (!mbar_wait_bounded(&gs.tail_empty[nho & 1], ((nho >> 1) & 1) ^ 1)) {
+                atomicOr(&s_abort, 1);
+                if (t == 0 && P.dev_status) atomicOr(P.dev_status, SSD_DEV_TIMEOUT);
+                break;
+            }
             cur = h.unit;
             k = h.k;
             b = h.b;
+            gmax = arrays + (nho & 1) * 2 * Gp;
+            gsum = gmax + Gp;
             const float tau = P.temperature[b];
             const bool tau_ok = (tau >= 0.f) && (tau < INFINITY);
-            greedy = tau_ok && tau == 0.f;
+            const bool greedy = tau_ok && tau == 0.f;
             sampled = tau_ok && tau > 0.f;
-            rowK = (k == K);
-            pair = sampled && !rowK;
+            pair = sampled && k < K;
             flags = tau_ok ? 0 : SSD_DEV_BAD_TEMPERATURE;
             xt = -1;
-            if (!rowK) {
+            if (k < K) {
                 xt = P.tokens[static_cast<int64_t>(b) * K + k];
                 if (xt < 0 || xt >= V) flags |= SSD_DEV_BAD_TOKEN;
             }
-            xmask = (greedy && !rowK) ? xt : -1;
-            Fk = do_cache ? P.F[k] : 0;
+            xmask = (greedy && k < K) ? xt : -1;
             active = flags == 0;
+            want_p2 = pair && (do_verify || (do_cache && P.F[k] > 0));
             c = sampled ? kLog2e / tau : 0.f;
-            shape = DraftShape{false, 0.f, 0, 0.f};
+            shape = DraftShape{0, 0.f, 0, 0.f};
             if (pair && P.reshape) {
-                const ssd_reshape_desc d = P.reshape[static_cast<int64_t>(b) * K + k];
-                shape.on = d.F > 0;
-                shape.thr = d.thr_val;
-                shape.thr_id = d.thr_id;
-                shape.l2C = d.C > 0.f ? (d.C == 1.f ? 0.f : lg2(d.C)) : -INFINITY;
+                const ssd_reshape_desc dd = P.reshape[static_cast<int64_t>(b) * K + k];
+                shape.on = dd.F > 0;
+                shape.thr = dd.thr_val;
+                shape.thr_id = dd.thr_id;
+                shape.l2C = dd.C > 0.f ? (dd.C == 1.f ? 0.f : lg2(dd.C)) : -INFINITY;
             }
-            trow = static_cast<const unsigned char *>(P.tgt) +
-                   (static_cast<int64_t>(b) * P.tgt_seq_stride + static_cast<int64_t>(k) * V) * S;
-            drow = pair ? static_cast<const unsigned char *>(P.drf) +
-                              (static_cast<int64_t>(b) * P.drf_seq_stride + static_cast<int64_t>(k) * V) * S
-                        : nullptr;
-            st_d = Stat{-INFINITY, 0.f};
-            rec = UnitRecord{};
-            rec.tk = -1;
-            rec.p_tok = NAN;
-            rec.q_tok = NAN;
-            rec.state = 1;
-            if (t == 0 && active && !rowK) {
+            st = Stat{-INFINITY, 0.f};
+            LT = 0.f;
+            LD = 0.f;
+            p_tok = NAN;
+            q_tok = NAN;
+            accept = 0;
+            if (t == 0 && active && pair) {
+                const unsigned char *trow = static_cast<const unsigned char *>(P.tgt) +
+                                            (static_cast<int64_t>(b) * P.tgt_seq_stride + static_cast<int64_t>(k) * V) * S;
+                const unsigned char *drow = static_cast<const unsigned char *>(P.drf) +
+                                            (static_cast<int64_t>(b) * P.drf_seq_stride + static_cast<int64_t>(k) * V) * S;
                 ztx = load_logit<D>(trow, xt);
-                if (pair) {
-                    zdx = load_logit<D>(drow, xt);
-                    u_k = P.uniforms ? P.uniforms[static_cast<int64_t>(b) * (K + 1) + k] : 0.f;
-                }
+                zdx = load_logit<D>(drow, xt);
+                u_k = P.uniforms ? P.uniforms[static_cast<int64_t>(b) * (K + 1) + k] : 0.f;
             }
         }
-        const unsigned char *st = ring + s * kSB;
-        if (h.pass == kPassSkip) {
+        if (pass == kPassSkip) {
             __syncwarp();
             if (lane == 0) mbar_arrive(&gs.empty_bar[s]);
             ++n;
-            rec.state = 2;
-            rec.flags = flags;
-            finish_unit();
+            handoff(kKindPass, 2, 0.f, 0.f);
             continue;
         }
+        const unsigned char *stg = ring + s * kSB;
+        const bool stage_pair = (h.code >> 5) & 1;
 
         // ---- stage processing -----------------------------------------------
         if (active) {
-            if (h.pass == kPassStats && h.pair) {
-                // threads [0, kGT/2) take target groups, the rest draft groups
-                const int row = t / (kGT / 2);
-                const int tr = t - row * (kGT / 2);
-                const int gl = tr / TPG1, part = tr % TPG1;
+            if (pass == kPassStats && stage_pair) {
+                // online statistics: threads [0, 128) target, the rest draft
                 uint4 w[VPT1];
-                load_vecs<D, VPT1>(st + row * HALF, gl * GV + part * VPT1, h.nvec, (tr >> 1) & 3, w);
-                const int g = h.chunk * GPR + gl;
-                if (row == 0 || !shape.on) {
-                    const float gm = tpg_max_nan<TPG1>(vecs_max<D, VPT1>(w));
-                    float vs = 0.f;
-                    if (gm != -INFINITY) vs = vecs_expsum<D, VPT1>(w, c, gm * c);
-                    const float gsv = tpg_sum<TPG1>(vs);
-                    if (part == 0) {
-                        if (row == 0) {
-                            if (g < G) {
-                                gmax[g] = gm;
-                                gsum[g] = gsv;
-                            }
-                        } else if (gm != -INFINITY) {
-                            st_d = (gm == gm) ? stat_merge(st_d, Stat{gm * c, gsv}) : Stat{NAN, NAN};
-                        }
-                    }
+                load_vecs<D, VPT1>(stg + p1_row * HALF, p1_vbase, h.nvec, p1_rot, h.nvec == FULL_PAIR, w);
+                if (p1_row == 0 || !shape.on) {
+                    const float xm = vecs_max<D, VPT1>(w) * c;
+                    stat_fold(st, xm, [&](float mn) { return vecs_expsum<D, VPT1>(w, c, mn); });
                 } else {
-                    // reshaped draft: weights 2^(z c + log2 c_t), maximum over weighted values
-                    const int e0 = h.chunk * GPR * kGroupTokens + (gl * GV + part * VPT1) * VEC;
+                    // reshaped draft: weights 2^(z c + log2 c_t)
+                    const int e0 = h.chunk * (FULL_PAIR * VEC) + p1_vbase * VEC;
                     float x[VPT1][VEC];
                     float xm = -INFINITY;
 #pragma unroll
                     for (int kk = 0; kk < VPT1; ++kk) {
                         float z[VEC];
                         decode_vec<D>(w[kk], z);
-                        const int ev = e0 + ((kk + ((tr >> 1) & 3)) & (VPT1 - 1)) * VEC;
+                        const int ev = e0 + ((kk + p1_rot) & (VPT1 - 1)) * VEC;
 #pragma unroll
                         for (int i = 0; i < VEC; ++i) {
                             x[kk][i] = z[i] * c + draft_bias(shape, z[i], ev + i);
                             xm = fmax_nan(xm, x[kk][i]);
                         }
                     }
-                    const float gxm = tpg_max_nan<TPG1>(xm);
-                    float vs = 0.f;
-                    if (gxm != -INFINITY) {
+                    stat_fold(st, xm, [&](float mn) {
+                        float vs = 0.f;
 #pragma unroll
                         for (int kk = 0; kk < VPT1; ++kk)
 #pragma unroll
-                            for (int i = 0; i < VEC; ++i) vs += ex2(x[kk][i] - gxm);
-                    }
-                    const float gsv = tpg_sum<TPG1>(vs);
-                    if (part == 0 && gxm != -INFINITY)
-                        st_d = (gxm == gxm) ? stat_merge(st_d, Stat{gxm, gsv}) : Stat{NAN, NAN};
+                            for (int i = 0; i < VEC; ++i) vs += ex2(x[kk][i] - mn);
+                        return vs;
+                    });
                 }
-            } else if (h.pass == kPassStats) {
-                // one row: sampled row K (max + mass) or greedy (max, drafted token excluded)
-                const int gl = t / TPGS, part = t % TPGS;
-                const int vbase = gl * GV + part * VPTS;
+            } else if (pass == kPassStats) {
+                // one row: sampled row K (maxima, masses, statistics) or greedy (maxima,
+                // drafted token excluded)
                 uint4 w[VPTS];
-                load_vecs<D, VPTS>(st, vbase, h.nvec, (t >> 1) & 3, w);
-                const int e0 = h.chunk * GPS * kGroupTokens + vbase * VEC;
+                load_vecs<D, VPTS>(stg, s_vbase, h.nvec, s_rot, h.nvec == FULL_ONE, w);
+                const int e0 = h.chunk * (FULL_ONE * VEC) + s_vbase * VEC;
                 if (static_cast<unsigned>(xmask - e0) < static_cast<unsigned>(VPTS * VEC)) {
 #pragma unroll
                     for (int kk = 0; kk < VPTS; ++kk) {
-                        const int ev = e0 + ((kk + ((t >> 1) & 3)) & (VPTS - 1)) * VEC;
+                        const int ev = e0 + ((kk + s_rot) & (VPTS - 1)) * VEC;
                         if (static_cast<unsigned>(xmask - ev) < static_cast<unsigned>(VEC))
                             mask_vec<D>(w[kk], ev, 0, V, xmask);
                     }
                 }
                 const float gm = tpg_max_nan<TPGS>(vecs_max<D, VPTS>(w));
-                float gsv = 0.f;
+                const int g = h.chunk * GPS + s_gl;
                 if (sampled) {
-                    float vs = 0.f;
-                    if (gm != -INFINITY) vs = vecs_expsum<D, VPTS>(w, c, gm * c);
-                    gsv = tpg_sum<TPGS>(vs);
-                }
-                const int g = h.chunk * GPS + gl;
-                if (part == 0 && g < G) {
+                    const float vs = (gm != -INFINITY) ? vecs_expsum<D, VPTS>(w, c, gm * c) : 0.f;
+                    const float gsv = tpg_sum<TPGS>(vs);
+                    if (s_part == 0) {
+                        if (gm != -INFINITY) st = (gm == gm) ? stat_merge_nan(st, Stat{gm * c, gsv}) : Stat{NAN, NAN};
+                        if (g < G) {
+                            gmax[g] = gm;
+                            gsum[g] = gsv;
+                        }
+                    }
+                } else if (s_part == 0 && g < G) {
                     gmax[g] = gm;
-                    gsum[g] = gsv;
                 }
             } else {
                 // pass 2 (pair): residual masses and maxima per group
-                const int gl = t / TPG2, part = t % TPG2;
-                const int vbase = gl * GV + part * VPT2;
-                const int rot = (t >> 2) & 1;
                 uint4 wt[VPT2], wd[VPT2];
-                load_vecs<D, VPT2>(st, vbase, h.nvec, rot, wt);
-                load_vecs<D, VPT2>(st + HALF, vbase, h.nvec, rot, wd);
+                const bool full = h.nvec == FULL_PAIR;
+                load_vecs<D, VPT2>(stg, r_vbase, h.nvec, r_rot, full, wt);
+                load_vecs<D, VPT2>(stg + HALF, r_vbase, h.nvec, r_rot, full, wd);
                 float2 acc = make_float2(0.f, 0.f);
                 float mx = 0.f;
                 if (!shape.on) {
@@ -1046,35 +1104,36 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                         for (int i = 0; i < VEC; i += 2) {
                             const float2 x0 = __ffma2_rn(make_float2(zt[i], zd[i]), cc, nl);
                             const float2 x1 = __ffma2_rn(make_float2(zt[i + 1], zd[i + 1]), cc, nl);
-                            const float2 d = __ffma2_rn(make_float2(ex2(x0.y), ex2(x1.y)),
-                                                        make_float2(-1.f, -1.f),
-                                                        make_float2(ex2(x0.x), ex2(x1.x)));
-                            const float w0 = fmaxf(d.x, 0.f), w1 = fmaxf(d.y, 0.f);
+                            const float2 dd = __ffma2_rn(make_float2(ex2(x0.y), ex2(x1.y)),
+                                                         make_float2(-1.f, -1.f),
+                                                         make_float2(ex2(x0.x), ex2(x1.x)));
+                            const float w0 = fmaxf(dd.x, 0.f), w1 = fmaxf(dd.y, 0.f);
                             acc = __fadd2_rn(acc, make_float2(w0, w1));
                             mx = fmaxf(mx, fmaxf(w0, w1));
                         }
                     }
                 } else {
-                    const int e0 = h.chunk * GPR * kGroupTokens + vbase * VEC;
+                    const int e0 = h.chunk * (FULL_PAIR * VEC) + r_vbase * VEC;
 #pragma unroll
                     for (int kk = 0; kk < VPT2; ++kk) {
                         float zt[VEC], zd[VEC];
                         decode_vec<D>(wt[kk], zt);
                         decode_vec<D>(wd[kk], zd);
-                        const int ev = e0 + ((kk + rot) & (VPT2 - 1)) * VEC;
+                        const int ev = e0 + ((kk + r_rot) & (VPT2 - 1)) * VEC;
 #pragma unroll
                         for (int i = 0; i < VEC; ++i) {
-                            const float wv = resid_e(zt[i], zd[i], ev + i);
+                            const float wv =
+                                resid_of(zt[i], zd[i], c, -LT, draft_bias(shape, zd[i], ev + i) - LD);
                             acc.x += wv;
                             mx = fmaxf(mx, wv);
                         }
                     }
                 }
                 const float gsv = tpg_sum<TPG2>(acc.x + acc.y);
-                const float gm = tpg_max<TPG2>(mx);
-                const int g = h.chunk * GPR + gl;
-                if (part == 0 && g < G) {
-                    gmax[g] = gm;
+                const float gmx = tpg_max<TPG2>(mx);
+                const int g = h.chunk * GPR + r_gl;
+                if (r_part == 0 && g < G) {
+                    gmax[g] = gmx;
                     gsum[g] = gsv;
                 }
             }
@@ -1082,122 +1141,71 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&gs.empty_bar[s]);
         ++n;
-        if (!h.last) continue;
+        if (!((h.code >> 4) & 1)) continue;
 
-        // ---- end of a pass: the unit's tail ----------------------------------
-        gbar(gc);  // group arrays complete
-        rec.flags = flags;
-        const bool want_p2 = pair && (do_verify || Fk > 0);
+        // ---- end of a pass ------------------------------------------------------
         if (!active) {
-            if (h.pass == kPassResid || !want_p2) finish_unit();
+            // an inactive pair still receives its second pass; hand off after it
+            if (pass == kPassResid || !want_p2) handoff(kKindPass, 1, 0.f, 0.f);
             continue;
         }
-        if (h.pass == kPassStats && sampled) {
-            gT = target_stats();
-            if (pair) gD = g_stat(gc, st_d, sc);
-            const bool okT = (gT.m < INFINITY) && (gT.S > 0.f) && (gT.S < INFINITY);
-            const bool okD = !pair || ((gD.m < INFINITY) && (gD.S > 0.f) && (gD.S < INFINITY));
-            if (!okT || !okD) {
+        if (pass == kPassStats && pair) {
+            // normalisers: warps 0-3 hold the target statistics, 4-7 the draft's
+            const Stat ws = warp_stat(st);
+            gbar();
+            if (lane == 0) gs.red[gw] = ws;
+            gbar();
+            Stat gT = gs.red[0], gD = gs.red[kGW / 2];
+#pragma unroll
+            for (int w = 1; w < kGW / 2; ++w) {
+                gT = stat_merge_nan(gT, gs.red[w]);
+                gD = stat_merge_nan(gD, gs.red[kGW / 2 + w]);
+            }
+            if (!stat_ok(gT) || !stat_ok(gD)) {
                 flags |= SSD_DEV_NONFINITE;
-                rec.flags = flags;
                 active = false;
-                if (!want_p2) finish_unit();
+                if (!want_p2) handoff(kKindPass, 1, 0.f, 0.f);
                 continue;
             }
             LT = gT.m + lg2(gT.S);
-            LD = pair ? gD.m + lg2(gD.S) : 0.f;
-            if (pair && t == 0) {
-                const float p = ex2(ztx * c - gT.m) / gT.S;
-                const float q = ex2(zdx * c + draft_bias(shape, zdx, xt) - gD.m) / gD.S;
-                rec.p_tok = p;
-                rec.q_tok = q;
-                rec.accept = (u_k * q < p) ? 1 : 0;
-            }
-            if (pair) {
-                if (!want_p2) finish_unit();
-                continue;
-            }
-            if (Fk > 0) top_f();
-            if (do_verify) crossing(true, gT.m);
-            finish_unit();
-            continue;
-        }
-        if (h.pass == kPassStats && greedy) {
-            uint64_t gk = 0;
-            for (int g = t; g < G; g += kGT) {
-                const uint64_t key = (static_cast<uint64_t>(ordered_bits(gmax[g])) << 32) |
-                                     static_cast<uint64_t>(0xFFFFFFFFu - static_cast<uint32_t>(g));
-                gk = key > gk ? key : gk;
-            }
-            const uint64_t best = g_max_u64(gc, gk, sc);
-            const float M = value_of_ordered(static_cast<uint32_t>(best >> 32));
-            const int gbest = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(best & 0xFFFFFFFFu));
-            if (M != M) {
-                flags |= SSD_DEV_NONFINITE;
-                rec.flags = flags;
-                finish_unit();
-                continue;
-            }
-            if (gc.warp == 0) {
-                const int e = gbest * kGroupTokens + lane;
-                bool m = false;
-                if (e < V && e != xmask) m = load_logit<D>(trow, e) == M;
-                const uint32_t who = __ballot_sync(kFull, m);
-                const int id = who ? gbest * kGroupTokens + __ffs(who) - 1 : gbest * kGroupTokens;
-                if (lane == 0) {
-                    sc.bkey = make_key(M, id);
-                    sc.bid = id;
-                }
-            }
-            gbar(gc);
+            LD = gD.m + lg2(gD.S);
             if (t == 0) {
-                rec.tk = sc.bid;
-                if (!rowK) {
-                    rec.accept = make_key(ztx, xt) > sc.bkey ? 1 : 0;
-                    rec.p_tok = rec.accept ? 1.f : 0.f;
-                    rec.q_tok = 1.f;
-                }
+                p_tok = ex2(ztx * c - gT.m) / gT.S;
+                q_tok = ex2(zdx * c + draft_bias(shape, zdx, xt) - gD.m) / gD.S;
+                accept = (u_k * q_tok < p_tok) ? 1 : 0;
             }
-            if (Fk > 0) top_f();
-            finish_unit();
+            if (!want_p2) handoff(kKindPass, 1, 0.f, 0.f);
             continue;
         }
-        // end of pass 2 (pair): residual mass, cache, bonus
-        {
-            float zs = 0.f;
-            for (int g = t; g < G; g += kGT) zs += gsum[g];
-            const float Z = g_sum_f32(gc, zs, sc);
-            if (Fk > 0) top_f();
-            if (do_verify) {
-                if (Z > 0.f) {
-                    crossing(false, 0.f);
-                } else {
-                    // no residual mass: draw from p at this row (group p-masses again)
-                    for (int g = t; g < G; g += kGT) {
-                        float m = -INFINITY;
-                        for (int i = 0; i < kGroupTokens; ++i) {
-                            const int e = g * kGroupTokens + i;
-                            if (e < V) m = fmaxf(m, load_logit<D>(trow, e));
-                        }
-                        float s2 = 0.f;
-                        for (int i = 0; i < kGroupTokens; ++i) {
-                            const int e = g * kGroupTokens + i;
-                            if (e < V) s2 += ex2(fmaf(load_logit<D>(trow, e), c, -m * c));
-                        }
-                        gmax[g] = m;
-                        gsum[g] = s2;
-                    }
-                    gbar(gc);
-                    crossing(true, gT.m);
-                }
+        if (pass == kPassStats && sampled) {
+            // sampled single row: target statistics for the tail's p-masses
+            const Stat ws = warp_stat(st);
+            gbar();
+            if (lane == 0) gs.red[gw] = ws;
+            gbar();
+            Stat gT = gs.red[0];
+#pragma unroll
+            for (int w = 1; w < kGW; ++w) gT = stat_merge_nan(gT, gs.red[w]);
+            if (!stat_ok(gT)) {
+                flags |= SSD_DEV_NONFINITE;
+                handoff(kKindPass, 1, 0.f, 0.f);
+                continue;
             }
-            finish_unit();
+            handoff(kKindSampled, 1, gT.m, gT.S);
+            continue;
         }
+        if (pass == kPassStats) {
+            handoff(kKindGreedy, 1, 0.f, 0.f);
+            continue;
+        }
+        handoff(kKindPair, 1, 0.f, 0.f);
     }
 
-    // this group is done
-    gbar(gc);
-    push_fin(1);
+    // this group is done: tell its tail warp
+    if (!mbar_wait_bounded(&gs.tail_empty[nho & 1], ((nho >> 1) & 1) ^ 1)) {
+        if (t == 0 && P.dev_status) atomicOr(P.dev_status, SSD_DEV_TIMEOUT);
+    }
+    handoff(kKindStop, 0, 0.f, 0.f);
 }
 
 int stream_setup(int dtype, size_t optin, size_t *max_dyn) {

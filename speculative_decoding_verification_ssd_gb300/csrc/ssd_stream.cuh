@@ -8,20 +8,20 @@ namespace ssd {
 
 constexpr int kStreamGroups = 2;       // consumer groups, each with its own ring
 constexpr int kStreamGroupWarps = 8;   // warps per consumer group
-// consumer warps, then one producer warp per ring, then one finisher warp
-constexpr int kStreamThreads = kStreamGroups * kStreamGroupWarps * 32 + kStreamGroups * 32 + 32;
+// consumer warps, then one producer warp per ring, then one tail warp per group
+constexpr int kStreamThreads = kStreamGroups * kStreamGroupWarps * 32 + 2 * kStreamGroups * 32;
 constexpr int kStreamRingStages = 4;   // stages per ring
 constexpr int kStreamStageBytes = 16384;
-constexpr int kGroupTokens = 32;
+constexpr int kGroupTokens = 64;  // tokens per group of the per-group arrays
 
 // Dynamic shared memory of the streaming kernel for a vocabulary of V tokens:
-// the stage rings plus, per consumer group, two float arrays with one entry per
-// 32-token group.
+// the stage rings plus, per consumer group, two buffers of two float arrays
+// with one entry per 64-token group.
 inline size_t stream_dyn_bytes(int V) {
     const size_t G = (static_cast<size_t>(V) + kGroupTokens - 1) / kGroupTokens;
     const size_t Gp = (G + 31) & ~static_cast<size_t>(31);
     return static_cast<size_t>(kStreamGroups) *
-           (static_cast<size_t>(kStreamRingStages) * kStreamStageBytes + 2 * Gp * sizeof(float));
+           (static_cast<size_t>(kStreamRingStages) * kStreamStageBytes + 2 * 2 * Gp * sizeof(float));
 }
 
 struct UnitParams;
