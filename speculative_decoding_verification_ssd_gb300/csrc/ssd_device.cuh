@@ -76,6 +76,35 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
 
 // Waits for phase `parity` of `bar` with a bounded number of polls.  Returns
 // false if the limit ran out (the caller records SSD_DEV_TIMEOUT).
+// Waits for phase `parity` of `bar` with the thread suspended in hardware
+// between polls (each poll sleeps up to kSuspendHintNs or until the phase
+// completes); gives up after kSuspendPolls polls (a few seconds) and returns
+// false.  The loop lives in one asm block, so the compiler sees no divergent
+// branch around it.
+constexpr uint32_t kSuspendHintNs = 500000;
+constexpr uint32_t kSuspendPolls = 8192;
+__device__ __forceinline__ bool mbar_wait_suspend(uint64_t *bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t"
+        ".reg .pred p;\n\t"
+        ".reg .u32 cnt;\n\t"
+        "mov.u32 cnt, %3;\n"
+        "SSD_WAIT:\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %4;\n\t"
+        "@p bra SSD_DONE;\n\t"
+        "sub.u32 cnt, cnt, 1;\n\t"
+        "setp.ne.u32 p, cnt, 0;\n\t"
+        "@p bra SSD_WAIT;\n"
+        "SSD_DONE:\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t"
+        "}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(kSuspendPolls), "r"(kSuspendHintNs)
+        : "memory");
+    return done != 0;
+}
+
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
     for (uint32_t i = 0; i < kSpinLimit; ++i) {
         if (mbar_try_wait(bar, parity)) return true;

@@ -194,23 +194,23 @@ __device__ __forceinline__ float tpg_sum(float v) {
     return v;
 }
 
-// NaN-propagating merge of two online statistics.
+// NaN-propagating merge of two online statistics (branch-free).
 __device__ __forceinline__ Stat stat_merge_nan(Stat a, Stat b) {
     const float m = fmax_nan(a.m, b.m);
-    if (m == -INFINITY) return {m, 0.f};
     const float sa = (a.m == -INFINITY) ? 0.f : a.S * ex2(a.m - m);
     const float sb = (b.m == -INFINITY) ? 0.f : b.S * ex2(b.m - m);
-    return {m, sa + sb};
+    return {m, (m == -INFINITY) ? 0.f : sa + sb};
 }
 
 // Folds a block whose largest base-2 value is xm into st; mass(mn) returns the
-// block's sum of 2^(x - mn) for the new maximum mn.
+// block's sum of 2^(x - mn) for the new maximum mn (branch-free: an all -inf
+// block leaves st unchanged, a NaN makes it NaN).
 template <class F>
 __device__ __forceinline__ void stat_fold(Stat &st, float xm, F mass) {
     const float mn = fmax_nan(st.m, xm);
-    if (mn == -INFINITY) return;
     const float keep = (st.m == -INFINITY) ? 0.f : st.S * ex2(st.m - mn);
-    st.S = keep + mass(mn);
+    const float add = mass(mn);
+    st.S = (mn == -INFINITY) ? 0.f : keep + add;
     st.m = mn;
 }
 
@@ -251,6 +251,65 @@ __device__ __forceinline__ double warp_incl_scan(double v, int lane) {
 
 __device__ __forceinline__ bool stat_ok(Stat s) {
     return (s.m < INFINITY) && (s.S > 0.f) && (s.S < INFINITY);
+}
+
+// Pass 1 of a sigma-reshaped draft row: weights 2^(z c + log2 c_t) folded into
+// st (kept out of line: the common path has no reshape).
+template <class D, int VPT>
+__device__ __noinline__ Stat reshaped_fold(Stat st, const unsigned char *row, int vbase, int nvec, int rot,
+                                           bool full, float c, DraftShape shape, int e0) {
+    constexpr int VEC = D::kVec;
+    uint4 w[VPT];
+    load_vecs<D, VPT>(row, vbase, nvec, rot, full, w);
+    float x[VPT][VEC];
+    float xm = -INFINITY;
+#pragma unroll
+    for (int kk = 0; kk < VPT; ++kk) {
+        float z[VEC];
+        decode_vec<D>(w[kk], z);
+        const int ev = e0 + ((kk + rot) & (VPT - 1)) * VEC;
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) {
+            x[kk][i] = z[i] * c + draft_bias(shape, z[i], ev + i);
+            xm = fmax_nan(xm, x[kk][i]);
+        }
+    }
+    stat_fold(st, xm, [&](float mn) {
+        float vs = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < VPT; ++kk)
+#pragma unroll
+            for (int i = 0; i < VEC; ++i) vs += ex2(x[kk][i] - mn);
+        return vs;
+    });
+    return st;
+}
+
+// Pass 2 of a pair with a sigma-reshaped draft: residual sum (x) and maximum (y)
+// of this thread's tokens (out of line, as above).
+template <class D, int VPT>
+__device__ __noinline__ float2 reshaped_resid(const unsigned char *stg, int half, int vbase, int nvec,
+                                              int rot, bool full, float c, float LT, float LD,
+                                              DraftShape shape, int e0) {
+    constexpr int VEC = D::kVec;
+    uint4 wt[VPT], wd[VPT];
+    load_vecs<D, VPT>(stg, vbase, nvec, rot, full, wt);
+    load_vecs<D, VPT>(stg + half, vbase, nvec, rot, full, wd);
+    float acc = 0.f, mx = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < VPT; ++kk) {
+        float zt[VEC], zd[VEC];
+        decode_vec<D>(wt[kk], zt);
+        decode_vec<D>(wd[kk], zd);
+        const int ev = e0 + ((kk + rot) & (VPT - 1)) * VEC;
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) {
+            const float wv = resid_of(zt[i], zd[i], c, -LT, draft_bias(shape, zd[i], ev + i) - LD);
+            acc += wv;
+            mx = fmaxf(mx, wv);
+        }
+    }
+    return make_float2(acc, mx);
 }
 
 }  // namespace
@@ -412,7 +471,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             const int u = pf_u;
             if (u >= nunits) {
                 const int s = static_cast<int>(n % kRS);
-                if (!mbar_wait_bounded(&gq.empty_bar[s], ((n / kRS) & 1) ^ 1)) {
+                if (!mbar_wait_suspend(&gq.empty_bar[s], ((n / kRS) & 1) ^ 1)) {
                     ok = false;
                     break;
                 }
@@ -438,7 +497,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             const int total = skip ? 1 : nch * (p2 ? 2 : 1);
             for (int i = 0; i < total; ++i) {
                 const int s = static_cast<int>(n % kRS);
-                if (!mbar_wait_bounded(&gq.empty_bar[s], ((n / kRS) & 1) ^ 1)) {
+                if (!mbar_wait_suspend(&gq.empty_bar[s], ((n / kRS) & 1) ^ 1)) {
                     ok = false;
                     break;
                 }
@@ -485,7 +544,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
 
         for (uint32_t j = 0;; ++j) {
             const int buf = static_cast<int>(j & 1);
-            if (!mbar_wait_bounded(&gs.tail_full[buf], (j >> 1) & 1)) {
+            if (!mbar_wait_suspend(&gs.tail_full[buf], (j >> 1) & 1)) {
                 if (lane == 0 && P.dev_status) atomicOr(P.dev_status, SSD_DEV_TIMEOUT);
                 break;
             }
@@ -953,7 +1012,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
 
     for (;;) {
         const int s = static_cast<int>(n & (kRS - 1));
-        if (!mbar_wait_bounded(&gs.full_bar[s], (n / kRS) & 1)) {
+        if (!mbar_wait_suspend(&gs.full_bar[s], (n / kRS) & 1)) {
             atomicOr(&s_abort, 1);
             if (t == 0 && P.dev_status) atomicOr(P.dev_status, SSD_DEV_TIMEOUT);
             break;
@@ -963,7 +1022,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         if (pass == kPassStop) break;
         if (h.unit != cur) {
             // a new unit: wait for its group-array buffer, then per-unit constants
-            if (!mbar_wait_bounded(&gs.tail_empty[nho & 1], ((nho >> 1) & 1) ^ 1)) {
+            if (!mbar_wait_suspend(&gs.tail_empty[nho & 1], ((nho >> 1) & 1) ^ 1)) {
                 atomicOr(&s_abort, 1);
                 if (t == 0 && P.dev_status) atomicOr(P.dev_status, SSD_DEV_TIMEOUT);
                 break;
@@ -1026,35 +1085,14 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         if (active) {
             if (pass == kPassStats && stage_pair) {
                 // online statistics: threads [0, 128) target, the rest draft
-                uint4 w[VPT1];
-                load_vecs<D, VPT1>(stg + p1_row * HALF, p1_vbase, h.nvec, p1_rot, h.nvec == FULL_PAIR, w);
                 if (p1_row == 0 || !shape.on) {
+                    uint4 w[VPT1];
+                    load_vecs<D, VPT1>(stg + p1_row * HALF, p1_vbase, h.nvec, p1_rot, h.nvec == FULL_PAIR, w);
                     const float xm = vecs_max<D, VPT1>(w) * c;
                     stat_fold(st, xm, [&](float mn) { return vecs_expsum<D, VPT1>(w, c, mn); });
                 } else {
-                    // reshaped draft: weights 2^(z c + log2 c_t)
-                    const int e0 = h.chunk * (FULL_PAIR * VEC) + p1_vbase * VEC;
-                    float x[VPT1][VEC];
-                    float xm = -INFINITY;
-#pragma unroll
-                    for (int kk = 0; kk < VPT1; ++kk) {
-                        float z[VEC];
-                        decode_vec<D>(w[kk], z);
-                        const int ev = e0 + ((kk + p1_rot) & (VPT1 - 1)) * VEC;
-#pragma unroll
-                        for (int i = 0; i < VEC; ++i) {
-                            x[kk][i] = z[i] * c + draft_bias(shape, z[i], ev + i);
-                            xm = fmax_nan(xm, x[kk][i]);
-                        }
-                    }
-                    stat_fold(st, xm, [&](float mn) {
-                        float vs = 0.f;
-#pragma unroll
-                        for (int kk = 0; kk < VPT1; ++kk)
-#pragma unroll
-                            for (int i = 0; i < VEC; ++i) vs += ex2(x[kk][i] - mn);
-                        return vs;
-                    });
+                    st = reshaped_fold<D, VPT1>(st, stg + HALF, p1_vbase, h.nvec, p1_rot, h.nvec == FULL_PAIR, c,
+                                                shape, h.chunk * (FULL_PAIR * VEC) + p1_vbase * VEC);
                 }
             } else if (pass == kPassStats) {
                 // one row: sampled row K (maxima, masses, statistics) or greedy (maxima,
@@ -1073,27 +1111,28 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                 const float gm = tpg_max_nan<TPGS>(vecs_max<D, VPTS>(w));
                 const int g = h.chunk * GPS + s_gl;
                 if (sampled) {
-                    const float vs = (gm != -INFINITY) ? vecs_expsum<D, VPTS>(w, c, gm * c) : 0.f;
-                    const float gsv = tpg_sum<TPGS>(vs);
-                    if (s_part == 0) {
-                        if (gm != -INFINITY) st = (gm == gm) ? stat_merge_nan(st, Stat{gm * c, gsv}) : Stat{NAN, NAN};
-                        if (g < G) {
-                            gmax[g] = gm;
-                            gsum[g] = gsv;
-                        }
+                    const float gmc = gm * c;
+                    const float vs = vecs_expsum<D, VPTS>(w, c, gmc);
+                    const float gsum_all = tpg_sum<TPGS>(vs);  // every lane shuffles
+                    const float gsv = (gm == -INFINITY) ? 0.f : gsum_all;
+                    const bool lead = s_part == 0 && gm != -INFINITY;
+                    st = stat_merge_nan(st, Stat{lead ? gmc : -INFINITY, lead ? gsv : 0.f});
+                    if (s_part == 0 && g < G) {
+                        gmax[g] = gm;
+                        gsum[g] = gsv;
                     }
                 } else if (s_part == 0 && g < G) {
                     gmax[g] = gm;
                 }
             } else {
                 // pass 2 (pair): residual masses and maxima per group
-                uint4 wt[VPT2], wd[VPT2];
                 const bool full = h.nvec == FULL_PAIR;
-                load_vecs<D, VPT2>(stg, r_vbase, h.nvec, r_rot, full, wt);
-                load_vecs<D, VPT2>(stg + HALF, r_vbase, h.nvec, r_rot, full, wd);
                 float2 acc = make_float2(0.f, 0.f);
                 float mx = 0.f;
                 if (!shape.on) {
+                    uint4 wt[VPT2], wd[VPT2];
+                    load_vecs<D, VPT2>(stg, r_vbase, h.nvec, r_rot, full, wt);
+                    load_vecs<D, VPT2>(stg + HALF, r_vbase, h.nvec, r_rot, full, wd);
                     const float2 cc = make_float2(c, c), nl = make_float2(-LT, -LD);
 #pragma unroll
                     for (int kk = 0; kk < VPT2; ++kk) {
@@ -1113,21 +1152,10 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                         }
                     }
                 } else {
-                    const int e0 = h.chunk * (FULL_PAIR * VEC) + r_vbase * VEC;
-#pragma unroll
-                    for (int kk = 0; kk < VPT2; ++kk) {
-                        float zt[VEC], zd[VEC];
-                        decode_vec<D>(wt[kk], zt);
-                        decode_vec<D>(wd[kk], zd);
-                        const int ev = e0 + ((kk + r_rot) & (VPT2 - 1)) * VEC;
-#pragma unroll
-                        for (int i = 0; i < VEC; ++i) {
-                            const float wv =
-                                resid_of(zt[i], zd[i], c, -LT, draft_bias(shape, zd[i], ev + i) - LD);
-                            acc.x += wv;
-                            mx = fmaxf(mx, wv);
-                        }
-                    }
+                    const float2 r2 = reshaped_resid<D, VPT2>(stg, HALF, r_vbase, h.nvec, r_rot, full, c, LT, LD, shape,
+                                                              h.chunk * (FULL_PAIR * VEC) + r_vbase * VEC);
+                    acc.x = r2.x;
+                    mx = r2.y;
                 }
                 const float gsv = tpg_sum<TPG2>(acc.x + acc.y);
                 const float gmx = tpg_max<TPG2>(mx);
@@ -1202,7 +1230,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     }
 
     // this group is done: tell its tail warp
-    if (!mbar_wait_bounded(&gs.tail_empty[nho & 1], ((nho >> 1) & 1) ^ 1)) {
+    if (!mbar_wait_suspend(&gs.tail_empty[nho & 1], ((nho >> 1) & 1) ^ 1)) {
         if (t == 0 && P.dev_status) atomicOr(P.dev_status, SSD_DEV_TIMEOUT);
     }
     handoff(kKindStop, 0, 0.f, 0.f);
