@@ -172,6 +172,7 @@ int run_units(int mode, const void *tgt, const void *drf, int dtype, int B, int 
     const size_t sdyn = ssd::stream_dyn_bytes(V);
     const bool streaming = aligned(tgt, 16) && aligned(drf, 16) &&
                            (static_cast<long long>(V) * elem) % 16 == 0 &&
+                           (V + ssd::kGroupTokens - 1) / ssd::kGroupTokens <= ssd::kStreamMaxGroups &&
                            sdyn <= dv->max_dyn[dtype == SSD_F32 ? 4 : 5];
     Geometry g;
     if (!streaming) {

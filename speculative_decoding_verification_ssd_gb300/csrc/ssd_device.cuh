@@ -76,31 +76,64 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
 
 // Waits for phase `parity` of `bar` with a bounded number of polls.  Returns
 // false if the limit ran out (the caller records SSD_DEV_TIMEOUT).
-// Waits for phase `parity` of `bar` with the thread suspended in hardware
-// between polls (each poll sleeps up to kSuspendHintNs or until the phase
-// completes); gives up after kSuspendPolls polls (a few seconds) and returns
-// false.  The loop lives in one asm block, so the compiler sees no divergent
-// branch around it.
-constexpr uint32_t kSuspendHintNs = 500000;
-constexpr uint32_t kSuspendPolls = 8192;
+// Waits for phase `parity` of `bar`, polling with try_wait (each poll may
+// suspend the thread for up to kSuspendHintNs or until the phase completes);
+// gives up after kWaitLimitNs of wall-clock time (%globaltimer) and returns
+// false.  A time bound rather than a poll count keeps roles that legitimately
+// idle for a long stretch of a large launch from giving up early.  The loop
+// lives in one asm block, so the compiler sees no divergent branch around it.
+constexpr uint32_t kSuspendHintNs = 200000;
+constexpr uint64_t kWaitLimitNs = 4000000000ull;
 __device__ __forceinline__ bool mbar_wait_suspend(uint64_t *bar, uint32_t parity) {
     uint32_t done;
     asm volatile(
         "{\n\t"
         ".reg .pred p;\n\t"
-        ".reg .u32 cnt;\n\t"
-        "mov.u32 cnt, %3;\n"
+        ".reg .u64 t0, t1;\n\t"
+        "mov.u64 t0, %%globaltimer;\n"
         "SSD_WAIT:\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %4;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "@p bra SSD_DONE;\n\t"
-        "sub.u32 cnt, cnt, 1;\n\t"
-        "setp.ne.u32 p, cnt, 0;\n\t"
+        "mov.u64 t1, %%globaltimer;\n\t"
+        "sub.u64 t1, t1, t0;\n\t"
+        "setp.lt.u64 p, t1, %4;\n\t"
         "@p bra SSD_WAIT;\n"
         "SSD_DONE:\n\t"
         "selp.u32 %0, 1, 0, p;\n\t"
         "}"
         : "=r"(done)
-        : "r"(smem_addr(bar)), "r"(parity), "r"(kSuspendPolls), "r"(kSuspendHintNs)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(kSuspendHintNs), "l"(kWaitLimitNs)
+        : "memory");
+    return done != 0;
+}
+
+// Waits for phase `parity` of `bar`, polling with try_wait and sleeping
+// SleepNs between polls (0: no sleep); gives up after kWaitLimitNs of
+// wall-clock time and returns false.  Roles that mostly idle (tail warps,
+// producers) sleep longer so that their polls take few issue slots from the
+// warps doing arithmetic.
+template <uint32_t SleepNs>
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t *bar, uint32_t parity) {
+    uint32_t done;
+    if (SleepNs == 0) return mbar_wait_suspend(bar, parity);
+    asm volatile(
+        "{\n\t"
+        ".reg .pred p;\n\t"
+        ".reg .u64 t0, t1;\n\t"
+        "mov.u64 t0, %%globaltimer;\n"
+        "SSD_SWAIT:\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "@p bra SSD_SDONE;\n\t"
+        "nanosleep.u32 %3;\n\t"
+        "mov.u64 t1, %%globaltimer;\n\t"
+        "sub.u64 t1, t1, t0;\n\t"
+        "setp.lt.u64 p, t1, %4;\n\t"
+        "@p bra SSD_SWAIT;\n"
+        "SSD_SDONE:\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t"
+        "}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity), "n"(SleepNs), "l"(kWaitLimitNs)
         : "memory");
     return done != 0;
 }

@@ -49,7 +49,7 @@ constexpr int kNG = kStreamGroups;      // consumer groups (= rings = tail warps
 constexpr int kRS = kStreamRingStages;  // stages per ring
 constexpr int kSB = kStreamStageBytes;  // bytes per stage
 constexpr int kGTok = kGroupTokens;     // tokens per group of the group arrays
-constexpr int kNBuf = 2;                // group-array buffers per consumer group
+constexpr int kNBuf = kStreamBuffers;   // group-array buffers per consumer group
 constexpr int kProducerWarp0 = kNG * kGW;
 constexpr int kTailWarp0 = kProducerWarp0 + kNG;
 constexpr unsigned kFull = 0xFFFFFFFFu;
@@ -99,7 +99,8 @@ struct TailDesc {
     float c;       // log2 e / tau
     float M, S;    // sampled single row: target statistics (base 2)
     float LT, LD;  // pair: normalisers (base 2)
-    float p_tok, q_tok, pad1;
+    float p_tok, q_tok;
+    float ztx;  // target logit of the drafted token (k < K)
     DraftShape shape;
 };
 
@@ -153,6 +154,19 @@ __device__ __forceinline__ void load_vecs(const unsigned char *row, int vbase, i
         else
             w[k] = v < nvec ? *reinterpret_cast<const uint4 *>(row + 16 * v) : neg_inf_vec<D>();
     }
+}
+
+// One 16-byte vector of a staged row, read afresh from shared memory (a second
+// sweep reloads instead of keeping the stage in registers); vectors at or past
+// nvec read as -inf unless the stage is full.
+template <class D>
+__device__ __forceinline__ uint4 lds_vec(const unsigned char *row, int v, int nvec, bool full) {
+    uint4 r = neg_inf_vec<D>();
+    if (full || v < nvec)
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                     : "r"(smem_addr(row + 16 * v)));
+    return r;
 }
 
 template <class D, int VPT>
@@ -328,9 +342,13 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     constexpr int TPG2 = kGT / GPR;        // pass 2: threads per group
     constexpr int VPT1 = FULL_PAIR / (kGT / 2), VPTS = GV / TPGS, VPT2 = GV / TPG2;
     static_assert(VPT1 == 4 && VPTS == 4 && VPT2 == 2, "stage geometry");
-    constexpr int LPG = GV;        // tail: lanes per group (one vector each)
-    constexpr int GPI = 32 / LPG;  // tail: groups per warp iteration
-    static_assert(32 % LPG == 0, "tail geometry");
+    constexpr int LPG = GV < 32 ? GV : 32;  // tail: lanes per group re-read (one vector each)
+    constexpr int GPI = 32 / LPG;           // tail: groups per warp iteration
+    constexpr int VPL = GV / LPG;           // tail: vectors per lane per group
+    constexpr int TPL = kGTok / 32;         // tail: tokens per lane of one group
+    constexpr int kBatch = 2;               // tail: vectors in flight per lane when re-reading
+    constexpr int kMaskWords = kStreamMaxGroups / (32 * 32);  // tail: candidate mask words per lane
+    static_assert(32 % LPG == 0 && TPL >= 1 && kBatch % VPL == 0, "tail geometry");
 
     extern __shared__ __align__(128) unsigned char dyn_smem[];
     __shared__ GroupShared gsh[kNG];
@@ -543,8 +561,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         const int g0 = min(G, lane * R), g1 = min(G, g0 + R);
 
         for (uint32_t j = 0;; ++j) {
-            const int buf = static_cast<int>(j & 1);
-            if (!mbar_wait_suspend(&gs.tail_full[buf], (j >> 1) & 1)) {
+            const int buf = static_cast<int>(j % kNBuf);
+            if (!mbar_wait_suspend(&gs.tail_full[buf], (j / kNBuf) & 1)) {
                 if (lane == 0 && P.dev_status) atomicOr(P.dev_status, SSD_DEV_TIMEOUT);
                 break;
             }
@@ -580,20 +598,26 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             };
 
             // ---- cache top-F_k (gmax holds the scores' group maxima) --------
-            auto top_f = [&](bool resid) {
-                uint32_t tv = 0;
-                for (int g = g0; g < g1; ++g) {
+            auto top_f = [&](bool resid) -> uint64_t {
+                // Threshold: the F-th largest of each lane's two largest group
+                // maxima (64 distinct groups), so at least F groups reach it.
+                // Lanes scan interleaved groups g = lane + 32 i (conflict-free).
+                uint32_t m1 = 0, m2 = 0;
+                for (int g = lane; g < G; g += 32) {
                     const uint32_t o = ordered_bits(gmax[g]);
-                    tv = o > tv ? o : tv;
+                    m2 = max(m2, min(m1, o));
+                    m1 = max(m1, o);
                 }
                 uint32_t th = 0;
-                if (Fk <= 32) {
-                    // F-th largest (with multiplicity) of the 32 lane maxima
-                    uint32_t v = tv;
+                if (Fk <= 64) {
+                    uint32_t v = m1, nxt = m2;
                     for (int it = 0; it < Fk; ++it) {
                         th = __reduce_max_sync(kFull, v);
                         const uint32_t who = __ballot_sync(kFull, v == th);
-                        if (lane == __ffs(who) - 1) v = 0;
+                        if (lane == __ffs(who) - 1) {
+                            v = nxt;
+                            nxt = 0;
+                        }
                     }
                 } else {
                     // largest th with at least F groups whose maximum reaches it
@@ -601,7 +625,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                     while (lo < hi) {
                         const uint32_t mid = lo + ((hi - lo) >> 1) + 1;
                         int cnt = 0;
-                        for (int g = g0; g < g1; ++g) cnt += ordered_bits(gmax[g]) >= mid ? 1 : 0;
+                        for (int g = lane; g < G; g += 32) cnt += ordered_bits(gmax[g]) >= mid ? 1 : 0;
                         cnt = __reduce_add_sync(kFull, cnt);
                         if (cnt >= Fk)
                             lo = mid;
@@ -610,35 +634,60 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                     }
                     th = lo;
                 }
-                if (lane == 0) {
-                    gs.cnt[0] = 0;
-                    gs.cnt[1] = 0;
+                // candidate groups (maximum reaches th): per-lane bit masks, then
+                // a warp prefix places each lane's groups in ascending order
+                uint32_t cm[kMaskWords];
+#pragma unroll
+                for (int w = 0; w < kMaskWords; ++w) {
+                    uint32_t m = 0;
+#pragma unroll 8
+                    for (int i = 0; i < 32; ++i) {
+                        const int g = lane + 32 * (32 * w + i);
+                        if (g < G) m |= (ordered_bits(gmax[g]) >= th ? 1u : 0u) << i;
+                    }
+                    cm[w] = m;
                 }
-                __syncwarp();
-                for (int g = g0; g < g1; ++g) {
-                    if (ordered_bits(gmax[g]) >= th) {
-                        const int idx = atomicAdd(&gs.cnt[0], 1);
-                        if (idx < kCandGroupsCap) gs.cgroups[idx] = g;
+                int mine = 0;
+#pragma unroll
+                for (int w = 0; w < kMaskWords; ++w) mine += __popc(cm[w]);
+                int incl = mine;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(kFull, incl, o);
+                    if (lane >= o) incl += y;
+                }
+                const int ncg = __shfl_sync(kFull, incl, 31);
+                if (ncg <= kCandGroupsCap) {
+                    int pos = incl - mine;
+#pragma unroll
+                    for (int w = 0; w < kMaskWords; ++w) {
+                        uint32_t m = cm[w];
+                        while (m) {
+                            const int i = __ffs(m) - 1;
+                            m &= m - 1;
+                            gs.cgroups[pos++] = lane + 32 * (32 * w + i);
+                        }
                     }
                 }
+                if (lane == 0) gs.cnt[1] = 0;
                 __syncwarp();
-                const int ncg = gs.cnt[0];
                 const bool all_groups = ncg > kCandGroupsCap;
                 const int ngroups = all_groups ? G : ncg;
                 uint64_t theta = static_cast<uint64_t>(th) << 32;
                 const int sub = lane / LPG, li = lane % LPG;
                 int count = 0;
                 for (int round = 0; round < 64; ++round) {
-                    for (int q0 = 0; q0 < ngroups; q0 += 2 * GPI) {
-                        uint4 wt[2], wd[2];
-                        int e0[2];
+                    // each lane holds kBatch vectors of one or more groups per batch
+                    for (int q0 = 0; q0 < ngroups; q0 += kBatch / VPL * GPI) {
+                        uint4 wt[kBatch], wd[kBatch];
+                        int e0[kBatch];
 #pragma unroll
-                        for (int x = 0; x < 2; ++x) {
-                            const int q = q0 + x * GPI + sub;
+                        for (int x = 0; x < kBatch; ++x) {
+                            const int q = q0 + (x / VPL) * GPI + sub;
                             e0[x] = V;
                             if (q < ngroups) {
                                 const int g = all_groups ? q : gs.cgroups[q];
-                                e0[x] = g * kGTok + li * VEC;
+                                e0[x] = g * kGTok + ((x % VPL) * LPG + li) * VEC;
                             }
                             if (e0[x] < V) {
                                 wt[x] = __ldg(reinterpret_cast<const uint4 *>(trow + static_cast<int64_t>(e0[x]) * S));
@@ -647,7 +696,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                             }
                         }
 #pragma unroll
-                        for (int x = 0; x < 2; ++x) {
+                        for (int x = 0; x < kBatch; ++x) {
                             if (e0[x] >= V) continue;
                             float zt[VEC], zd[VEC];
                             decode_vec<D>(wt[x], zt);
@@ -694,13 +743,16 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                 }
                 if (count > kCandCap) count = kCandCap;
                 // rank by counting; ranks below F go straight to the cache row
+                uint64_t best = 0;
                 for (int i = lane; i < count; i += 32) {
                     const uint64_t key = gs.cand[i];
+                    best = key > best ? key : best;
                     int rr = 0;
                     for (int jx = 0; jx < count; ++jx) rr += gs.cand[jx] > key ? 1 : 0;
                     if (rr < Fk) P.cache_tok[static_cast<int64_t>(b) * P.budget + P.off[k] + rr] = key_id(key);
                 }
                 __syncwarp();
+                return warp_max_u64(best);
             };
 
             // ---- inverse-CDF bonus at u_K over ascending token id -----------
@@ -773,34 +825,37 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                     gstar = lp > 0 ? lp - 1 : 0;
                     cut = 1e300;
                 }
-                // element level: two tokens per lane, ascending
-                const int e0 = gstar * kGTok + 2 * lane;
-                float w[2] = {0.f, 0.f};
+                // element level: TPL consecutive tokens per lane, ascending
+                const int e0 = gstar * kGTok + TPL * lane;
+                float w[TPL];
+                double lsum = 0.0;
 #pragma unroll
-                for (int x = 0; x < 2; ++x) {
+                for (int x = 0; x < TPL; ++x) {
                     const int e = e0 + x;
+                    w[x] = 0.f;
                     if (e < V) {
                         const float zt = load_logit<D>(trow, e);
                         w[x] = pmode ? ex2(fmaf(zt, c, -Mc)) : resid_e(zt, load_logit<D>(drow, e), e);
                     }
+                    lsum += static_cast<double>(w[x]);
                 }
-                const double pairsum = static_cast<double>(w[0]) + static_cast<double>(w[1]);
-                const double ex = warp_incl_scan(pairsum, lane) - pairsum;
-                const double c0 = ex + static_cast<double>(w[0]);
-                const double c1 = c0 + static_cast<double>(w[1]);
-                const bool o0 = c0 > cut && e0 < V, o1 = c1 > cut && e0 + 1 < V;
-                const uint32_t over = __ballot_sync(kFull, o0 || o1);
-                const bool q0 = w[0] > 0.f && e0 < V, q1 = w[1] > 0.f && e0 + 1 < V;
-                const uint32_t pos = __ballot_sync(kFull, q0 || q1);
+                double cum = warp_incl_scan(lsum, lane) - lsum;
+                int first_over = -1, last_pos = -1;
+#pragma unroll
+                for (int x = 0; x < TPL; ++x) {
+                    cum += static_cast<double>(w[x]);
+                    if (first_over < 0 && cum > cut && e0 + x < V) first_over = x;
+                    if (w[x] > 0.f && e0 + x < V) last_pos = x;
+                }
+                const uint32_t over = __ballot_sync(kFull, first_over >= 0);
+                const uint32_t pos = __ballot_sync(kFull, last_pos >= 0);
                 int pick;
                 if (over) {
                     const int l = __ffs(over) - 1;
-                    const int first = __shfl_sync(kFull, o0 ? 0 : 1, l);
-                    pick = gstar * kGTok + 2 * l + first;
+                    pick = gstar * kGTok + TPL * l + __shfl_sync(kFull, first_over, l);
                 } else if (pos) {
                     const int l = 31 - __clz(pos);
-                    const int last = __shfl_sync(kFull, q1 ? 1 : 0, l);
-                    pick = gstar * kGTok + 2 * l + last;
+                    pick = gstar * kGTok + TPL * l + __shfl_sync(kFull, last_pos, l);
                 } else {
                     pick = gstar * kGTok;
                 }
@@ -851,24 +906,33 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                 if (M != M) {
                     rec.flags |= SSD_DEV_NONFINITE;
                 } else {
-                    const int e0 = gbest * kGTok + 2 * lane;
-                    bool m0 = false, m1 = false;
-                    if (e0 < V && e0 != xmask) m0 = load_logit<D>(trow, e0) == M;
-                    if (e0 + 1 < V && e0 + 1 != xmask) m1 = load_logit<D>(trow, e0 + 1) == M;
-                    const uint32_t who = __ballot_sync(kFull, m0 || m1);
-                    int id = gbest * kGTok;
-                    if (who) {
-                        const int l = __ffs(who) - 1;
-                        id = gbest * kGTok + 2 * l + __shfl_sync(kFull, m0 ? 0 : 1, l);
+                    // the argmax is the largest cache candidate (same exclusion, same
+                    // (value, lowest id) order); without a cache, re-read the best group
+                    const uint64_t top = (Fk > 0) ? top_f(false) : 0;
+                    int id;
+                    if (Fk > 0 && key_value(top) == M) {
+                        id = key_id(top);
+                    } else {
+                        const int e0 = gbest * kGTok + TPL * lane;
+                        int mfirst = -1;
+#pragma unroll
+                        for (int x = TPL - 1; x >= 0; --x) {
+                            const int e = e0 + x;
+                            if (e < V && e != xmask && load_logit<D>(trow, e) == M) mfirst = x;
+                        }
+                        const uint32_t who = __ballot_sync(kFull, mfirst >= 0);
+                        id = gbest * kGTok;
+                        if (who) {
+                            const int l = __ffs(who) - 1;
+                            id = gbest * kGTok + TPL * l + __shfl_sync(kFull, mfirst, l);
+                        }
                     }
                     rec.tk = id;
                     if (k < K) {
-                        const float ztx = load_logit<D>(trow, xt);
-                        rec.accept = make_key(ztx, xt) > make_key(M, id) ? 1 : 0;
+                        rec.accept = make_key(d.ztx, xt) > make_key(M, id) ? 1 : 0;
                         rec.p_tok = rec.accept ? 1.f : 0.f;
                         rec.q_tok = 1.f;
                     }
-                    if (Fk > 0) top_f(false);
                 }
             } else if (d.kind == kKindSampled) {
                 if (Fk > 0) top_f(false);
@@ -989,7 +1053,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     auto handoff = [&](int hk, int state, float M, float Ssum) {
         gbar();
         if (t == 0) {
-            TailDesc &D0 = gs.desc[nho & 1];
+            TailDesc &D0 = gs.desc[nho % kNBuf];
             D0.kind = hk;
             D0.b = b;
             D0.k = k;
@@ -1004,14 +1068,15 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             D0.LD = LD;
             D0.p_tok = p_tok;
             D0.q_tok = q_tok;
+            D0.ztx = ztx;
             D0.shape = shape;
-            mbar_arrive(&gs.tail_full[nho & 1]);
+            mbar_arrive(&gs.tail_full[nho % kNBuf]);
         }
         ++nho;
     };
 
     for (;;) {
-        const int s = static_cast<int>(n & (kRS - 1));
+        const int s = static_cast<int>(n % kRS);
         if (!mbar_wait_suspend(&gs.full_bar[s], (n / kRS) & 1)) {
             atomicOr(&s_abort, 1);
             if (t == 0 && P.dev_status) atomicOr(P.dev_status, SSD_DEV_TIMEOUT);
@@ -1022,7 +1087,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         if (pass == kPassStop) break;
         if (h.unit != cur) {
             // a new unit: wait for its group-array buffer, then per-unit constants
-            if (!mbar_wait_suspend(&gs.tail_empty[nho & 1], ((nho >> 1) & 1) ^ 1)) {
+            if (!mbar_wait_suspend(&gs.tail_empty[nho % kNBuf], ((nho / kNBuf) & 1) ^ 1)) {
                 atomicOr(&s_abort, 1);
                 if (t == 0 && P.dev_status) atomicOr(P.dev_status, SSD_DEV_TIMEOUT);
                 break;
@@ -1030,7 +1095,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             cur = h.unit;
             k = h.k;
             b = h.b;
-            gmax = arrays + (nho & 1) * 2 * Gp;
+            gmax = arrays + (nho % kNBuf) * 2 * Gp;
             gsum = gmax + Gp;
             const float tau = P.temperature[b];
             const bool tau_ok = (tau >= 0.f) && (tau < INFINITY);
@@ -1061,14 +1126,17 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             p_tok = NAN;
             q_tok = NAN;
             accept = 0;
-            if (t == 0 && active && pair) {
+            ztx = 0.f;
+            if (t == 0 && active && k < K) {
                 const unsigned char *trow = static_cast<const unsigned char *>(P.tgt) +
                                             (static_cast<int64_t>(b) * P.tgt_seq_stride + static_cast<int64_t>(k) * V) * S;
-                const unsigned char *drow = static_cast<const unsigned char *>(P.drf) +
-                                            (static_cast<int64_t>(b) * P.drf_seq_stride + static_cast<int64_t>(k) * V) * S;
                 ztx = load_logit<D>(trow, xt);
-                zdx = load_logit<D>(drow, xt);
-                u_k = P.uniforms ? P.uniforms[static_cast<int64_t>(b) * (K + 1) + k] : 0.f;
+                if (pair) {
+                    const unsigned char *drow = static_cast<const unsigned char *>(P.drf) +
+                                                (static_cast<int64_t>(b) * P.drf_seq_stride + static_cast<int64_t>(k) * V) * S;
+                    zdx = load_logit<D>(drow, xt);
+                    u_k = P.uniforms ? P.uniforms[static_cast<int64_t>(b) * (K + 1) + k] : 0.f;
+                }
             }
         }
         if (pass == kPassSkip) {
@@ -1080,7 +1148,6 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         }
         const unsigned char *stg = ring + s * kSB;
         const bool stage_pair = (h.code >> 5) & 1;
-
         // ---- stage processing -----------------------------------------------
         if (active) {
             if (pass == kPassStats && stage_pair) {
@@ -1230,7 +1297,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     }
 
     // this group is done: tell its tail warp
-    if (!mbar_wait_suspend(&gs.tail_empty[nho & 1], ((nho >> 1) & 1) ^ 1)) {
+    if (!mbar_wait_suspend(&gs.tail_empty[nho % kNBuf], ((nho / kNBuf) & 1) ^ 1)) {
         if (t == 0 && P.dev_status) atomicOr(P.dev_status, SSD_DEV_TIMEOUT);
     }
     handoff(kKindStop, 0, 0.f, 0.f);

@@ -12,16 +12,19 @@ constexpr int kStreamGroupWarps = 8;   // warps per consumer group
 constexpr int kStreamThreads = kStreamGroups * kStreamGroupWarps * 32 + 2 * kStreamGroups * 32;
 constexpr int kStreamRingStages = 4;   // stages per ring
 constexpr int kStreamStageBytes = 16384;
-constexpr int kGroupTokens = 64;  // tokens per group of the per-group arrays
+constexpr int kGroupTokens = 64;   // tokens per group of the per-group arrays
+constexpr int kStreamBuffers = 2;  // group-array buffers per consumer group
+constexpr int kStreamMaxGroups = 3 * 32 * 32;  // groups per row the tail warp's masks cover
 
 // Dynamic shared memory of the streaming kernel for a vocabulary of V tokens:
-// the stage rings plus, per consumer group, two buffers of two float arrays
-// with one entry per 64-token group.
+// the stage rings plus, per consumer group, kStreamBuffers buffers of two float
+// arrays with one entry per 64-token group.
 inline size_t stream_dyn_bytes(int V) {
     const size_t G = (static_cast<size_t>(V) + kGroupTokens - 1) / kGroupTokens;
     const size_t Gp = (G + 31) & ~static_cast<size_t>(31);
     return static_cast<size_t>(kStreamGroups) *
-           (static_cast<size_t>(kStreamRingStages) * kStreamStageBytes + 2 * 2 * Gp * sizeof(float));
+           (static_cast<size_t>(kStreamRingStages) * kStreamStageBytes +
+            static_cast<size_t>(kStreamBuffers) * 2 * Gp * sizeof(float));
 }
 
 struct UnitParams;
