@@ -347,7 +347,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     constexpr int VPL = GV / LPG;           // tail: vectors per lane per group
     constexpr int TPL = kGTok / 32;         // tail: tokens per lane of one group
     constexpr int kBatch = 2;               // tail: vectors in flight per lane when re-reading
-    constexpr int kMaskWords = kStreamMaxGroups / (32 * 32);  // tail: candidate mask words per lane
+    constexpr int kMaskWords = kStreamMaxGroups / (32 * 32);  // tail: candidate mask words per lane (4 bits per strip)
     static_assert(32 % LPG == 0 && TPL >= 1 && kBatch % VPL == 0, "tail geometry");
 
     extern __shared__ __align__(128) unsigned char dyn_smem[];
@@ -360,7 +360,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int B = P.B, K = P.K, V = P.V;
     const int G = (V + kGTok - 1) / kGTok;
-    const int Gp = (G + 31) & ~31;
+    const int Gp = (G + 127) & ~127;  // group arrays padded to whole strips of 4 x 32 groups
     const bool do_verify = (P.mode & kModeVerify) != 0;
     const bool do_cache = (P.mode & kModeCache) != 0;
     const int nunits = B * (K + 1);
@@ -601,12 +601,19 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             auto top_f = [&](bool resid) -> uint64_t {
                 // Threshold: the F-th largest of each lane's two largest group
                 // maxima (64 distinct groups), so at least F groups reach it.
-                // Lanes scan interleaved groups g = lane + 32 i (conflict-free).
+                // Lane l scans groups 4l..4l+3 of every 128-group strip with one
+                // 16-byte load (conflict-free); the padding reads as -inf.
+                const int nstrip = Gp / 128;
+                const float4 *gm4 = reinterpret_cast<const float4 *>(gmax) + lane;
                 uint32_t m1 = 0, m2 = 0;
-                for (int g = lane; g < G; g += 32) {
-                    const uint32_t o = ordered_bits(gmax[g]);
-                    m2 = max(m2, min(m1, o));
-                    m1 = max(m1, o);
+                for (int i = 0; i < nstrip; ++i) {
+                    const float4 v = gm4[32 * i];
+                    const uint32_t o[4] = {ordered_bits(v.x), ordered_bits(v.y), ordered_bits(v.z), ordered_bits(v.w)};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        m2 = max(m2, min(m1, o[j]));
+                        m1 = max(m1, o[j]);
+                    }
                 }
                 uint32_t th = 0;
                 if (Fk <= 64) {
@@ -625,7 +632,11 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                     while (lo < hi) {
                         const uint32_t mid = lo + ((hi - lo) >> 1) + 1;
                         int cnt = 0;
-                        for (int g = lane; g < G; g += 32) cnt += ordered_bits(gmax[g]) >= mid ? 1 : 0;
+                        for (int i = 0; i < nstrip; ++i) {
+                            const float4 v = gm4[32 * i];
+                            cnt += (ordered_bits(v.x) >= mid) + (ordered_bits(v.y) >= mid) + (ordered_bits(v.z) >= mid) +
+                                   (ordered_bits(v.w) >= mid);
+                        }
                         cnt = __reduce_add_sync(kFull, cnt);
                         if (cnt >= Fk)
                             lo = mid;
@@ -634,18 +645,18 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                     }
                     th = lo;
                 }
-                // candidate groups (maximum reaches th): per-lane bit masks, then
-                // a warp prefix places each lane's groups in ascending order
+                // candidate groups (maximum reaches th): per-lane bit masks (bit 4i + j:
+                // group 128 i + 4 lane + j), then a warp prefix places each lane's groups
                 uint32_t cm[kMaskWords];
 #pragma unroll
-                for (int w = 0; w < kMaskWords; ++w) {
-                    uint32_t m = 0;
-#pragma unroll 8
-                    for (int i = 0; i < 32; ++i) {
-                        const int g = lane + 32 * (32 * w + i);
-                        if (g < G) m |= (ordered_bits(gmax[g]) >= th ? 1u : 0u) << i;
-                    }
-                    cm[w] = m;
+                for (int w = 0; w < kMaskWords; ++w) cm[w] = 0;
+                for (int i = 0; i < nstrip; ++i) {
+                    const float4 v = gm4[32 * i];
+                    const uint32_t bits = (ordered_bits(v.x) >= th ? 1u : 0u) | (ordered_bits(v.y) >= th ? 2u : 0u) |
+                                          (ordered_bits(v.z) >= th ? 4u : 0u) | (ordered_bits(v.w) >= th ? 8u : 0u);
+#pragma unroll
+                    for (int w = 0; w < kMaskWords; ++w)
+                        if ((i >> 3) == w) cm[w] |= bits << (4 * (i & 7));
                 }
                 int mine = 0;
 #pragma unroll
@@ -663,9 +674,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                     for (int w = 0; w < kMaskWords; ++w) {
                         uint32_t m = cm[w];
                         while (m) {
-                            const int i = __ffs(m) - 1;
+                            const int bt = 32 * w + __ffs(m) - 1;
                             m &= m - 1;
-                            gs.cgroups[pos++] = lane + 32 * (32 * w + i);
+                            gs.cgroups[pos++] = 128 * (bt >> 2) + 4 * lane + (bt & 3);
                         }
                     }
                 }
@@ -1044,6 +1055,12 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     float c = 0.f, LT = 0.f, LD = 0.f;
     DraftShape shape{0, 0.f, 0, 0.f};
     Stat st{-INFINITY, 0.f};
+    // the padding [G, Gp) of every buffer reads as an empty group (never written later)
+    for (int i = G + t; i < Gp; i += kGT)
+        for (int bf = 0; bf < kNBuf; ++bf) {
+            arrays[bf * 2 * Gp + i] = -INFINITY;
+            arrays[bf * 2 * Gp + Gp + i] = 0.f;
+        }
     float *gmax = arrays, *gsum = arrays + Gp;
     // thread 0: the accept test's gathers and results
     float ztx = 0.f, zdx = 0.f, u_k = 0.f, p_tok = NAN, q_tok = NAN;

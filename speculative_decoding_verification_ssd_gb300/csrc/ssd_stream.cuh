@@ -21,7 +21,7 @@ constexpr int kStreamMaxGroups = 3 * 32 * 32;  // groups per row the tail warp's
 // arrays with one entry per 64-token group.
 inline size_t stream_dyn_bytes(int V) {
     const size_t G = (static_cast<size_t>(V) + kGroupTokens - 1) / kGroupTokens;
-    const size_t Gp = (G + 31) & ~static_cast<size_t>(31);
+    const size_t Gp = (G + 127) & ~static_cast<size_t>(127);  // padded to whole 4 x 32-group strips
     return static_cast<size_t>(kStreamGroups) *
            (static_cast<size_t>(kStreamRingStages) * kStreamStageBytes +
             static_cast<size_t>(kStreamBuffers) * 2 * Gp * sizeof(float));
