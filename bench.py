@@ -175,7 +175,7 @@ def to_device(inp, torch, dev):
 
 def traffic_record(kernel_digest: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken of this build."""
-    path = os.path.join(ROOT, "profiles", "ssd_unit_kernel_c5_traffic.json")
+    path = os.path.join(ROOT, "profiles", "ssd_stream_kernel_c5_traffic.json")
     try:
         d = json.load(open(path))
     except Exception:
