@@ -1282,8 +1282,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             LT = gT.m + lg2(gT.S);
             LD = gD.m + lg2(gD.S);
             if (t == 0) {
-                p_tok = ex2(ztx * c - gT.m) / gT.S;
-                q_tok = ex2(zdx * c + draft_bias(shape, zdx, xt) - gD.m) / gD.S;
+                // the same operations for both, so identical rows give identical p and q
+                p_tok = ex2(fmaf(ztx, c, -gT.m)) / gT.S;
+                q_tok = ex2(fmaf(zdx, c, draft_bias(shape, zdx, xt) - gD.m)) / gD.S;
                 accept = (u_k * q_tok < p_tok) ? 1 : 0;
             }
             if (!want_p2) handoff(kKindPass, 1, 0.f, 0.f);

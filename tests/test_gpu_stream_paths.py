@@ -1,0 +1,128 @@
+"""Rarely taken paths of the streaming kernel (rows on the 16-byte grid), each
+compared with the float64 oracle:
+
+* a draft row equal to its target row: no residual mass, so the bonus prepared
+  for each position is drawn from p;
+* a fan-out with F_k above 64, where the top-F threshold is found by bisection
+  over the group maxima instead of from the lanes' two largest maxima;
+* rows whose logits are all equal, where every group reaches the threshold
+  (the candidate-group list overflows and all groups are re-read) and every
+  element ties (the candidate-key buffer overflows and the threshold is raised
+  by sorting) -- ties rank by ascending token id.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from tests._parity import Tally, compare_cache, compare_verify, lookup_from, np_out, to_device
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def ssd():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import speculative_decoding_verification_ssd_gb300 as m
+    from speculative_decoding_verification_ssd_gb300 import _build
+    _build.build()
+    return m
+
+
+def _pack(zt, zd, tok, u, taus, dtype):
+    B, K1, V = zt.shape
+    wl = synth.Workload("paths", B=B, K=K1 - 1, V=V, dtype=dtype, sigma_d=0, zipf_s=0, sigma_n=0,
+                        tau=1.0)
+    return {"tgt": synth.store(zt, dtype), "drf": synth.store(zd, dtype),
+            "tokens": tok.astype(np.int32), "uniforms": u.astype(np.float32),
+            "temperature": np.asarray(taus, np.float32), "workload": wl}
+
+
+def _round_and_compare(ssd, inp, budget, a_p, r):
+    wl = inp["workload"]
+    K, V = wl.K, wl.V
+    F, off = ssd.ssd_fanout(K, budget, a_p, r, V)
+    d = to_device(inp)
+    assert d["tgt"].data_ptr() % 16 == 0 and (V * wl.elem_bytes) % 16 == 0  # streaming path
+    g = np_out(ssd.ssd_round(d["tgt"], d["drf"], d["tokens"], d["uniforms"], d["temperature"], F,
+                             budget))
+    o = oracle.round_(inp["tgt"], inp["drf"], inp["tokens"], inp["uniforms"], inp["temperature"],
+                      wl.dtype, off, budget)
+    t = Tally()
+    compare_verify(g, o, K, t)
+    compare_cache(g["cache_tok"], o, off, K, t)
+    h, s = lookup_from(g["cache_tok"], off, g["accept_len"], g["bonus"])
+    np.testing.assert_array_equal(g["hit"], h)
+    np.testing.assert_array_equal(g["slot"], s)
+    t.check()
+    return g, o, F
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_draft_equal_to_target_prepares_bonus_from_p(ssd, dtype):
+    """q = p: every position accepts (u < 1), and the bonus the round would draw had it
+    stopped at k -- prepared for every k and kept in the workspace record -- comes from
+    p_k, since the residual has no mass."""
+    rng = np.random.default_rng(31)
+    B, K, V = 8, 3, 20000
+    zt = (rng.standard_normal((B, K + 1, V)) * 2.5).astype(np.float32)
+    zd = zt[:, :K].copy()
+    tok = rng.integers(0, V, (B, K))
+    u = rng.random((B, K + 1))
+    inp = _pack(zt, zd, tok, u, [1.0] * B, dtype)
+    budget, a_p, r = 24, 0.7, 0.5
+    F, off = ssd.ssd_fanout(K, budget, a_p, r, V)
+    d = to_device(inp)
+    ws = ssd.workspace(B, K)
+    g = np_out(ssd.ssd_round(d["tgt"], d["drf"], d["tokens"], d["uniforms"], d["temperature"], F,
+                             budget, workspace=ws))
+    rec = ws[: B * (K + 1) * 32].view(torch.int32).reshape(B, K + 1, 8).cpu().numpy()
+    o = oracle.round_(inp["tgt"], inp["drf"], inp["tokens"], inp["uniforms"], inp["temperature"],
+                      dtype, off, budget)
+    t = Tally()
+    compare_verify(g, o, K, t)
+    compare_cache(g["cache_tok"], o, off, K, t)
+    t.check()
+    assert (g["accept_len"] == K).all()
+    zs = synth.stored_to_f32(inp["tgt"], dtype)
+    checked = 0
+    for b in range(B):
+        for k in range(K):
+            p = oracle.softmax(zs[b, k].astype(np.float64), 1.0)
+            cum = np.cumsum(p)
+            T = float(inp["uniforms"][b, K]) * cum[-1]
+            want = int(np.searchsorted(cum, T, side="right"))
+            if abs(cum[min(want, V - 1)] - T) < 1e-6 or (want > 0 and abs(cum[want - 1] - T) < 1e-6):
+                continue  # too close to a boundary to be a clean decision
+            assert rec[b, k, 3] == want, (b, k, rec[b, k, 3], want)
+            checked += 1
+    assert checked >= B * K - 2
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_fanout_above_64_uses_bisection(ssd, dtype):
+    rng = np.random.default_rng(32)
+    B, K, V = 6, 2, 24000
+    zt = (rng.standard_normal((B, K + 1, V)) * 2.5).astype(np.float32)
+    zd = (zt[:, :K] + rng.standard_normal((B, K, V)) * 0.8).astype(np.float32)
+    tok = np.argmax(zd, axis=-1)
+    u = rng.random((B, K + 1))
+    _, _, F = _round_and_compare(ssd, _pack(zt, zd, tok, u, [1.0, 0.0, 0.7] * 2, dtype), 450, 0.8, 0.5)
+    assert max(F) > 64
+
+
+def test_all_equal_rows_overflow_both_candidate_buffers(ssd):
+    rng = np.random.default_rng(33)
+    B, K, V = 4, 2, 128256
+    zt = (rng.standard_normal((B, K + 1, V)) * 2.0).astype(np.float32)
+    zd = (zt[:, :K] + rng.standard_normal((B, K, V)) * 0.8).astype(np.float32)
+    zt[0] = 0.0          # sampled sequence, all rows flat; draft flat too
+    zd[0] = 0.0
+    zt[1, :, :] = 1.5    # greedy sequence with flat target rows
+    zt[2, 1] = -3.0      # one flat target row among random ones
+    tok = rng.integers(0, V, (B, K))
+    u = rng.random((B, K + 1))
+    _round_and_compare(ssd, _pack(zt, zd, tok, u, [1.0, 0.0, 1.0, 0.0], "bf16"), 32, 0.75, 0.5)
