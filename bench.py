@@ -51,6 +51,13 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch (greedy share scaled); for profiling")
+    ap.add_argument("--study", choices=["fanout"], default=None,
+                    help="fanout: cache hit rate of the geometric and the uniform fan-out at "
+                         "several temperatures, with the batch all-hit rate p_hit^b")
+    ap.add_argument("--study-draws", type=int, default=4,
+                    help="independent draft-token draws per temperature (study mode)")
+    ap.add_argument("--study-rounds", type=int, default=64,
+                    help="rounds with fresh uniforms per draft-token draw (study mode)")
     return ap.parse_args()
 
 
@@ -328,7 +335,7 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
-                     "traffic": traffic_record(_build.source_digest()),
+                     "traffic": traffic_record(_build.stream_kernel_digest()),
                      "kernel": "ssd_stream_kernel<BF16Tag>"},
         "e2e": {"value": world * args.e2e_steps / (e2e_ms * 1e-3), "unit": "rounds/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -398,11 +405,89 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_fanout_study(args):
+    """Cache-topology comparison of the Saguaro notes ("关键设计" item 1 and the
+    component analysis): the same synthetic round (the workload's shapes, every
+    sequence at one temperature) is run with the geometric and with the uniform
+    fan-out of the same budget, and the share of sequences whose true outcome
+    (a, t*) was cached is counted.  For a batch of b sequences the round only
+    avoids the fallback when all b hit (item 3): the empirical all-hit rate of
+    consecutive groups of b is reported beside p_hit^b."""
+    import torch
+    import speculative_decoding_verification_ssd_gb300 as ssd
+    wl = chosen_workload(args).replace(greedy_first=0)
+    if wl.budget == 0:
+        wl = synth.WORKLOADS["c5"].replace(B=wl.B, K=wl.K, V=wl.V, dtype=wl.dtype)
+    B, K, V = wl.B, wl.K, wl.V
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    rng = np.random.default_rng(synth.BENCH_SEED[WORKLOAD] + 17)
+    tgt, drf = synth.make_logits(wl, rng)
+    tt = torch.from_numpy(tgt.view(np.int16) if wl.dtype == synth.BF16 else tgt).to(dev)
+    td = torch.from_numpy(drf.view(np.int16) if wl.dtype == synth.BF16 else drf).to(dev)
+    if wl.dtype == synth.BF16:
+        tt, td = tt.view(torch.bfloat16), td.view(torch.bfloat16)
+    drf_f32 = synth.stored_to_f32(drf, wl.dtype)
+    sizes = [b for b in (1, 2, 4, 8, 16, 32, 64, 128, 256) if b <= B]
+    ws = ssd.workspace(B, K, dev)
+    rows = []
+    for tau in (0.0, 0.7, 1.0):
+        taus = np.full(B, tau, np.float32)
+        t_dev = torch.from_numpy(taus).to(dev)
+        draws = [(torch.from_numpy(synth.sample_draft_tokens(rng, drf_f32, taus)).to(dev),
+                  [torch.from_numpy(rng.random((B, K + 1), dtype=np.float32)).to(dev)
+                   for _ in range(args.study_rounds)]) for _ in range(args.study_draws)]
+        # the acceptance rate seen at this temperature (maximum likelihood of a geometric
+        # accepted length truncated at K: accepted positions / tested positions) gives
+        # the fan-out's a_p its fitted value
+        a = torch.cat([ssd.ssd_round(tt, td, tok, draws[0][1][0], t_dev,
+                                     ssd.ssd_fanout_uniform(K, wl.budget, V)[0], wl.budget,
+                                     probs=False, workspace=ws)["accept_len"] for tok, _ in draws])
+        a = a.cpu().numpy()
+        tested = int((a + (a < K)).sum())
+        a_fit = min(max(float(a.sum()) / max(tested, 1), 0.01), 0.99)
+        shapes = {"geometric": (ssd.ssd_fanout(K, wl.budget, wl.a_p, wl.r, V), wl.a_p),
+                  "geometric_fitted": (ssd.ssd_fanout(K, wl.budget, a_fit, wl.r, V), a_fit),
+                  "uniform": (ssd.ssd_fanout_uniform(K, wl.budget, V), None)}
+        hits = {name: [] for name in shapes}
+        acc = {name: [] for name in shapes}
+        for tokens, us in draws:
+            for u in us:
+                for name, ((F, _), _) in shapes.items():
+                    o = ssd.ssd_round(tt, td, tokens, u, t_dev, F, wl.budget, probs=False,
+                                      workspace=ws)
+                    hits[name].append(o["hit"])
+                    acc[name].append(o["accept_len"])
+        torch.cuda.synchronize()
+        for name, ((F, _), a_p) in shapes.items():
+            H = torch.stack(hits[name]).cpu().numpy().astype(bool)      # [rounds, B]
+            A = torch.stack(acc[name]).cpu().numpy()
+            p_hat = float(H.mean())
+            all_hit = {}
+            for b in sizes:
+                g = H[:, : (B // b) * b].reshape(H.shape[0], B // b, b).all(axis=2)
+                all_hit[str(b)] = {"empirical": float(g.mean()), "p_hit^b": p_hat ** b}
+            rows.append({"tau": tau, "fanout": name, "a_p": a_p, "F": [int(f) for f in F],
+                         "hit_rate": p_hat, "accept_mean": float(A.mean()),
+                         "hit_rate_by_accept_len": {
+                             str(k): float(H[A == k].mean()) if (A == k).any() else None
+                             for k in range(K + 1)},
+                         "batch_all_hit": all_hit})
+    line = {"study": "fanout", "workload": f"{wl.name}-shaped: B={B}, K={K}, V={V} {wl.dtype}, "
+            f"budget {wl.budget}, geometric a_p={wl.a_p} r={wl.r}",
+            "data": "synthetic (seeded Gaussian + Zipf log-bias logits; no datasets, no weights)",
+            "rounds_per_temperature": args.study_draws * args.study_rounds,
+            "rows": rows}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
-    if args.impl == "reference":
+    if args.study == "fanout":
+        run_fanout_study(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

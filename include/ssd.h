@@ -149,6 +149,29 @@ int ssd_fanout(int K, int budget, double a_p, double r, int V, int32_t *F_host,
                int32_t *off_host);
 
 /*
+ * ssd_fanout_uniform -- the uniform fan-out that [SSD] item 1 compares the
+ * geometric shape against: every accepted length k = 0..K gets the same share,
+ * F_k = floor(budget / (K+1)), plus one for the first budget mod (K+1)
+ * positions; each F_k is then clamped to V.  Outputs as ssd_fanout.
+ * Requires budget >= 0, V >= 1.
+ */
+int ssd_fanout_uniform(int K, int budget, int V, int32_t *F_host, int32_t *off_host);
+
+/*
+ * ssd_backup_fill -- the fast random-token backup speculator of [SSD] item 3
+ * (batch-size-aware fallback): for every sequence whose round missed the
+ * cache (hit[b] == 0) the next round's K draft tokens are drawn uniformly
+ * from the vocabulary, next_tokens[b, i] = min(V - 1, floor(u[b, i] * V))
+ * with the caller's uniforms u [B, K] in [0, 1) (the product is taken exactly
+ * in double; an fp32 uniform resolves 2^-24, so with V above 2^24 the top ids
+ * are never drawn); rows of sequences that hit are left untouched.  hit [B] uint8, uniforms
+ * [B, K] fp32, next_tokens [B, K] int32, all device pointers owned by the
+ * caller.  Requires B >= 1, 1 <= K <= SSD_MAX_K, V >= 1.
+ */
+int ssd_backup_fill(const uint8_t *hit, const float *uniforms, int B, int K, int V,
+                    int32_t *next_tokens, void *stream);
+
+/*
  * ssd_reshape_draft -- [SSD] item 2 on `rows` independent draft rows
  * drf [rows, V]: the top-F set of each row (raw logits, lowest id on ties) and,
  * when q_out is not NULL, the reshaped distribution

@@ -47,6 +47,10 @@ def lib():
         L.oracle_sigma.restype = i
         L.oracle_fanout.argtypes = [i, i, d, d, i, P, P, P]
         L.oracle_fanout.restype = i
+        L.oracle_fanout_uniform.argtypes = [i, i, i, P, P]
+        L.oracle_fanout_uniform.restype = i
+        L.oracle_backup_fill.argtypes = [P, P, i, i, i, P]
+        L.oracle_backup_fill.restype = None
         L.oracle_verify.argtypes = [i, i, i, i, i, i, P, P, i, P, P, P, i, d,
                                     P, P, P, P, P, P, P]
         L.oracle_verify.restype = i
@@ -117,6 +121,25 @@ def fanout(K: int, budget: int, a_p: float, r: float, V: int = 1 << 30):
     if rc != 0:
         raise ValueError("invalid fan-out parameters")
     return F, off, x
+
+
+def fanout_uniform(K: int, budget: int, V: int = 1 << 30):
+    """Uniform fan-out: returns (F [K+1], off [K+2])."""
+    F = np.empty(K + 1, dtype=np.int32)
+    off = np.empty(K + 2, dtype=np.int32)
+    if lib().oracle_fanout_uniform(int(K), int(budget), int(V), _ptr(F), _ptr(off)) != 0:
+        raise ValueError("invalid fan-out parameters")
+    return F, off
+
+
+def backup_fill(hit, uniforms, V: int, next_tokens):
+    """Random-token backup: fills next_tokens [B, K] (int32, in place) for hit == 0."""
+    hit = np.ascontiguousarray(hit, dtype=np.uint8)
+    u = np.ascontiguousarray(uniforms, dtype=np.float32)
+    assert next_tokens.dtype == np.int32 and next_tokens.flags.c_contiguous
+    B, K = u.shape
+    lib().oracle_backup_fill(_ptr(hit), _ptr(u), int(B), int(K), int(V), _ptr(next_tokens))
+    return next_tokens
 
 
 # ---------------------------------------------------------------------------

@@ -16,7 +16,8 @@
  *   [WHY]  "Why does speculative decoding exist?" (til.phipham141.dev), section
  *          "How it works", Fix 2 / Fix 3 (bonus token, greedy rule).
  *   [SSD]  "Speculative Speculative Decoding" notes (papernotes.org), section
- *          "关键设计" items 1 (fan-out) and 2 (SAGUARO sampling), and the SSD
+ *          "关键设计" items 1 (fan-out), 2 (SAGUARO sampling) and 3 (batch-aware
+ *          fallback, random-token backup), and the SSD
  *          iteration of section "整体框架" (outcome (k, t*), cache S_T, hit test).
  *
  * Readings where the pages are silent (each also listed in the design notes):
@@ -28,6 +29,8 @@
  *   - Z == 0 in the residual: the bonus is drawn from p at that row instead;
  *   - greedy (tau == 0): compare raw stored logits, lowest id wins ties;
  *   - fan-out: real-valued F_k rounded by the largest-remainder method;
+ *   - uniform fan-out: floor(budget/(K+1)) each, remainder to the lowest k;
+ *   - random backup token: floor(u * V) for a supplied uniform u in [0, 1);
  *   - cache scores: (p_k - q_k)^+ for k < K, p_K for k = K (tau > 0); raw target
  *     logits with the drafted token excluded (tau == 0).
  */
@@ -235,6 +238,54 @@ int oracle_fanout(int K, int budget, double a_p, double r, int V, int *F, int *o
     free(x);
     free(w);
     return 0;
+}
+
+/* ------------------------------------------------------------------------
+ * [SSD] item 1, uniform fan-out: the allocation the geometric shape is
+ * compared with (and beats at higher temperature): the budget is spread evenly
+ * over the K+1 accepted lengths.  Reading: equal integer shares floor(budget/(K+1)),
+ * the remainder one slot each to the lowest k, each share clamped to V.
+ * Writes F[0..K], off[0..K+1].  Returns 0 or -1.
+ * ------------------------------------------------------------------------ */
+int oracle_fanout_uniform(int K, int budget, int V, int *F, int *off)
+{
+    if (K < 1 || budget < 0 || V < 1)
+        return -1;
+    off[0] = 0;
+    for (int k = 0; k <= K; ++k) {
+        int f = budget / (K + 1);
+        if (k < budget % (K + 1))
+            f += 1;
+        if (f > V)
+            f = V;
+        F[k] = f;
+        off[k + 1] = off[k] + f;
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------
+ * [SSD] item 3, fast backup speculator: at large batch the sequences that miss
+ * the cache are re-drafted by a very fast, low-quality speculator; the notes
+ * name random tokens as the one implemented.  Reading: token i of sequence b
+ * is floor(u[b, i] * V) (clamped to V-1) for a uniform u in [0, 1) supplied by
+ * the caller, for every sequence with hit[b] == 0; other rows are untouched.
+ * ------------------------------------------------------------------------ */
+void oracle_backup_fill(const unsigned char *hit, const float *u, int B, int K, int V, int *next)
+{
+    for (int b = 0; b < B; ++b) {
+        if (hit[b])
+            continue;
+        for (int i = 0; i < K; ++i) {
+            double x = (double)u[(size_t)b * K + i] * (double)V;
+            long t = (long)floor(x);
+            if (t > V - 1)
+                t = V - 1;
+            if (t < 0)
+                t = 0;
+            next[(size_t)b * K + i] = (int)t;
+        }
+    }
 }
 
 /* --------------------------------------------------------------------------

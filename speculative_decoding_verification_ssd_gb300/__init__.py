@@ -41,7 +41,8 @@ LIB_PATH = _build.LIB
 # Symbols declared in include/ssd.h.
 ABI_SYMBOLS = ("ssd_strerror", "ssd_version", "ssd_workspace_size", "ssd_verify", "ssd_fanout",
                "ssd_reshape_draft", "ssd_build_cache", "ssd_cache_lookup", "ssd_round",
-               "ssd_noalloc_max_scratch", "ssd_round_noalloc")
+               "ssd_noalloc_max_scratch", "ssd_round_noalloc", "ssd_fanout_uniform",
+               "ssd_backup_fill")
 
 
 class SSDError(RuntimeError):
@@ -87,6 +88,10 @@ def lib() -> ctypes.CDLL:
         L.ssd_round_noalloc.argtypes = [P, P, i, i, i, i, i, P, P, P, P, P, i, P, P, P, P, P, P, P, P,
                                         P]
         L.ssd_round_noalloc.restype = i
+        L.ssd_fanout_uniform.argtypes = [i, i, i, P, P]
+        L.ssd_fanout_uniform.restype = i
+        L.ssd_backup_fill.argtypes = [P, P, i, i, i, P, P]
+        L.ssd_backup_fill.restype = i
         _lib = L
     return _lib
 
@@ -155,6 +160,15 @@ def ssd_fanout(K: int, budget: int, a_p: float, r: float, V: int):
     off = np.empty(K + 2, np.int32)
     _check(lib().ssd_fanout(int(K), int(budget), float(a_p), float(r), int(V), _ptr(F), _ptr(off)),
            "ssd_fanout")
+    return F, off
+
+
+def ssd_fanout_uniform(K: int, budget: int, V: int):
+    """Uniform fan-out: (F [K+1], off [K+2]) as numpy int32 arrays."""
+    F = np.empty(K + 1, np.int32)
+    off = np.empty(K + 2, np.int32)
+    _check(lib().ssd_fanout_uniform(int(K), int(budget), int(V), _ptr(F), _ptr(off)),
+           "ssd_fanout_uniform")
     return F, off
 
 
@@ -257,6 +271,21 @@ def ssd_cache_lookup(cache_tok, F, accept_len, bonus, *, hit=None, slot=None, st
         _ptr(_dev(bonus, "bonus", torch.int32)), _ptr(hit), _ptr(slot), _stream(stream)),
         "ssd_cache_lookup")
     return hit, slot
+
+
+def ssd_backup_fill(hit, uniforms, V: int, next_tokens, *, stream=None):
+    """Random-token backup for the sequences that missed: next_tokens [B, K] int32 is
+    written in place where hit[b] == 0 (token floor(u * V)); returns next_tokens."""
+    _dev(hit, "hit", torch.uint8)
+    _dev(uniforms, "uniforms", torch.float32)
+    _dev(next_tokens, "next_tokens", torch.int32)
+    if uniforms.dim() != 2 or tuple(next_tokens.shape) != tuple(uniforms.shape) \
+            or hit.shape != (uniforms.shape[0],):
+        raise ValueError("uniforms and next_tokens must be [B, K] and hit [B]")
+    B, K = uniforms.shape
+    _check(lib().ssd_backup_fill(_ptr(hit), _ptr(uniforms), B, K, int(V), _ptr(next_tokens),
+                                 _stream(stream)), "ssd_backup_fill")
+    return next_tokens
 
 
 def ssd_round(tgt, drf, tokens, uniforms, temperature, F, budget, reshape=None, *, out=None,

@@ -21,7 +21,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libssd.so")
 
-SOURCES = ["ssd_unit.cu", "ssd_stream.cu", "ssd_reshape.cu", "ssd_api.cu", "ssd_fanout.cpp"]
+SOURCES = ["ssd_unit.cu", "ssd_stream.cu", "ssd_reshape.cu", "ssd_api.cu", "ssd_fanout.cpp", "ssd_backup.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -45,15 +45,22 @@ def _inputs_digest() -> str:
     return h.hexdigest()
 
 
-def source_digest() -> str:
-    """Digest of the kernel sources (used to tag profiles taken of this build)."""
+def source_digest(names=None) -> str:
+    """Digest of kernel sources (used to tag profiles taken of a build): all of csrc/,
+    or only the named files."""
     h = hashlib.sha256()
-    for name in sorted(os.listdir(CSRC)):
+    for name in sorted(names if names is not None else os.listdir(CSRC)):
         p = os.path.join(CSRC, name)
         if os.path.isfile(p):
             h.update(name.encode())
             h.update(open(p, "rb").read())
     return h.hexdigest()[:16]
+
+
+def stream_kernel_digest() -> str:
+    """Digest of the streaming kernel's translation unit: ssd_stream.cu and the
+    device headers it includes."""
+    return source_digest(["ssd_stream.cu"] + [n for n in os.listdir(CSRC) if n.endswith(".cuh")])
 
 
 def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:

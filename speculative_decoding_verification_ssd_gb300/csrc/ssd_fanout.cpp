@@ -53,3 +53,20 @@ extern "C" int ssd_fanout(int K, int budget, double a_p, double r, int V, int32_
     }
     return SSD_OK;
 }
+
+// The uniform fan-out the geometric shape is compared against in [SSD] item 1:
+// an equal share of the budget for every accepted length, the remainder going
+// one slot each to the lowest k, each share clamped to V.
+extern "C" int ssd_fanout_uniform(int K, int budget, int V, int32_t *F_host, int32_t *off_host) {
+    if (K < 1 || K > SSD_MAX_K || budget < 0 || V < 1 || !F_host || !off_host)
+        return SSD_ERR_INVALID_ARG;
+    const int share = budget / (K + 1);
+    const int extra = budget % (K + 1);
+    off_host[0] = 0;
+    for (int k = 0; k <= K; ++k) {
+        const int f = share + (k < extra ? 1 : 0);
+        F_host[k] = f > V ? V : f;
+        off_host[k + 1] = off_host[k] + F_host[k];
+    }
+    return SSD_OK;
+}

@@ -86,6 +86,20 @@ def test_fanout_rejects_bad_arguments(ssd):
         assert e.value.status == ssd.SSD_ERR_INVALID_ARG
 
 
+def test_fanout_uniform_matches_oracle(ssd):
+    for K in range(1, 33):
+        for budget in [0, 1, K, K + 1, 2 * K + 3, 32, 64, 255, 1000]:
+            for V in [1, 3, 50, 128256]:
+                F, off = ssd.ssd_fanout_uniform(K, budget, V)
+                Fo, offo = oracle.fanout_uniform(K, budget, V)
+                np.testing.assert_array_equal(F, Fo)
+                np.testing.assert_array_equal(off, offo)
+    for args in [(0, 10, 10), (33, 10, 10), (3, -1, 10), (3, 10, 0)]:
+        with pytest.raises(ssd.SSDError) as e:
+            ssd.ssd_fanout_uniform(*args)
+        assert e.value.status == ssd.SSD_ERR_INVALID_ARG
+
+
 def _fake(addr=0x10000):
     return ctypes.c_void_p(addr)
 
@@ -134,6 +148,13 @@ def test_device_calls_validate_before_any_cuda_call(ssd):
                        p, ws_ok, None, None) == ssd.SSD_ERR_INVALID_ARG  # hit missing
     assert L.ssd_cache_lookup(p, 4, 2, 5, Fp, p, p, p, p, None) == ssd.SSD_ERR_INVALID_ARG
     assert L.ssd_cache_lookup(p, 0, 2, 6, Fp, p, p, p, p, None) == ssd.SSD_ERR_INVALID_ARG
+    bf = L.ssd_backup_fill
+    assert bf(p, p, 0, 4, 100, p, None) == ssd.SSD_ERR_INVALID_ARG
+    assert bf(p, p, 4, 0, 100, p, None) == ssd.SSD_ERR_INVALID_ARG
+    assert bf(p, p, 4, 33, 100, p, None) == ssd.SSD_ERR_INVALID_ARG
+    assert bf(p, p, 4, 2, 0, p, None) == ssd.SSD_ERR_INVALID_ARG
+    assert bf(None, p, 4, 2, 100, p, None) == ssd.SSD_ERR_INVALID_ARG
+    assert bf(p, p, 4, 2, 100, None, None) == ssd.SSD_ERR_INVALID_ARG
     rs = L.ssd_reshape_draft
     assert rs(p, 3, 4, 100, p, 8, ctypes.c_float(0.5), p, None, None, None) == ssd.SSD_ERR_DTYPE
     assert rs(p, 0, 4, 100, p, 300, ctypes.c_float(0.5), p, None, None, None) == ssd.SSD_ERR_INVALID_ARG

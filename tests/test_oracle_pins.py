@@ -360,6 +360,85 @@ def test_fanout_rejects_bad_parameters():
             oracle.fanout(*args)
 
 
+@pytest.mark.parametrize("K,budget", [(1, 0), (1, 5), (2, 7), (3, 4), (3, 9), (4, 6)])
+def test_fanout_uniform_is_the_even_split(K, budget):
+    """Brute force over every allocation of the budget to the K+1 lengths: the even
+    split is the only one whose shares differ by at most one and that gives the
+    spare slots to the shortest accepted lengths (non-increasing in k)."""
+    import itertools
+    best = [F for F in itertools.product(range(budget + 1), repeat=K + 1)
+            if sum(F) == budget and max(F) - min(F) <= 1
+            and all(F[k] >= F[k + 1] for k in range(K))]
+    assert len(best) == 1
+    F, off = oracle.fanout_uniform(K, budget)
+    assert tuple(F) == best[0]
+    assert list(off) == [0] + list(np.cumsum(best[0]))
+
+
+@pytest.mark.parametrize("K,budget", [(4, 32), (6, 64), (3, 10), (8, 100), (2, 1)])
+def test_fanout_uniform_is_the_flat_limit_of_the_geometric_shape(K, budget):
+    """As r grows the geometric shape F_0 a_p^{k/(1+r)} flattens to one value for every
+    k (the all-accepted factor (1-a_p)^{-1/(1+r)} goes to 1 as well): the geometric
+    allocation at r = 1e6 must equal the uniform one."""
+    Fu, offu = oracle.fanout_uniform(K, budget)
+    Fg, offg, _ = oracle.fanout(K, budget, 0.5, 1e6)
+    np.testing.assert_array_equal(Fu, Fg)
+    np.testing.assert_array_equal(offu, offg)
+
+
+def test_fanout_uniform_clamps_and_rejects():
+    F, off = oracle.fanout_uniform(2, 100, V=20)
+    assert list(F) == [20, 20, 20] and off[-1] == 60
+    for args in [(0, 10), (3, -1)]:
+        with pytest.raises(ValueError):
+            oracle.fanout_uniform(*args)
+
+
+# ---------------------------------------------------------------------------
+# Random-token backup.
+# ---------------------------------------------------------------------------
+
+def test_backup_fill_brute_force():
+    """Exact rational arithmetic: token = floor(u * V) of the float u as a fraction,
+    only on the rows that missed; rows that hit keep their previous contents."""
+    from fractions import Fraction
+    rng = np.random.default_rng(7)
+    B, K = 12, 5
+    below1 = np.nextafter(np.float32(1), np.float32(0))
+    for V in [1, 2, 3, 1000, 128256, 152064, (1 << 24) + 3]:
+        u = rng.random((B, K)).astype(np.float32)
+        u[0, 0], u[0, 1] = 0.0, below1
+        u[0, 2] = np.float32(0.5)
+        hit = (rng.random(B) < 0.4).astype(np.uint8)
+        hit[0] = 0
+        nxt = np.full((B, K), -7, np.int32)
+        oracle.backup_fill(hit, u, V, nxt)
+        for b in range(B):
+            for i in range(K):
+                want = -7 if hit[b] else int(Fraction(float(u[b, i])) * V // 1)
+                assert nxt[b, i] == want, (V, b, i)
+        assert nxt[0, 0] == 0 and nxt[0, 2] == V // 2
+        if V <= 1 << 24:  # an fp32 uniform resolves 2^-24: larger vocabularies lose the top ids
+            assert nxt[0, 1] == V - 1
+
+
+def test_backup_fill_is_uniform_over_the_vocabulary():
+    """Uniforms on an even grid of n = 64 V points land exactly 64 times on each
+    token; random uniforms pass a chi-square test."""
+    V = 1000
+    n = 64 * V
+    u = ((np.arange(n, dtype=np.float64) + 0.5) / n).astype(np.float32).reshape(1, n)
+    nxt = np.zeros((1, n), np.int32)
+    oracle.backup_fill(np.zeros(1, np.uint8), u, V, nxt)
+    np.testing.assert_array_equal(np.bincount(nxt[0], minlength=V), np.full(V, 64))
+    rng = np.random.default_rng(8)
+    u = rng.random((200, 500)).astype(np.float32)
+    nxt = np.zeros((200, 500), np.int32)
+    oracle.backup_fill(np.zeros(200, np.uint8), u, V, nxt)
+    counts = np.bincount(nxt.ravel(), minlength=V)
+    assert scipy.stats.chisquare(counts).pvalue > 1e-4
+
+
 # ---------------------------------------------------------------------------
 # sigma_{F,C} reshape.
 # ---------------------------------------------------------------------------
