@@ -51,9 +51,11 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch (greedy share scaled); for profiling")
-    ap.add_argument("--study", choices=["fanout"], default=None,
+    ap.add_argument("--study", choices=["fanout", "csweep"], default=None,
                     help="fanout: cache hit rate of the geometric and the uniform fan-out at "
-                         "several temperatures, with the batch all-hit rate p_hit^b")
+                         "several temperatures, with the batch all-hit rate p_hit^b; "
+                         "csweep: draft-only cache keys with sigma_{F_k,C} drafting, hit rate "
+                         "and acceptance as C goes from 1 to 0")
     ap.add_argument("--study-draws", type=int, default=4,
                     help="independent draft-token draws per temperature (study mode)")
     ap.add_argument("--study-rounds", type=int, default=64,
@@ -481,12 +483,88 @@ def run_fanout_study(args):
     print(json.dumps(line), flush=True)
 
 
+def run_csweep_study(args):
+    """The acceptance / cache-hit trade-off of SAGUARO sampling (the Saguaro notes,
+    "关键设计" item 2): the cache keys of outcome k are the F_k best draft tokens of
+    draft row k (the drafted token left out), and the draft samples x~_k from
+    sigma_{F_k,C}, which scales the weight of those same tokens by C.  Lower C moves
+    residual mass onto the cached tokens (more hits) and moves q away from p (fewer
+    acceptances).  Per C: draft keys and descriptors (ssd_draft_cache), drafting by
+    Gumbel-max on the device (input synthesis, not a step of the method), then
+    rounds of ssd_verify on the reshaped q and ssd_cache_lookup."""
+    import torch
+    import speculative_decoding_verification_ssd_gb300 as ssd
+    wl = chosen_workload(args).replace(greedy_first=0)
+    if wl.budget == 0:
+        wl = synth.WORKLOADS["c5"].replace(B=wl.B, K=wl.K, V=wl.V, dtype=wl.dtype)
+    B, K, V = wl.B, wl.K, wl.V
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    rng = np.random.default_rng(synth.BENCH_SEED[WORKLOAD] + 29)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(int(rng.integers(1 << 62)))
+    tgt, drf = synth.make_logits(wl, rng, draft_rows=K + 1)
+
+    def logits(a):
+        if wl.dtype == synth.F32:
+            return torch.from_numpy(a).to(dev)
+        return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+
+    tt, td = logits(tgt), logits(drf)
+    zd = td[:, :K].float()
+    F, _ = ssd.ssd_fanout(K, wl.budget, wl.a_p, wl.r, V)
+    ids = torch.arange(V, device=dev)
+    sizes = [b for b in (1, 4, 16, 64) if b <= B]
+    rows = []
+    for tau in (0.7, 1.0):
+        taus = torch.full((B,), tau, dtype=torch.float32, device=dev)
+        for C in (1.0, 0.75, 0.5, 0.25, 0.1, 0.0):
+            _, desc = ssd.ssd_draft_cache(td, None, F, wl.budget, C, cache=False, reshape=True)
+            thr_val, thr_id, _, _ = ssd.desc_fields(desc)
+            thr_val = thr_val.view(B, K, 1)
+            thr_id = thr_id.view(B, K, 1)
+            member = (zd > thr_val) | ((zd == thr_val) & (ids.view(1, 1, V) <= thr_id))
+            logc = torch.where(member, torch.tensor(float(np.log(C)) if C > 0 else -float("inf"),
+                                                    device=dev), torch.zeros((), device=dev))
+            H, A = [], []
+            for _ in range(args.study_draws):
+                g = -torch.log(-torch.log(torch.rand(zd.shape, generator=gen, device=dev)
+                                          .clamp_min(1e-30)))
+                tokens = torch.argmax(zd / tau + logc + g, dim=-1).to(torch.int32).contiguous()
+                cache, desc = ssd.ssd_draft_cache(td, tokens, F, wl.budget, C, reshape=True)
+                for _ in range(args.study_rounds):
+                    u = torch.rand((B, K + 1), generator=gen, device=dev)
+                    v = ssd.ssd_verify(tt, td, tokens, u, taus, reshape=desc, probs=False)
+                    h, _ = ssd.ssd_cache_lookup(cache, F, v["accept_len"], v["bonus"])
+                    H.append(h)
+                    A.append(v["accept_len"])
+            H = torch.stack(H).cpu().numpy().astype(bool)
+            A = torch.stack(A).cpu().numpy()
+            tested = int((A + (A < K)).sum())
+            p_hat = float(H.mean())
+            rows.append({
+                "tau": tau, "C": C, "hit_rate": p_hat, "accept_mean": float(A.mean()),
+                "acceptance_rate": float(A.sum()) / max(tested, 1),
+                "tokens_per_round": float(A.mean()) + 1.0,
+                "batch_all_hit": {str(b): {
+                    "empirical": float(H[:, : (B // b) * b].reshape(H.shape[0], B // b, b)
+                                       .all(axis=2).mean()),
+                    "p_hit^b": p_hat ** b} for b in sizes}})
+    line = {"study": "csweep", "workload": f"{wl.name}-shaped: B={B}, K={K}, V={V} {wl.dtype}, "
+            f"K+1 draft rows, budget {wl.budget}, geometric F={[int(f) for f in F]}",
+            "data": "synthetic (seeded Gaussian + Zipf log-bias logits; no datasets, no weights)",
+            "rounds_per_point": args.study_draws * args.study_rounds, "rows": rows}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
     if args.study == "fanout":
         run_fanout_study(args)
+    elif args.study == "csweep":
+        run_csweep_study(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

@@ -185,6 +185,30 @@ int ssd_reshape_draft(const void *drf, int dtype, int rows, int V, const float *
                       void *stream);
 
 /*
+ * ssd_draft_cache -- the draft side of a Saguaro round ([SSD] item 2: the
+ * cache keys are chosen from the draft logits; sampling is reshaped by
+ * sigma_{F,C} with F the position's fan-out).  drf [B, K+1, V] holds the draft
+ * logits of positions 0..K of every sequence (row K: the draft's distribution
+ * after all K drafted tokens, which the all-accepted outcome needs).
+ * For each sequence b and position k = 0..K, segment k of cache_tok[b]
+ * (columns off[k] .. off[k+1], off the prefix sums of F_host) receives the
+ * F_k tokens of largest raw draft logit at row k, best first (ties to the
+ * lowest id), leaving out the drafted token x~_k = tokens[b, k] for k < K;
+ * a slot with no token left (F_k == V and x~_k excluded) holds -1.
+ * tokens may be NULL (nothing left out).  desc [B, K] (may be NULL) receives
+ * the sigma_{F_k,C} descriptor of draft row k < K (ssd_reshape_desc, same
+ * set as ssd_reshape_draft with F = F_k); give it to ssd_verify / ssd_round
+ * with drf_rows = K+1 so that verification uses the reshaped q.
+ * At least one of cache_tok and desc must be non-NULL.  Requires
+ * 1 <= K <= SSD_MAX_K, V >= 2, 0 <= F_k <= min(V, SSD_MAX_F),
+ * budget >= sum F_k, and with desc: 0 <= C <= 1, not (C == 0 and F_k >= V).
+ * One thread-block cluster per draft row; every row is read once.
+ */
+int ssd_draft_cache(const void *drf, int dtype, int B, int K, int V, const int32_t *tokens,
+                    const int32_t *F_host, int budget, float C, int32_t *cache_tok,
+                    ssd_reshape_desc *desc, int32_t *dev_status, void *stream);
+
+/*
  * ssd_build_cache -- the speculation-cache keys of [SSD] "整体框架" / item 1:
  * for each sequence b and accepted length k = 0..K, the F_k bonus tokens most
  * likely to be drawn at outcome (k, t*), ranked by (score desc, id asc):

@@ -51,10 +51,14 @@ def lib():
         L.oracle_fanout_uniform.restype = i
         L.oracle_backup_fill.argtypes = [P, P, i, i, i, P]
         L.oracle_backup_fill.restype = None
-        L.oracle_verify.argtypes = [i, i, i, i, i, i, P, P, i, P, P, P, i, d,
+        L.oracle_verify.argtypes = [i, i, i, i, i, i, P, P, i, P, P, P, i, P, d,
                                     P, P, P, P, P, P, P]
         L.oracle_verify.restype = i
-        L.oracle_build_cache.argtypes = [i, i, i, i, i, i, P, P, i, P, P, i, d, P, i, P, P, P]
+        L.oracle_build_cache.argtypes = [i, i, i, i, i, i, P, P, i, P, P, i, P, d, P, i, P, P, P]
+        L.oracle_draft_cache.argtypes = [i, i, i, i, P, P, P, i, P]
+        L.oracle_draft_cache.restype = i
+        L.oracle_p_hit.argtypes = [i, i, i, i, i, i, P, P, i, P, P, i, P, d, P, i, P, P]
+        L.oracle_p_hit.restype = i
         L.oracle_build_cache.restype = i
         L.oracle_lookup.argtypes = [i, i, P, P, P, P, P, P]
         L.oracle_lookup.restype = None
@@ -155,9 +159,19 @@ def _problem(tgt, drf, tokens, dtype):
     return tgt, drf, tokens, B, K, V, _dtype_code(dtype), drf.shape[1]
 
 
-def verify(tgt, drf, tokens, uniforms, temperature, dtype, reshape_F: int = 0,
+def _reshape_arg(reshape_F, K):
+    """reshape_F: one F for every position, or a sequence of K per-position F_k."""
+    if np.ndim(reshape_F) == 0:
+        return int(reshape_F), None
+    Fk = np.ascontiguousarray(np.asarray(reshape_F, dtype=np.int32).reshape(-1)[:K])
+    assert Fk.size == K
+    return 0, Fk
+
+
+def verify(tgt, drf, tokens, uniforms, temperature, dtype, reshape_F=0,
            reshape_C: float = 1.0, threads: int | None = None) -> dict:
     tgt, drf, tokens, B, K, V, dt, drf_rows = _problem(tgt, drf, tokens, dtype)
+    F1, Fk = _reshape_arg(reshape_F, K)
     u = np.ascontiguousarray(uniforms, dtype=np.float32).reshape(B, K + 1)
     tau = np.ascontiguousarray(temperature, dtype=np.float32).reshape(B)
     out = {
@@ -170,7 +184,7 @@ def verify(tgt, drf, tokens, uniforms, temperature, dtype, reshape_F: int = 0,
     def run(rng):
         return lib().oracle_verify(
             rng[0], rng[1], B, K, V, dt, _ptr(tgt), _ptr(drf), drf_rows, _ptr(tokens), _ptr(u),
-            _ptr(tau), int(reshape_F), float(reshape_C), _ptr(out["accept_len"]),
+            _ptr(tau), F1, _ptr(Fk), float(reshape_C), _ptr(out["accept_len"]),
             _ptr(out["bonus"]), _ptr(out["p_tok"]), _ptr(out["q_tok"]), _ptr(out["acc_margin"]),
             _ptr(out["bonus_margin"]), _ptr(out["Z"]))
 
@@ -178,9 +192,10 @@ def verify(tgt, drf, tokens, uniforms, temperature, dtype, reshape_F: int = 0,
     return out
 
 
-def build_cache(tgt, drf, tokens, temperature, dtype, off, budget: int, reshape_F: int = 0,
+def build_cache(tgt, drf, tokens, temperature, dtype, off, budget: int, reshape_F=0,
                 reshape_C: float = 1.0, threads: int | None = None) -> dict:
     tgt, drf, tokens, B, K, V, dt, drf_rows = _problem(tgt, drf, tokens, dtype)
+    F1, Fk = _reshape_arg(reshape_F, K)
     tau = np.ascontiguousarray(temperature, dtype=np.float32).reshape(B)
     off = np.ascontiguousarray(off, dtype=np.int32)
     out = {"cache_tok": np.empty((B, budget), np.int32),
@@ -190,10 +205,46 @@ def build_cache(tgt, drf, tokens, temperature, dtype, off, budget: int, reshape_
     def run(rng):
         return lib().oracle_build_cache(
             rng[0], rng[1], B, K, V, dt, _ptr(tgt), _ptr(drf), drf_rows, _ptr(tokens), _ptr(tau),
-            int(reshape_F), float(reshape_C), _ptr(off), int(budget), _ptr(out["cache_tok"]),
+            F1, _ptr(Fk), float(reshape_C), _ptr(off), int(budget), _ptr(out["cache_tok"]),
             _ptr(out["cache_score"]), _ptr(out["cache_margin"]))
 
     out["invalid"] = _parallel(run, B, threads)
+    return out
+
+
+def draft_cache(drf, tokens, dtype, off, budget: int) -> np.ndarray:
+    """Cache keys from the draft logits drf [B, K+1, V]: cache_tok [B, budget] int32
+    (columns past off[K+1] are -2); tokens [B, K] (left out of their segment) or None."""
+    drf = np.ascontiguousarray(drf)
+    B, K1, V = drf.shape
+    K = K1 - 1
+    tok = None if tokens is None else np.ascontiguousarray(tokens, dtype=np.int32).reshape(B, K)
+    off = np.ascontiguousarray(off, dtype=np.int32)
+    cache = np.full((B, budget), -2, np.int32)
+    if lib().oracle_draft_cache(B, K, V, _dtype_code(dtype), _ptr(drf), _ptr(tok), _ptr(off),
+                                int(budget), _ptr(cache)) != 0:
+        raise MemoryError("oracle_draft_cache")
+    return cache
+
+
+def p_hit(tgt, drf, tokens, temperature, dtype, off, budget: int, cache_tok, reshape_F=0,
+          reshape_C: float = 1.0, threads: int | None = None) -> np.ndarray:
+    """Per-sequence probability [B] that the round's outcome (a, t*) is in cache_tok,
+    given the drafted tokens (the law of (a, t*) over the round's uniforms)."""
+    tgt, drf, tokens, B, K, V, dt, drf_rows = _problem(tgt, drf, tokens, dtype)
+    F1, Fk = _reshape_arg(reshape_F, K)
+    tau = np.ascontiguousarray(temperature, dtype=np.float32).reshape(B)
+    off = np.ascontiguousarray(off, dtype=np.int32)
+    cache = np.ascontiguousarray(cache_tok, dtype=np.int32).reshape(B, budget)
+    out = np.empty(B, np.float64)
+
+    def run(rng):
+        return lib().oracle_p_hit(rng[0], rng[1], B, K, V, dt, _ptr(tgt), _ptr(drf), drf_rows,
+                                  _ptr(tokens), _ptr(tau), F1, _ptr(Fk), float(reshape_C),
+                                  _ptr(off), int(budget), _ptr(cache), _ptr(out))
+
+    if _parallel(run, B, threads):
+        raise ValueError("invalid sequence")
     return out
 
 

@@ -32,7 +32,9 @@
  *   - uniform fan-out: floor(budget/(K+1)) each, remainder to the lowest k;
  *   - random backup token: floor(u * V) for a supplied uniform u in [0, 1);
  *   - cache scores: (p_k - q_k)^+ for k < K, p_K for k = K (tau > 0); raw target
- *     logits with the drafted token excluded (tau == 0).
+ *     logits with the drafted token excluded (tau == 0);
+ *   - draft-only cache keys: raw draft logits of row k (of K+1 draft rows), the
+ *     drafted token left out for k < K; the reshape at position k uses F = F_k.
  */
 #include <math.h>
 #include <stdint.h>
@@ -331,6 +333,7 @@ typedef struct {
     const float *uniforms;      /* [B, K+1] */
     const float *tau;           /* [B] temperatures */
     int reshape_F;              /* sigma_{F,C} on the draft rows (0 = none) */
+    const int *reshape_Fk;      /* [K] per-position F (overrides reshape_F), or NULL */
     double reshape_C;
 } problem_t;
 
@@ -344,8 +347,9 @@ static void target_probs(const problem_t *P, int b, int i, double tau, scratch_t
 static int draft_probs(const problem_t *P, int b, int i, double tau, scratch_t *s)
 {
     load_row(P->drf, P->dtype, ((int64_t)b * P->drf_rows + i) * P->V, P->V, s->zd);
-    if (P->reshape_F > 0)
-        return oracle_sigma(s->zd, P->V, tau, P->reshape_F, P->reshape_C, s->q, NULL);
+    const int F = P->reshape_Fk ? P->reshape_Fk[i] : P->reshape_F;
+    if (F > 0)
+        return oracle_sigma(s->zd, P->V, tau, F, P->reshape_C, s->q, NULL);
     oracle_softmax(s->zd, P->V, tau, s->q);
     return 0;
 }
@@ -574,13 +578,14 @@ static void lookup_sequence(const int *cache_row, const int *off, int a, int bon
  * ------------------------------------------------------------------------ */
 static problem_t make_problem(int B, int K, int V, int dtype, const void *tgt, const void *drf,
                               int drf_rows, const int *tokens, const float *uniforms,
-                              const float *tau, int reshape_F, double reshape_C)
+                              const float *tau, int reshape_F, const int *reshape_Fk,
+                              double reshape_C)
 {
     problem_t P;
     P.B = B; P.K = K; P.V = V; P.dtype = dtype;
     P.tgt = tgt; P.drf = drf; P.drf_rows = drf_rows;
     P.tokens = tokens; P.uniforms = uniforms; P.tau = tau;
-    P.reshape_F = reshape_F; P.reshape_C = reshape_C;
+    P.reshape_F = reshape_F; P.reshape_Fk = reshape_Fk; P.reshape_C = reshape_C;
     return P;
 }
 
@@ -590,12 +595,12 @@ static problem_t make_problem(int B, int K, int V, int dtype, const void *tgt, c
  * acc_margin [K], bonus_margin, Z.  Returns the number of invalid sequences. */
 int oracle_verify(int b0, int b1, int B, int K, int V, int dtype, const void *tgt,
                   const void *drf, int drf_rows, const int *tokens, const float *uniforms,
-                  const float *tau, int reshape_F, double reshape_C, int *accept_len,
-                  int *bonus, double *p_tok, double *q_tok, double *acc_margin,
-                  double *bonus_margin, double *Z)
+                  const float *tau, int reshape_F, const int *reshape_Fk, double reshape_C,
+                  int *accept_len, int *bonus, double *p_tok, double *q_tok,
+                  double *acc_margin, double *bonus_margin, double *Z)
 {
     problem_t P = make_problem(B, K, V, dtype, tgt, drf, drf_rows, tokens, uniforms, tau,
-                               reshape_F, reshape_C);
+                               reshape_F, reshape_Fk, reshape_C);
     scratch_t s;
     if (scratch_init(&s, V) != 0) {
         scratch_free(&s);
@@ -622,11 +627,11 @@ int oracle_verify(int b0, int b1, int B, int K, int V, int dtype, const void *tg
  * cache_margin [B, K+1].  off [K+2] from the fan-out. */
 int oracle_build_cache(int b0, int b1, int B, int K, int V, int dtype, const void *tgt,
                        const void *drf, int drf_rows, const int *tokens, const float *tau,
-                       int reshape_F, double reshape_C, const int *off, int budget,
-                       int *cache_tok, double *cache_score, double *cache_margin)
+                       int reshape_F, const int *reshape_Fk, double reshape_C, const int *off,
+                       int budget, int *cache_tok, double *cache_score, double *cache_margin)
 {
     problem_t P = make_problem(B, K, V, dtype, tgt, drf, drf_rows, tokens, NULL, tau,
-                               reshape_F, reshape_C);
+                               reshape_F, reshape_Fk, reshape_C);
     scratch_t s;
     if (scratch_init(&s, V) != 0) {
         scratch_free(&s);
@@ -654,6 +659,139 @@ void oracle_lookup(int B, int budget, const int *off, const int *cache_tok,
     for (int b = 0; b < B; ++b)
         lookup_sequence(cache_tok + (int64_t)b * budget, off, accept_len[b], bonus[b], hit + b,
                         slot + b);
+}
+
+/* --------------------------------------------------------------------------
+ * [SSD] item 2, cache keys chosen from the draft logits.  For sequence b and
+ * accepted length k, segment k of the cache row holds the F_k tokens ranked
+ * highest by raw draft logit (row k of drf [B, K+1, V]; ties to the lowest
+ * id).  Reading: for k < K the drafted token x~_k is left out (after x~_k is
+ * rejected the residual max(0, p - q) is zero there, so it is never the
+ * bonus); a slot with no token left (F_k == V) holds -1.  tokens may be NULL.
+ * ------------------------------------------------------------------------ */
+int oracle_draft_cache(int B, int K, int V, int dtype, const void *drf, const int *tokens,
+                       const int *off, int budget, int *cache_tok)
+{
+    double *z = (double *)malloc(sizeof(double) * (size_t)V);
+    ranked_t *work = (ranked_t *)malloc(sizeof(ranked_t) * (size_t)V);
+    int *order = (int *)malloc(sizeof(int) * (size_t)V);
+    if (!z || !work || !order) {
+        free(z); free(work); free(order);
+        return -1;
+    }
+    for (int b = 0; b < B; ++b) {
+        for (int k = 0; k <= K; ++k) {
+            load_row(drf, dtype, ((int64_t)b * (K + 1) + k) * V, V, z);
+            int excl = (tokens && k < K) ? tokens[(int64_t)b * K + k] : -1;
+            rank_tokens(z, V, excl, work, order);
+            int *seg = cache_tok + (int64_t)b * budget + off[k];
+            for (int j = 0; j < off[k + 1] - off[k]; ++j)
+                seg[j] = (j < V && order[j] != excl) ? order[j] : -1;
+        }
+    }
+    free(z); free(work); free(order);
+    return 0;
+}
+
+/* --------------------------------------------------------------------------
+ * Probability that the true outcome (a, t*) of one round is in the cache,
+ * given the drafted tokens and the cache ([SSD] "整体框架": the round hits when
+ * (a, t*) is among the cached outcomes; [SD] step 3 fixes the law of (a, t*)):
+ *   tau > 0:  position i is accepted with probability min(1, p_i(x~_i) / q_i(x~_i));
+ *             a rejection at k draws t* from max(0, p_k - q_k) / Z (from p_k
+ *             when Z == 0), acceptance of all K draws t* from p_K; so
+ *             P_hit = sum_k P(a = k) * (weight of segment k) / (total weight).
+ *   tau == 0: a and t* are fixed by the target argmaxes; P_hit is 0 or 1.
+ * q is sigma_{F,C} when reshape_F / reshape_Fk is given (as in oracle_verify).
+ * Writes p_hit[b0..b1).  Returns the number of invalid sequences (-1 there).
+ * ------------------------------------------------------------------------ */
+int oracle_p_hit(int b0, int b1, int B, int K, int V, int dtype, const void *tgt,
+                 const void *drf, int drf_rows, const int *tokens, const float *tau,
+                 int reshape_F, const int *reshape_Fk, double reshape_C, const int *off,
+                 int budget, const int *cache_tok, double *p_hit)
+{
+    problem_t P = make_problem(B, K, V, dtype, tgt, drf, drf_rows, tokens, NULL, tau,
+                               reshape_F, reshape_Fk, reshape_C);
+    scratch_t s;
+    if (scratch_init(&s, V) != 0) {
+        scratch_free(&s);
+        return -1;
+    }
+    int bad = 0;
+    for (int b = b0; b < b1; ++b) {
+        const int *x = tokens + (int64_t)b * K;
+        const int *row = cache_tok + (int64_t)b * budget;
+        const double t = (double)tau[b];
+        int ok = (t >= 0.0);
+        for (int i = 0; i < K; ++i)
+            if (x[i] < 0 || x[i] >= V)
+                ok = 0;
+        if (!ok) {
+            p_hit[b] = -1.0;
+            ++bad;
+            continue;
+        }
+        if (t == 0.0) {
+            int a = K, tstar = -1;
+            for (int i = 0; i <= K; ++i) {
+                load_row(tgt, dtype, ((int64_t)b * (K + 1) + i) * V, V, s.zt);
+                int am = row_argmax(s.zt, V);
+                if (i == K || am != x[i]) {
+                    a = i;
+                    tstar = am;
+                    break;
+                }
+            }
+            double h = 0.0;
+            for (int j = off[a]; j < off[a + 1]; ++j)
+                if (row[j] == tstar)
+                    h = 1.0;
+            p_hit[b] = h;
+            continue;
+        }
+        double reach = 1.0, total = 0.0;
+        for (int k = 0; k <= K && reach > 0.0; ++k) {
+            double pa, acc = 1.0;
+            target_probs(&P, b, k, t, &s);
+            if (k < K) {
+                if (draft_probs(&P, b, k, t, &s) != 0) {
+                    ok = 0;
+                    break;
+                }
+                double pt = s.p[x[k]], qt = s.q[x[k]];
+                acc = (qt > 0.0) ? fmin(1.0, pt / qt) : (pt > 0.0 ? 1.0 : 0.0);
+                pa = reach * (1.0 - acc);
+                double Z = 0.0;
+                for (int v = 0; v < V; ++v) {
+                    s.w[v] = fmax(0.0, s.p[v] - s.q[v]);
+                    Z += s.w[v];
+                }
+                if (Z == 0.0)
+                    for (int v = 0; v < V; ++v)
+                        s.w[v] = s.p[v];
+            } else {
+                pa = reach;
+                for (int v = 0; v < V; ++v)
+                    s.w[v] = s.p[v];
+            }
+            double W = 0.0, in = 0.0;
+            for (int v = 0; v < V; ++v)
+                W += s.w[v];
+            for (int j = off[k]; j < off[k + 1]; ++j)
+                if (row[j] >= 0 && row[j] < V)
+                    in += s.w[row[j]];
+            total += pa * (in / W);
+            reach *= acc;
+        }
+        if (!ok) {
+            p_hit[b] = -1.0;
+            ++bad;
+            continue;
+        }
+        p_hit[b] = total;
+    }
+    scratch_free(&s);
+    return bad;
 }
 
 /* sigma_{F,C} over independent rows: q_out [rows, V] (may be NULL), member

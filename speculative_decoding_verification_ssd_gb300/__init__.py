@@ -42,7 +42,7 @@ LIB_PATH = _build.LIB
 ABI_SYMBOLS = ("ssd_strerror", "ssd_version", "ssd_workspace_size", "ssd_verify", "ssd_fanout",
                "ssd_reshape_draft", "ssd_build_cache", "ssd_cache_lookup", "ssd_round",
                "ssd_noalloc_max_scratch", "ssd_round_noalloc", "ssd_fanout_uniform",
-               "ssd_backup_fill")
+               "ssd_backup_fill", "ssd_draft_cache")
 
 
 class SSDError(RuntimeError):
@@ -92,6 +92,8 @@ def lib() -> ctypes.CDLL:
         L.ssd_fanout_uniform.restype = i
         L.ssd_backup_fill.argtypes = [P, P, i, i, i, P, P]
         L.ssd_backup_fill.restype = i
+        L.ssd_draft_cache.argtypes = [P, i, i, i, i, P, P, i, f, P, P, P, P]
+        L.ssd_draft_cache.restype = i
         _lib = L
     return _lib
 
@@ -344,6 +346,43 @@ def ssd_reshape_draft(drf, F, C, temperature_rows=None, *, want_q=False, desc=No
         _ptr(q_out if want_q else None), _ptr(_opt(dev_status, "dev_status", torch.int32)),
         _stream(stream)), "ssd_reshape_draft")
     return desc, (q_out if want_q else None)
+
+
+def ssd_draft_cache(drf, tokens, F, budget, C=1.0, *, cache=True, reshape=False, cache_tok=None,
+                    desc=None, dev_status=None, stream=None):
+    """Draft-side cache keys and sigma_{F_k,C} descriptors from drf [B, K+1, V].
+
+    Returns (cache_tok [B, budget] int32 or None, desc [B*K, 4] int32 or None); tokens
+    [B, K] int32 (the drafted tokens left out of their segment) may be None."""
+    _dev(drf, "drf")
+    if drf.dim() != 3:
+        raise ValueError("drf must be [B, K+1, V]")
+    B, K1, V = drf.shape
+    K = K1 - 1
+    Fh = _F_host(F)
+    if len(Fh) != K + 1:
+        raise ValueError("F must have K+1 entries")
+    dev = drf.device
+    if tokens is not None:
+        _dev(tokens, "tokens", torch.int32)
+        if tuple(tokens.shape) != (B, K):
+            raise ValueError("tokens must be [B, K]")
+    if cache:
+        cache_tok = cache_tok if cache_tok is not None else torch.empty(
+            (B, budget), dtype=torch.int32, device=dev)
+        _dev(cache_tok, "cache_tok", torch.int32)
+    else:
+        cache_tok = None
+    if reshape:
+        desc = desc if desc is not None else torch.empty((B * K, 4), dtype=torch.int32, device=dev)
+        _dev(desc, "desc", torch.int32)
+    else:
+        desc = None
+    _check(lib().ssd_draft_cache(
+        _ptr(drf), _logit_dtype(drf), B, K, V, _ptr(tokens), _ptr(Fh), int(budget), float(C),
+        _ptr(cache_tok), _ptr(desc), _ptr(_opt(dev_status, "dev_status", torch.int32)),
+        _stream(stream)), "ssd_draft_cache")
+    return cache_tok, desc
 
 
 def desc_fields(desc: torch.Tensor):

@@ -331,6 +331,48 @@ int ssd_reshape_draft(const void *drf, int dtype, int rows, int V, const float *
     return ssd::reshape_launch(dtype, P, grid, g.CL, g.dyn, stream);
 }
 
+int ssd_draft_cache(const void *drf, int dtype, int B, int K, int V, const int32_t *tokens,
+                    const int32_t *F_host, int budget, float C, int32_t *cache_tok,
+                    ssd_reshape_desc *desc, int32_t *dev_status, void *stream) {
+    if (dtype != SSD_F32 && dtype != SSD_BF16) return SSD_ERR_DTYPE;
+    if (!drf || B < 1 || K < 1 || K > SSD_MAX_K || V < 2) return SSD_ERR_INVALID_ARG;
+    if (!cache_tok && !desc) return SSD_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(B) * (K + 1) > INT_MAX / 16) return SSD_ERR_UNSUPPORTED;
+    ssd::ReshapeParams P = {};
+    int st = check_fanout(F_host, K, V, budget, P.off);
+    if (st != SSD_OK) return st;
+    if (desc) {
+        if (!(C >= 0.f && C <= 1.f)) return SSD_ERR_INVALID_ARG;
+        for (int k = 0; k < K; ++k)
+            if (C == 0.f && F_host[k] >= V) return SSD_ERR_INVALID_ARG;
+    }
+    if (V > (dtype == SSD_F32 ? SSD_MAX_V_F32 : SSD_MAX_V_BF16)) return SSD_ERR_UNSUPPORTED;
+    DeviceInfo *dv = nullptr;
+    st = device_info(&dv);
+    if (st != SSD_OK) return st;
+    const int elem = dtype == SSD_F32 ? 4 : 2;
+    const int rows = B * (K + 1);
+    Geometry g;
+    st = choose_geometry(V, elem, 1, rows, *dv, dv->max_dyn[dtype == SSD_F32 ? 2 : 3], &g);
+    if (st != SSD_OK) return st;
+    P.drf = drf;
+    P.rows = rows;
+    P.V = V;
+    P.CL = g.CL;
+    P.slice = g.slice;
+    P.row_buf_bytes = g.row_buf_bytes;
+    P.C = C;
+    P.desc = desc;
+    P.dev_status = dev_status;
+    P.seq_rows = K + 1;
+    P.K = K;
+    for (int k = 0; k <= K; ++k) P.Fk[k] = F_host[k];
+    P.tokens = tokens;
+    P.cache_tok = cache_tok;
+    P.budget = budget;
+    return ssd::reshape_launch(dtype, P, rows * g.CL, g.CL, g.dyn, stream);
+}
+
 }  // extern "C"
 
 // ---------------------------------------------------------------------------

@@ -219,7 +219,8 @@ __device__ __forceinline__ float load_logit<BF16Tag>(const void *base, int64_t i
 // ---------------------------------------------------------------------------
 // Monotone map of float bits to uint32 (total order; +NaN above +inf).
 __device__ __forceinline__ uint32_t ordered_bits(float v) {
-    const uint32_t u = __float_as_uint(v);
+    uint32_t u = __float_as_uint(v);
+    u = (u == 0x80000000u) ? 0u : u;  // -0 and +0 are the same value: one key, ties by id
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 __device__ __forceinline__ float value_of_ordered(uint32_t o) {

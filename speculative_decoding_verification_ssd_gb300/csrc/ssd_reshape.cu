@@ -14,7 +14,17 @@
 // non-member, which fixes the shift of the reshaped softmax).  When q' is
 // requested, two more passes over the staged slice give the normaliser and
 // write q'_t = c_t 2^(x_t - m') / S'.
+//
+// Draft-cache mode runs the same selection on the K+1 draft rows of every
+// sequence with F = F_k at position k and also writes segment k of the
+// speculation cache: the F_k tokens of largest raw draft logit (ties to the
+// lowest id), best first, with the drafted token x~_k left out for k < K
+// (a bonus drawn after rejecting x~_k is never x~_k).  These are the cache
+// keys the notes' item 2 describes as chosen from the draft logits; the
+// per-position descriptors are the sigma_{F_k,C} reshape of the same rows.
 #include <cooperative_groups.h>
+
+#include <climits>
 
 #include "ssd_device.cuh"
 #include "ssd_launch.cuh"
@@ -28,6 +38,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 struct RXchg {
     int nlist;
+    int xpos;          // global rank of the excluded token (INT_MAX when not in the lists)
     float ssum;
     uint64_t slot[3];  // written by peers into rank 0: keys of global rank 0, F-1, F
 };
@@ -39,6 +50,7 @@ __global__ void __launch_bounds__(kThreads)
     constexpr int VEC = D::kVec, S = D::kBytes;
     extern __shared__ __align__(128) unsigned char dyn_smem[];
     __shared__ __align__(16) uint64_t cand[kCandCap];
+    __shared__ int cpos[kCandCap];
     __shared__ RXchg xc;
     __shared__ __align__(8) uint64_t bar;
     __shared__ float red_f[kWarps];
@@ -52,6 +64,11 @@ __global__ void __launch_bounds__(kThreads)
     const int row = blockIdx.x / CL;
     const int V = P.V;
     const int lo = min(V, rank * P.slice), hi = min(V, lo + P.slice);
+    const int seq = P.seq_rows > 0 ? row / P.seq_rows : row;
+    const int pos_k = P.seq_rows > 0 ? row - seq * P.seq_rows : 0;
+    const int F = P.seq_rows > 0 ? P.Fk[pos_k] : P.F;
+    const int xt = (P.seq_rows > 0 && P.tokens && pos_k < P.K)
+                       ? __ldg(P.tokens + static_cast<int64_t>(seq) * P.K + pos_k) : -1;
     const unsigned char *grow =
         static_cast<const unsigned char *>(P.drf) + static_cast<int64_t>(row) * V * S;
 
@@ -68,6 +85,7 @@ __global__ void __launch_bounds__(kThreads)
         mbar_init(&bar, 1);
         fence_mbar_init();
         s_timeout = 0;
+        xc.xpos = INT_MAX;
         xc.slot[0] = xc.slot[1] = xc.slot[2] = 0;
     }
     __syncthreads();
@@ -120,7 +138,7 @@ __global__ void __launch_bounds__(kThreads)
             }
         }
     }
-    const int Fsel = P.F + 1;
+    const int Fsel = F + 1;
     const int nlist = block_topf(
         Fsel, tb,
         [&](uint64_t theta, auto emit) {
@@ -161,9 +179,11 @@ __global__ void __launch_bounds__(kThreads)
             pos += l;
         }
         RXchg *r0 = cluster.map_shared_rank(&xc, 0);
+        cpos[i] = pos;
         if (pos == 0) r0->slot[0] = key;
-        if (P.F > 0 && pos == P.F - 1) r0->slot[1] = key;
-        if (pos == P.F) r0->slot[2] = key;
+        if (F > 0 && pos == F - 1) r0->slot[1] = key;
+        if (pos == F) r0->slot[2] = key;
+        if (static_cast<int>(key_id(key)) == xt) r0->xpos = pos;
     }
     cluster.sync();
     const RXchg *r0 = cluster.map_shared_rank(&xc, 0);
@@ -171,9 +191,9 @@ __global__ void __launch_bounds__(kThreads)
     const bool timed_out = s_timeout != 0;
 
     ssd_reshape_desc d;
-    d.F = P.F;
+    d.F = F;
     d.C = P.C;
-    if (P.F > 0) {
+    if (F > 0) {
         d.thr_val = key_value(thr);
         d.thr_id = key_id(thr);
     } else {
@@ -181,8 +201,28 @@ __global__ void __launch_bounds__(kThreads)
         d.thr_id = -1;
     }
     if (rank == 0 && tid == 0) {
-        P.desc[row] = d;
+        if (P.desc && P.seq_rows == 0)
+            P.desc[row] = d;
+        else if (P.desc && pos_k < P.K)
+            P.desc[static_cast<int64_t>(seq) * P.K + pos_k] = d;
         if (timed_out && P.dev_status) atomicOr(P.dev_status, SSD_DEV_TIMEOUT);
+    }
+    if (P.cache_tok) {
+        // ranks 0..F of the row, the excluded token dropped: slot = rank minus one
+        // past the excluded token's rank; slots left over (F_k = V with a token
+        // excluded) hold -1
+        int32_t *seg = P.cache_tok + static_cast<int64_t>(seq) * P.budget + P.off[pos_k];
+        const int xpos = r0->xpos;
+        for (int i = tid; i < nlist; i += kThreads) {
+            const int pos = cpos[i];
+            if (pos == xpos) continue;
+            const int slot = pos - (xpos < pos ? 1 : 0);
+            if (slot < F) seg[slot] = static_cast<int32_t>(key_id(cand[i]));
+        }
+        if (rank == 0) {
+            const int avail = V - ((xt >= 0 && xt < V) ? 1 : 0);
+            for (int j = avail + tid; j < F; j += kThreads) seg[j] = -1;
+        }
     }
 
     if (P.q_out) {
@@ -192,14 +232,14 @@ __global__ void __launch_bounds__(kThreads)
         // shift m' = max over weighted tokens of x_t + log2 c_t
         float mprime;
         const float xtop = key_value(top1) * c;
-        if (P.F == 0)
+        if (F == 0)
             mprime = xtop;
         else {
             const float xnext = next ? key_value(next) * c : -INFINITY;
             mprime = fmaxf(xtop + l2C, xnext);
         }
         auto wx = [&](float z, int e) -> float {  // log2 of the unnormalised weight
-            const bool mem = P.F > 0 && (z > d.thr_val || (z == d.thr_val && e <= d.thr_id));
+            const bool mem = F > 0 && (z > d.thr_val || (z == d.thr_val && e <= d.thr_id));
             return z * c + (mem ? l2C : 0.f) - mprime;
         };
         float acc = 0.f;

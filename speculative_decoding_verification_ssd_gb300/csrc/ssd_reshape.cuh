@@ -15,9 +15,17 @@ struct ReshapeParams {
     const float *tau;      // [rows] (needed only for q_out)
     int F;
     float C;
-    ssd_reshape_desc *desc;  // [rows]
+    ssd_reshape_desc *desc;  // [rows] (or [B, K] in draft-cache mode), or nullptr
     float *q_out;            // [rows, V] or nullptr
     int32_t *dev_status;
+    // Draft-cache mode (seq_rows > 0): rows are [B, seq_rows = K+1, V] and row r
+    // is position k = r mod (K+1) of sequence r / (K+1), with F = Fk[k].
+    int seq_rows, K;
+    int Fk[SSD_MAX_K + 1];
+    int off[SSD_MAX_K + 2];
+    const int32_t *tokens;   // [B, K] drafted tokens excluded from segment k < K, or nullptr
+    int32_t *cache_tok;      // [B, budget] or nullptr
+    int budget;
 };
 
 struct LookupParams {

@@ -173,17 +173,22 @@ def sample_draft_tokens(rng: np.random.Generator, drf_f32: np.ndarray, tau: np.n
     return out
 
 
-def make_logits(wl: Workload, rng: np.random.Generator):
-    """Draws the stored target logits [B, K+1, V] and draft logits [B, K, V]."""
+def make_logits(wl: Workload, rng: np.random.Generator, draft_rows: int | None = None):
+    """Draws the stored target logits [B, K+1, V] and draft logits [B, draft_rows, V]
+    (draft_rows K by default; K+1 keeps the draft row of position K, which a cache
+    built from draft logits alone needs for the all-accepted outcome).  The random
+    stream is the same for either choice."""
     B, K, V = wl.B, wl.K, wl.V
+    R = K if draft_rows is None else int(draft_rows)
+    assert R in (K, K + 1)
     bias = zipf_log_bias(V, wl.zipf_s)
     tgt = np.empty((B, K + 1, V), dtype=np.float32 if wl.dtype == F32 else np.uint16)
-    drf = np.empty((B, K, V), dtype=tgt.dtype)
+    drf = np.empty((B, R, V), dtype=tgt.dtype)
     for b in range(B):
         zd = rng.standard_normal((K + 1, V), dtype=np.float32) * np.float32(wl.sigma_d) + bias
         zt = zd + rng.standard_normal((K + 1, V), dtype=np.float32) * np.float32(wl.sigma_n)
         tgt[b] = store(zt, wl.dtype)
-        drf[b] = store(zd[:K], wl.dtype)
+        drf[b] = store(zd[:R], wl.dtype)
     return tgt, drf
 
 

@@ -148,6 +148,21 @@ def test_device_calls_validate_before_any_cuda_call(ssd):
                        p, ws_ok, None, None) == ssd.SSD_ERR_INVALID_ARG  # hit missing
     assert L.ssd_cache_lookup(p, 4, 2, 5, Fp, p, p, p, p, None) == ssd.SSD_ERR_INVALID_ARG
     assert L.ssd_cache_lookup(p, 0, 2, 6, Fp, p, p, p, p, None) == ssd.SSD_ERR_INVALID_ARG
+    dc = L.ssd_draft_cache
+    Fz = np.array([2, 100, 3], np.int32).ctypes.data_as(ctypes.c_void_p)
+    c = ctypes.c_float
+    assert dc(p, 5, 4, 2, 100, p, Fp, 6, c(1), p, None, None, None) == ssd.SSD_ERR_DTYPE
+    assert dc(p, 0, 4, 2, 100, p, Fp, 6, c(1), None, None, None, None) == \
+        ssd.SSD_ERR_INVALID_ARG  # neither cache nor descriptors
+    assert dc(p, 0, 4, 2, 100, p, Fp, 5, c(1), p, None, None, None) == \
+        ssd.SSD_ERR_INVALID_ARG  # budget < sum F
+    assert dc(p, 0, 4, 2, 100, p, None, 6, c(1), p, None, None, None) == ssd.SSD_ERR_INVALID_ARG
+    assert dc(p, 0, 4, 2, 100, p, Fp, 6, c(1.5), None, p, None, None) == ssd.SSD_ERR_INVALID_ARG
+    assert dc(p, 0, 4, 2, 100, p, Fz, 105, c(0), None, p, None, None) == \
+        ssd.SSD_ERR_INVALID_ARG  # C == 0 with F_k = V: no weight left
+    Fv = np.array([2, 101, 3], np.int32).ctypes.data_as(ctypes.c_void_p)
+    assert dc(p, 0, 4, 2, 100, p, Fv, 106, c(1), p, None, None, None) == \
+        ssd.SSD_ERR_INVALID_ARG  # F_k > V
     bf = L.ssd_backup_fill
     assert bf(p, p, 0, 4, 100, p, None) == ssd.SSD_ERR_INVALID_ARG
     assert bf(p, p, 4, 0, 100, p, None) == ssd.SSD_ERR_INVALID_ARG

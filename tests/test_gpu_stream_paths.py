@@ -126,3 +126,26 @@ def test_all_equal_rows_overflow_both_candidate_buffers(ssd):
     tok = rng.integers(0, V, (B, K))
     u = rng.random((B, K + 1))
     _round_and_compare(ssd, _pack(zt, zd, tok, u, [1.0, 0.0, 1.0, 0.0], "bf16"), 32, 0.75, 0.5)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_signed_zeros_tie(ssd, dtype):
+    """-0.0 and +0.0 are one value: a row whose largest logit is zero, stored as -0.0
+    at a low id and +0.0 at a higher id, has its argmax at the low id, and zero-valued
+    cache candidates rank by id."""
+    rng = np.random.default_rng(34)
+    B, K, V = 4, 2, 24000
+    zt = -np.abs(rng.standard_normal((B, K + 1, V)).astype(np.float32)) - 0.5
+    zd = -np.abs(rng.standard_normal((B, K, V)).astype(np.float32)) - 0.5
+    for b in range(B):
+        for k in range(K + 1):
+            zt[b, k, 100 + k] = -0.0
+            zt[b, k, 5000 + k] = 0.0
+            zt[b, k, 7000 + k] = -0.0
+    zd[:, :, 300] = 0.0
+    zd[:, :, 200] = -0.0
+    tok = np.zeros((B, K), np.int64)
+    tok[:, 0] = 100
+    tok[:, 1] = 5001               # not the argmax (101): rejected, greedy bonus 101
+    u = rng.random((B, K + 1))
+    _round_and_compare(ssd, _pack(zt, zd, tok, u, [0.0, 1.0, 0.0, 0.5], dtype), 12, 0.7, 0.5)

@@ -395,6 +395,107 @@ def test_fanout_uniform_clamps_and_rejects():
 
 
 # ---------------------------------------------------------------------------
+# Draft-only cache keys and the analytic hit probability.
+# ---------------------------------------------------------------------------
+
+def test_draft_cache_brute_force():
+    """Library sort (numpy lexsort on (-value, id)) of every draft row, the drafted
+    token dropped from its own segment; bf16-quantised rows make ties common."""
+    rng = np.random.default_rng(50)
+    B, K, V = 6, 3, 40
+    z = np.round(rng.standard_normal((B, K + 1, V)) * 2).astype(np.float32) / 2
+    drf = synth.store(z, "bf16")
+    zs = synth.stored_to_f32(drf, "bf16").astype(np.float64)
+    tok = rng.integers(0, V, (B, K)).astype(np.int32)
+    tok[0] = np.argmax(zs[0, :K], axis=-1)           # drafted token at the top of its row
+    for F in ([5, 3, 2, 7], [0, 1, 40, 4], [40, 40, 40, 40]):
+        off = np.concatenate([[0], np.cumsum(F)]).astype(np.int32)
+        budget = int(off[-1]) + 3
+        got = oracle.draft_cache(drf, tok, "bf16", off, budget)
+        for b in range(B):
+            for k in range(K + 1):
+                order = np.lexsort((np.arange(V), -zs[b, k]))
+                if k < K:
+                    order = order[order != tok[b, k]]
+                want = np.full(F[k], -1)
+                n = min(F[k], len(order))
+                want[:n] = order[:n]
+                np.testing.assert_array_equal(got[b, off[k]:off[k + 1]], want)
+            assert (got[b, off[-1]:] == -2).all()  # columns past the segments untouched
+    no_excl = oracle.draft_cache(drf, None, "bf16", off, budget)
+    assert (no_excl[:, :off[-1]] >= 0).all()
+
+
+def _sigma_np(z, F, C):
+    """sigma_{F,C} of one row at tau = 1 with numpy: weight C on the F largest
+    logits (lowest id on ties), 1 elsewhere."""
+    order = np.lexsort((np.arange(len(z)), -z))
+    c = np.ones(len(z))
+    c[order[:F]] = C
+    w = c * np.exp(z - z.max())
+    return w / w.sum()
+
+
+def test_p_hit_matches_monte_carlo():
+    """The analytic per-sequence hit probability against the frequency of hits over
+    200k rounds of the oracle's own sampling (same drafted tokens, fresh uniforms),
+    with per-position sigma_{F_k, C} and draft-only cache keys."""
+    rng = np.random.default_rng(51)
+    K, V, n = 3, 48, 200_000
+    F = [4, 3, 2, 5]
+    off = np.concatenate([[0], np.cumsum(F)]).astype(np.int32)
+    budget = int(off[-1])
+    zp = (rng.standard_normal((K + 1, V)) * 1.5).astype(np.float32)
+    zq = (zp + rng.standard_normal((K + 1, V)) * 0.8).astype(np.float32)
+    x = np.array([int(np.argsort(-zq[i])[1]) for i in range(K)], np.int32)  # a top-F token
+    C = 0.4
+    cache = oracle.draft_cache(zq[None], x[None], "f32", off, budget)
+    ph = oracle.p_hit(zp[None], zq[None], x[None], np.ones(1, np.float32), "f32", off, budget,
+                      cache, reshape_F=F[:K], reshape_C=C)[0]
+    u = rng.random((n, K + 1), dtype=np.float32)
+    v = oracle.verify(_batch(zp, n), _batch(zq, n), _batch(x, n), u, np.ones(n, np.float32),
+                      "f32", reshape_F=F[:K], reshape_C=C)
+    h = oracle.lookup(_batch(cache[0], n), off, v["accept_len"], v["bonus"])["hit"]
+    se = np.sqrt(ph * (1 - ph) / n)
+    assert 0.05 < ph < 0.95
+    assert abs(h.mean() - ph) < 4 * se, (h.mean(), ph)
+    # greedy: the outcome is fixed, so the probability is exactly the hit
+    g = oracle.p_hit(zp[None], zq[None], x[None], np.zeros(1, np.float32), "f32", off, budget,
+                     cache)[0]
+    vg = oracle.verify(zp[None], zq[None], x[None], u[:1], np.zeros(1, np.float32), "f32")
+    hg = oracle.lookup(cache, off, vg["accept_len"], vg["bonus"])["hit"][0]
+    assert g == float(hg)
+
+
+@pytest.mark.parametrize("C", [1.0, 0.6, 0.2, 0.0])
+def test_p_hit_averaged_over_the_draft_is_the_residual_mass(C):
+    """K = 1, cache keys without the drafted token left out: averaged over
+    x~ ~ q' = sigma_{F,C}(z_d), the probability of (reject, t* = t) is
+    max(0, p(t) - q'(t)) for every t, and all-accepted has probability
+    sum_t min(p, q'), so E[P_hit] = sum_{t in S_0} max(0, p - q') +
+    sum_t min(p, q') * p_1(S_1) -- exact enumeration over the V drafted tokens.
+    As C falls, q' shrinks on S_0 = top-F_0(z_d), so the first term grows."""
+    rng = np.random.default_rng(52)
+    V, F = 10, [3, 2]
+    off = np.array([0, 3, 5], np.int32)
+    zp = rng.standard_normal((2, V)).astype(np.float32)
+    zq = (zp + rng.standard_normal((2, V)) * 0.9).astype(np.float32)
+    cache = oracle.draft_cache(zq[None], None, "f32", off, 5)
+    S0, S1 = cache[0, 0:3], cache[0, 3:5]
+    tok = np.arange(V, dtype=np.int32).reshape(V, 1)
+    ph = oracle.p_hit(_batch(zp, V), _batch(zq[:1], V), tok, np.ones(V, np.float32), "f32", off,
+                      5, _batch(cache[0], V), reshape_F=[F[0]], reshape_C=C)
+    p0 = scipy.special.softmax(zp[0].astype(np.float64))
+    p1 = scipy.special.softmax(zp[1].astype(np.float64))
+    q0 = _sigma_np(zq[0].astype(np.float64), F[0], C)
+    expect = np.maximum(p0 - q0, 0)[S0].sum() + np.minimum(p0, q0).sum() * p1[S1].sum()
+    assert abs(float(q0 @ ph) - expect) < 1e-12
+    if C < 1.0:
+        q1 = _sigma_np(zq[0].astype(np.float64), F[0], 1.0)
+        assert np.maximum(p0 - q0, 0)[S0].sum() >= np.maximum(p0 - q1, 0)[S0].sum()
+
+
+# ---------------------------------------------------------------------------
 # Random-token backup.
 # ---------------------------------------------------------------------------
 
