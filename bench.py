@@ -51,6 +51,9 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch (greedy share scaled); for profiling")
+    ap.add_argument("--two-pass-sigma", action="store_true",
+                    help="workloads with a sigma_{F,C} draft: find the descriptors in a separate "
+                         "pass (ssd_reshape_draft) before ssd_verify instead of in the same pass")
     ap.add_argument("--study", choices=["fanout", "csweep"], default=None,
                     help="fanout: cache hit rate of the geometric and the uniform fan-out at "
                          "several temperatures, with the batch all-hit rate p_hit^b; "
@@ -234,11 +237,40 @@ def run_ours(args):
     ws = ssd.workspace(wl.B, wl.K, dev)
     stream = torch.cuda.current_stream(dev)
     out = None
+    sig = wl.reshape_F > 0
+    sig_F = [wl.reshape_F] * wl.K
+    launches_per_step = 2 if (sig and args.two_pass_sigma) else 1
+    desc = torch.zeros((wl.B * wl.K, 4), dtype=torch.int32, device=dev)
+    if sig:
+        # the draft samples from sigma_{F,C}: redraw the drafted tokens from it (input
+        # synthesis on the device: Gumbel-max over the reshaped draft logits)
+        ssd.ssd_reshape_draft(d["drf"], wl.reshape_F, wl.reshape_C, desc=desc)
+        thr_val, thr_id, _, _ = ssd.desc_fields(desc)
+        zd = d["drf"].float()
+        ids = torch.arange(wl.V, device=dev).view(1, 1, wl.V)
+        mem = (zd > thr_val.view(wl.B, wl.K, 1)) | ((zd == thr_val.view(wl.B, wl.K, 1)) &
+                                                     (ids <= thr_id.view(wl.B, wl.K, 1)))
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(synth.BENCH_SEED[wl.name] + 7 + rank)
+        gum = -torch.log(-torch.log(torch.rand(zd.shape, generator=gen, device=dev).clamp_min(1e-30)))
+        tau = d["temperature"].view(wl.B, 1, 1)
+        score = zd / tau.clamp_min(1e-30) + mem.float() * float(np.log(wl.reshape_C)) + gum
+        d["tokens"] = torch.where(tau.view(wl.B, 1) > 0, torch.argmax(score, dim=-1),
+                                  torch.argmax(zd, dim=-1)).to(torch.int32).contiguous()
+        del zd, mem, gum, score
 
     def step():
         if wl.mode == "round":
             return ssd.ssd_round(d["tgt"], d["drf"], d["tokens"], d["uniforms"], d["temperature"], F,
                                  wl.budget, out=out, probs=False, workspace=ws, stream=stream)
+        if sig and args.two_pass_sigma:
+            ssd.ssd_reshape_draft(d["drf"], wl.reshape_F, wl.reshape_C, desc=desc, stream=stream)
+            return ssd.ssd_verify(d["tgt"], d["drf"], d["tokens"], d["uniforms"], d["temperature"],
+                                  reshape=desc, probs=False, workspace=ws, stream=stream)
+        if sig:
+            return ssd.ssd_verify_sigma(d["tgt"], d["drf"], d["tokens"], d["uniforms"],
+                                        d["temperature"], sig_F, wl.reshape_C, desc_out=desc,
+                                        probs=False, workspace=ws, stream=stream)
         return ssd.ssd_verify(d["tgt"], d["drf"], d["tokens"], d["uniforms"], d["temperature"],
                               probs=False, workspace=ws, stream=stream)
 
@@ -296,6 +328,11 @@ def run_ours(args):
             o = ssd.ssd_round(dev_in["tgt"], dev_in["drf"], dev_in["tokens"], dev_in["uniforms"],
                               dev_in["temperature"], F, wl.budget, out=out, probs=False,
                               workspace=ws, stream=stream)
+        elif sig:
+            o = ssd.ssd_verify_sigma(dev_in["tgt"], dev_in["drf"], dev_in["tokens"],
+                                     dev_in["uniforms"], dev_in["temperature"], sig_F,
+                                     wl.reshape_C, desc_out=desc, probs=False, workspace=ws,
+                                     stream=stream)
         else:
             o = ssd.ssd_verify(dev_in["tgt"], dev_in["drf"], dev_in["tokens"], dev_in["uniforms"],
                                dev_in["temperature"], probs=False, workspace=ws, stream=stream)
@@ -341,11 +378,17 @@ def run_ours(args):
                      "kernel": "ssd_stream_kernel<BF16Tag>"},
         "e2e": {"value": world * args.e2e_steps / (e2e_ms * 1e-3), "unit": "rounds/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * launches_per_step,
         "clocks": clocks,
         "accept_mean": float(np.mean(acc[acc >= 0])) if (acc >= 0).any() else None,
         "hit_rate": float(out["hit"].float().mean().item()) if wl.mode == "round" else None,
     }
+    if sig:
+        line["config"]["sigma"] = {
+            "F": wl.reshape_F, "C": wl.reshape_C,
+            "descriptors": ("separate pass (ssd_reshape_draft, then ssd_verify)" if args.two_pass_sigma
+                            else "found in the verification pass (ssd_verify_sigma)"),
+            "drafted_tokens": "drawn from sigma_{F,C} of the draft (Gumbel-max on the device)"}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(inp, wl, off)
     if pg:

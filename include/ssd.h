@@ -248,6 +248,34 @@ int ssd_round(const void *tgt, const void *drf, int dtype, int B, int K, int V, 
               size_t workspace_bytes, int32_t *dev_status, void *stream);
 
 /*
+ * ssd_verify_sigma / ssd_round_sigma -- ssd_verify / ssd_round on the
+ * sigma_{F_k,C}-reshaped draft ([SSD] item 2) without descriptors computed
+ * beforehand: the top-F_k set of each sampled draft row is found while the
+ * row streams through for verification, so the draft rows are read once.
+ * sigma_F_host [K] (host): F_k of position k (0 = no reshape there), each
+ * 0 <= F_k <= min(V, SSD_MAX_F); 0 <= sigma_C <= 1, and not (sigma_C == 0
+ * and F_k >= V).  desc_out [B, K] (device, required) receives the
+ * descriptor found for every position of every sampled sequence (the same
+ * set ssd_reshape_draft gives with F = F_k); entries of greedy sequences,
+ * and of sequences flagged invalid, may be left untouched.  Everything else
+ * as ssd_verify / ssd_round with reshape = the descriptors found.
+ * When the rows do not suit the streaming kernel (a row not on a 16-byte
+ * boundary, or V too large for its shared memory) the descriptors are found
+ * by a separate pass over the draft rows first.
+ */
+int ssd_verify_sigma(const void *tgt, const void *drf, int dtype, int B, int K, int V, int drf_rows,
+                     const int32_t *tokens, const float *uniforms, const float *temperature,
+                     const int32_t *sigma_F_host, float sigma_C, ssd_reshape_desc *desc_out,
+                     int32_t *accept_len, int32_t *bonus, float *p_tok, float *q_tok,
+                     void *workspace, size_t workspace_bytes, int32_t *dev_status, void *stream);
+int ssd_round_sigma(const void *tgt, const void *drf, int dtype, int B, int K, int V, int drf_rows,
+                    const int32_t *tokens, const float *uniforms, const float *temperature,
+                    const int32_t *sigma_F_host, float sigma_C, ssd_reshape_desc *desc_out,
+                    const int32_t *F_host, int budget, int32_t *accept_len, int32_t *bonus,
+                    float *p_tok, float *q_tok, int32_t *cache_tok, uint8_t *hit, int32_t *slot,
+                    void *workspace, size_t workspace_bytes, int32_t *dev_status, void *stream);
+
+/*
  * ssd_round_noalloc -- ssd_round for callers that cannot allocate device
  * memory (no counterpart on the pages: this is plumbing of this library).
  * Some hosts own every device buffer and forbid allocation while they enqueue

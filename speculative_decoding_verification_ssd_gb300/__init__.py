@@ -42,7 +42,7 @@ LIB_PATH = _build.LIB
 ABI_SYMBOLS = ("ssd_strerror", "ssd_version", "ssd_workspace_size", "ssd_verify", "ssd_fanout",
                "ssd_reshape_draft", "ssd_build_cache", "ssd_cache_lookup", "ssd_round",
                "ssd_noalloc_max_scratch", "ssd_round_noalloc", "ssd_fanout_uniform",
-               "ssd_backup_fill", "ssd_draft_cache")
+               "ssd_backup_fill", "ssd_draft_cache", "ssd_verify_sigma", "ssd_round_sigma")
 
 
 class SSDError(RuntimeError):
@@ -94,6 +94,11 @@ def lib() -> ctypes.CDLL:
         L.ssd_backup_fill.restype = i
         L.ssd_draft_cache.argtypes = [P, i, i, i, i, P, P, i, f, P, P, P, P]
         L.ssd_draft_cache.restype = i
+        L.ssd_verify_sigma.argtypes = [P, P, i, i, i, i, i, P, P, P, P, f, P, P, P, P, P, P, z, P, P]
+        L.ssd_verify_sigma.restype = i
+        L.ssd_round_sigma.argtypes = [P, P, i, i, i, i, i, P, P, P, P, f, P, P, i, P, P, P, P, P, P,
+                                      P, P, z, P, P]
+        L.ssd_round_sigma.restype = i
         _lib = L
     return _lib
 
@@ -324,6 +329,71 @@ def ssd_round(tgt, drf, tokens, uniforms, temperature, F, budget, reshape=None, 
         _ptr(o["accept_len"]), _ptr(o["bonus"]), _ptr(o.get("p_tok")), _ptr(o.get("q_tok")),
         _ptr(o["cache_tok"]), _ptr(o["hit"]), _ptr(o["slot"]), _ptr(ws), ws.numel(),
         _ptr(_opt(dev_status, "dev_status", torch.int32)), _stream(stream)), "ssd_round")
+    return o
+
+
+def _sigma_args(sigma_F, K, B, desc_out, dev):
+    Fs = _F_host(sigma_F)
+    if Fs.shape != (K,):
+        raise ValueError("sigma_F must have K entries")
+    desc_out = desc_out if desc_out is not None else torch.zeros((B * K, 4), dtype=torch.int32,
+                                                                 device=dev)
+    _dev(desc_out, "desc_out", torch.int32)
+    if desc_out.numel() != B * K * 4:
+        raise ValueError("desc_out must hold B*K descriptors")
+    return Fs, desc_out
+
+
+def ssd_verify_sigma(tgt, drf, tokens, uniforms, temperature, sigma_F, sigma_C, *, desc_out=None,
+                     probs=True, workspace=None, dev_status=None, stream=None):
+    """ssd_verify on sigma_{F_k,C} with the descriptors found in the same pass:
+    returns dict(accept_len, bonus[, p_tok, q_tok], desc)."""
+    B, K, V, drf_rows = _shapes(tgt, drf, tokens)
+    dev = tgt.device
+    _dev(uniforms, "uniforms", torch.float32)
+    _dev(temperature, "temperature", torch.float32)
+    Fs, desc_out = _sigma_args(sigma_F, K, B, desc_out, dev)
+    accept_len = torch.empty(B, dtype=torch.int32, device=dev)
+    bonus = torch.empty(B, dtype=torch.int32, device=dev)
+    p_tok = torch.empty((B, K), dtype=torch.float32, device=dev) if probs else None
+    q_tok = torch.empty((B, K), dtype=torch.float32, device=dev) if probs else None
+    ws = _workspace(workspace, B, K, dev)
+    _check(lib().ssd_verify_sigma(
+        _ptr(tgt), _ptr(drf), _logit_dtype(tgt), B, K, V, drf_rows, _ptr(tokens), _ptr(uniforms),
+        _ptr(temperature), _ptr(Fs), float(sigma_C), _ptr(desc_out), _ptr(accept_len), _ptr(bonus),
+        _ptr(p_tok), _ptr(q_tok), _ptr(ws), ws.numel(),
+        _ptr(_opt(dev_status, "dev_status", torch.int32)), _stream(stream)), "ssd_verify_sigma")
+    out = {"accept_len": accept_len, "bonus": bonus, "desc": desc_out}
+    if probs:
+        out.update(p_tok=p_tok, q_tok=q_tok)
+    return out
+
+
+def ssd_round_sigma(tgt, drf, tokens, uniforms, temperature, sigma_F, sigma_C, F, budget, *,
+                    desc_out=None, probs=True, workspace=None, dev_status=None, stream=None):
+    """ssd_round on sigma_{F_k,C} with the descriptors found in the same pass: returns the
+    outputs of ssd_round plus desc."""
+    B, K, V, drf_rows = _shapes(tgt, drf, tokens)
+    dev = tgt.device
+    _dev(uniforms, "uniforms", torch.float32)
+    _dev(temperature, "temperature", torch.float32)
+    Fs, desc_out = _sigma_args(sigma_F, K, B, desc_out, dev)
+    Fh = _F_host(F)
+    o = {"accept_len": torch.empty(B, dtype=torch.int32, device=dev),
+         "bonus": torch.empty(B, dtype=torch.int32, device=dev),
+         "cache_tok": torch.full((B, budget), -1, dtype=torch.int32, device=dev),
+         "hit": torch.empty(B, dtype=torch.uint8, device=dev),
+         "slot": torch.empty(B, dtype=torch.int32, device=dev), "desc": desc_out}
+    if probs:
+        o["p_tok"] = torch.empty((B, K), dtype=torch.float32, device=dev)
+        o["q_tok"] = torch.empty((B, K), dtype=torch.float32, device=dev)
+    ws = _workspace(workspace, B, K, dev)
+    _check(lib().ssd_round_sigma(
+        _ptr(tgt), _ptr(drf), _logit_dtype(tgt), B, K, V, drf_rows, _ptr(tokens), _ptr(uniforms),
+        _ptr(temperature), _ptr(Fs), float(sigma_C), _ptr(desc_out), _ptr(Fh), int(budget),
+        _ptr(o["accept_len"]), _ptr(o["bonus"]), _ptr(o.get("p_tok")), _ptr(o.get("q_tok")),
+        _ptr(o["cache_tok"]), _ptr(o["hit"]), _ptr(o["slot"]), _ptr(ws), ws.numel(),
+        _ptr(_opt(dev_status, "dev_status", torch.int32)), _stream(stream)), "ssd_round_sigma")
     return o
 
 

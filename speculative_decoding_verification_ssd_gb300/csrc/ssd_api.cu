@@ -139,10 +139,20 @@ int run_units(int mode, const void *tgt, const void *drf, int dtype, int B, int 
               const ssd_reshape_desc *reshape, const int32_t *F_host, int budget,
               int32_t *accept_len, int32_t *bonus, float *p_tok, float *q_tok, int32_t *cache_tok,
               uint8_t *hit, int32_t *slot, void *workspace, size_t workspace_bytes,
-              int32_t *dev_status, void *stream) {
+              int32_t *dev_status, void *stream, const int32_t *sig_F = nullptr, float sig_C = 1.f,
+              ssd_reshape_desc *desc_out = nullptr) {
     if (dtype != SSD_F32 && dtype != SSD_BF16) return SSD_ERR_DTYPE;
     if (B < 1 || K < 1 || K > SSD_MAX_K || V < 2) return SSD_ERR_INVALID_ARG;
     if (drf_rows != K && drf_rows != K + 1) return SSD_ERR_INVALID_ARG;
+    if (sig_F) {
+        // sigma_{F_k,C} found in the pass: no descriptors in, descriptors out
+        if (reshape || !desc_out) return SSD_ERR_INVALID_ARG;
+        if (!(sig_C >= 0.f && sig_C <= 1.f)) return SSD_ERR_INVALID_ARG;
+        for (int k = 0; k < K; ++k) {
+            if (sig_F[k] < 0 || sig_F[k] > SSD_MAX_F || sig_F[k] > V) return SSD_ERR_INVALID_ARG;
+            if (sig_C == 0.f && sig_F[k] >= V) return SSD_ERR_INVALID_ARG;
+        }
+    }
     if (!tgt || !temperature || !tokens) return SSD_ERR_INVALID_ARG;
     const bool verify = (mode & ssd::kModeVerify) != 0;
     const bool cache = (mode & ssd::kModeCache) != 0;
@@ -169,7 +179,7 @@ int run_units(int mode, const void *tgt, const void *drf, int dtype, int B, int 
     const int units = B * (K + 1);
     // The persistent streaming kernel needs every row on a 16-byte boundary and
     // its per-group arrays within shared memory; other inputs take the cluster kernel.
-    const size_t sdyn = ssd::stream_dyn_bytes(V);
+    const size_t sdyn = ssd::stream_dyn_bytes(V, sig_F != nullptr);
     const bool streaming = aligned(tgt, 16) && aligned(drf, 16) &&
                            (static_cast<long long>(V) * elem) % 16 == 0 &&
                            (V + ssd::kGroupTokens - 1) / ssd::kGroupTokens <= ssd::kStreamMaxGroups &&
@@ -215,8 +225,37 @@ int run_units(int mode, const void *tgt, const void *drf, int dtype, int B, int 
     P.exit_counter = sched + 1;
     P.perm_mul = coprime_stride(B);
     if (streaming) {
+        if (sig_F) {
+            P.sig_on = 1;
+            for (int k = 0; k < K; ++k) P.sig_F[k] = sig_F[k];
+            P.sig_C = sig_C;
+            P.desc_out = desc_out;
+        }
         const int grid = std::min(dv->sm_count, units);
         return ssd::stream_launch(dtype, P, grid, sdyn, stream);
+    }
+    if (sig_F) {
+        // the cluster kernel takes descriptors: find them first (one more read of
+        // the draft rows), into desc_out
+        ssd::ReshapeParams R = {};
+        Geometry rg;
+        st = choose_geometry(V, elem, 1, B * drf_rows, *dv, dv->max_dyn[dtype == SSD_F32 ? 2 : 3], &rg);
+        if (st != SSD_OK) return st;
+        R.drf = drf;
+        R.rows = B * drf_rows;
+        R.V = V;
+        R.CL = rg.CL;
+        R.slice = rg.slice;
+        R.row_buf_bytes = rg.row_buf_bytes;
+        R.C = sig_C;
+        R.desc = desc_out;
+        R.dev_status = dev_status;
+        R.seq_rows = drf_rows;
+        R.K = K;
+        for (int k = 0; k < K; ++k) R.Fk[k] = sig_F[k];
+        st = ssd::reshape_launch(dtype, R, R.rows * rg.CL, rg.CL, rg.dyn, stream);
+        if (st != SSD_OK) return st;
+        P.reshape = desc_out;
     }
     const int grid = units * g.CL;
     return ssd::unit_launch(dtype, P, grid, g.CL, g.dyn, stream);
@@ -275,6 +314,31 @@ int ssd_round(const void *tgt, const void *drf, int dtype, int B, int K, int V, 
                      V, drf_rows, tokens, uniforms, temperature, reshape, F_host, budget,
                      accept_len, bonus, p_tok, q_tok, cache_tok, hit, slot, workspace,
                      workspace_bytes, dev_status, stream);
+}
+
+int ssd_verify_sigma(const void *tgt, const void *drf, int dtype, int B, int K, int V, int drf_rows,
+                     const int32_t *tokens, const float *uniforms, const float *temperature,
+                     const int32_t *sigma_F_host, float sigma_C, ssd_reshape_desc *desc_out,
+                     int32_t *accept_len, int32_t *bonus, float *p_tok, float *q_tok,
+                     void *workspace, size_t workspace_bytes, int32_t *dev_status, void *stream) {
+    if (!sigma_F_host) return SSD_ERR_INVALID_ARG;
+    return run_units(ssd::kModeVerify, tgt, drf, dtype, B, K, V, drf_rows, tokens, uniforms,
+                     temperature, nullptr, nullptr, 0, accept_len, bonus, p_tok, q_tok, nullptr,
+                     nullptr, nullptr, workspace, workspace_bytes, dev_status, stream, sigma_F_host,
+                     sigma_C, desc_out);
+}
+
+int ssd_round_sigma(const void *tgt, const void *drf, int dtype, int B, int K, int V, int drf_rows,
+                    const int32_t *tokens, const float *uniforms, const float *temperature,
+                    const int32_t *sigma_F_host, float sigma_C, ssd_reshape_desc *desc_out,
+                    const int32_t *F_host, int budget, int32_t *accept_len, int32_t *bonus,
+                    float *p_tok, float *q_tok, int32_t *cache_tok, uint8_t *hit, int32_t *slot,
+                    void *workspace, size_t workspace_bytes, int32_t *dev_status, void *stream) {
+    if (!sigma_F_host) return SSD_ERR_INVALID_ARG;
+    return run_units(ssd::kModeVerify | ssd::kModeCache | ssd::kModeLookup, tgt, drf, dtype, B, K,
+                     V, drf_rows, tokens, uniforms, temperature, nullptr, F_host, budget, accept_len,
+                     bonus, p_tok, q_tok, cache_tok, hit, slot, workspace, workspace_bytes,
+                     dev_status, stream, sigma_F_host, sigma_C, desc_out);
 }
 
 int ssd_cache_lookup(const int32_t *cache_tok, int B, int K, int budget, const int32_t *F_host,

@@ -223,6 +223,14 @@ __device__ __forceinline__ uint32_t ordered_bits(float v) {
     u = (u == 0x80000000u) ? 0u : u;  // -0 and +0 are the same value: one key, ties by id
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
+// The same map for values that are never -0 (saves the zero test on scans
+// over arrays written through canon_zero).
+__device__ __forceinline__ uint32_t ordered_bits_nz(float v) {
+    const uint32_t u = __float_as_uint(v);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+// -0 -> +0 (IEEE: the sum of zeros of opposite sign is +0); other values unchanged.
+__device__ __forceinline__ float canon_zero(float v) { return __fadd_rn(v, 0.f); }
 __device__ __forceinline__ float value_of_ordered(uint32_t o) {
     return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
 }
@@ -300,12 +308,18 @@ __device__ __forceinline__ uint64_t block_max_u64(uint64_t v, uint64_t *red) {
     return r;
 }
 
-// Block-wide bitonic sort, descending, of buf[0..n), n a power of two.
-// Ends with a __syncthreads.
-__device__ __forceinline__ void block_sort_desc(uint64_t *buf, int n) {
+// Bitonic sort, descending, of buf[0..n) (n a power of two) by a group of
+// kThreads threads: ti is the caller's index in the group and bar() the
+// group's barrier.  Ends with a barrier.
+struct BlockBar {
+    __device__ __forceinline__ void operator()() const { __syncthreads(); }
+};
+
+template <class Bar>
+__device__ __forceinline__ void group_sort_desc(uint64_t *buf, int n, int ti, const Bar &bar) {
     for (int k = 2; k <= n; k <<= 1) {
         for (int j = k >> 1; j > 0; j >>= 1) {
-            for (int i = threadIdx.x; i < n; i += kThreads) {
+            for (int i = ti; i < n; i += kThreads) {
                 const int ixj = i ^ j;
                 if (ixj > i) {
                     const uint64_t a = buf[i], c = buf[ixj];
@@ -316,9 +330,14 @@ __device__ __forceinline__ void block_sort_desc(uint64_t *buf, int n) {
                     }
                 }
             }
-            __syncthreads();
+            bar();
         }
     }
+}
+
+// Block-wide form (the whole CTA of kThreads threads).
+__device__ __forceinline__ void block_sort_desc(uint64_t *buf, int n) {
+    group_sort_desc(buf, n, static_cast<int>(threadIdx.x), BlockBar{});
 }
 
 __host__ __device__ __forceinline__ int next_pow2(int n) {
@@ -328,13 +347,14 @@ __host__ __device__ __forceinline__ int next_pow2(int n) {
 }
 
 // ---------------------------------------------------------------------------
-// Block top-F selection.
+// Top-F selection by a group of kThreads threads (ti: index in the group,
+// bar: the group's barrier); block_topf is the whole-CTA form.
 //
 // `thread_best` is this thread's largest key over its own elements (0 if it
-// has none).  `visit(theta, emit)` must call emit(key) for every element of
+// has none), or any key at or below it.  `visit(theta, emit)` must call emit(key) for every element of
 // the CTA's slice whose key is >= theta (in any order, from any thread).
 // On return cand[0..count) holds the CTA's top-min(F, #elements) keys in
-// descending order (count is returned to every thread).  F <= SSD_MAX_F.
+// descending order (count is returned to every thread).  F <= SSD_MAX_F + 1.
 //
 // Method: theta = F-th largest thread maximum is a lower bound on the F-th
 // largest key of the slice (F distinct elements reach it); the elements at or
@@ -342,38 +362,45 @@ __host__ __device__ __forceinline__ int next_pow2(int n) {
 // is raised to the F-th largest of the first kCandCap gathered and the gather
 // repeats (each round strictly shrinks the qualifying set).
 // ---------------------------------------------------------------------------
-template <class Visit>
-__device__ int block_topf(int F, uint64_t thread_best, Visit &&visit, uint64_t *cand, int *cnt) {
+template <class Visit, class Bar>
+__device__ int group_topf(int F, uint64_t thread_best, Visit &&visit, uint64_t *cand, int *cnt,
+                          int ti, const Bar &bar) {
     if (F <= 0) return 0;
     // 1. theta from the thread maxima.
-    cand[threadIdx.x] = thread_best;
-    for (int i = kThreads + threadIdx.x; i < kCandCap; i += kThreads) cand[i] = 0;
-    __syncthreads();
-    block_sort_desc(cand, kThreads);
+    cand[ti] = thread_best;
+    for (int i = kThreads + ti; i < kCandCap; i += kThreads) cand[i] = 0;
+    bar();
+    group_sort_desc(cand, kThreads, ti, bar);
     uint64_t theta = (F <= kThreads) ? cand[F - 1] : 0;
-    __syncthreads();
+    bar();
     int count = 0;
     for (int round = 0; round < 64; ++round) {
-        if (threadIdx.x == 0) *cnt = 0;
-        __syncthreads();
+        if (ti == 0) *cnt = 0;
+        bar();
         visit(theta, [&](uint64_t key) {
             const int idx = atomicAdd(cnt, 1);
             if (idx < kCandCap) cand[idx] = key;
         });
-        __syncthreads();
+        bar();
         count = *cnt;
         if (count <= kCandCap) break;
         // Overflow: all kCandCap stored keys are >= theta.
-        block_sort_desc(cand, kCandCap);
+        group_sort_desc(cand, kCandCap, ti, bar);
         theta = cand[F - 1];
-        __syncthreads();
+        bar();
     }
     if (count > kCandCap) count = kCandCap;  // unreachable for finite slices
     const int n = next_pow2(count < 2 ? 2 : count);
-    for (int i = count + threadIdx.x; i < n; i += kThreads) cand[i] = 0;
-    __syncthreads();
-    block_sort_desc(cand, n);
+    for (int i = count + ti; i < n; i += kThreads) cand[i] = 0;
+    bar();
+    group_sort_desc(cand, n, ti, bar);
     return count < F ? count : F;
+}
+
+template <class Visit>
+__device__ int block_topf(int F, uint64_t thread_best, Visit &&visit, uint64_t *cand, int *cnt) {
+    return group_topf(F, thread_best, static_cast<Visit &&>(visit), cand, cnt,
+                      static_cast<int>(threadIdx.x), BlockBar{});
 }
 
 }  // namespace ssd

@@ -56,6 +56,7 @@ constexpr unsigned kFull = 0xFFFFFFFFu;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kCandGroupsCap = 512;
 constexpr int kSchedCap = 2048;  // largest batch ordered by unit kind
+static_assert(kStreamSigKeys == kCandCap && kGT == kThreads, "fused sigma selection geometry");
 
 static_assert(kTailWarp0 + kNG == kStreamThreads / 32, "warp roles");
 
@@ -116,6 +117,7 @@ struct GroupShared {
     uint64_t cand[kCandCap];
     int cgroups[kCandGroupsCap];
     int cnt[2];
+    int scnt;  // consumer group: candidate count of the fused sigma selection
 };
 
 __device__ __forceinline__ uint64_t policy_evict_first() {
@@ -229,7 +231,7 @@ __device__ __forceinline__ void stat_fold(Stat &st, float xm, F mass) {
 }
 
 __device__ __forceinline__ Stat warp_stat(Stat s) {
-    const uint32_t mo = __reduce_max_sync(kFull, ordered_bits(s.m));
+    const uint32_t mo = __reduce_max_sync(kFull, ordered_bits_nz(s.m));  // -0 vs +0: same value
     const float M = value_of_ordered(mo);
     float S = (s.m == -INFINITY) ? 0.f : s.S * ex2(s.m - M);
     if (M == -INFINITY) S = 0.f;
@@ -326,9 +328,185 @@ __device__ __noinline__ float2 reshaped_resid(const unsigned char *stg, int half
     return make_float2(acc, mx);
 }
 
-}  // namespace
+// Number of threads of a named-barrier group whose predicate holds (one
+// barrier reduction; every thread of the group must call it).
+__device__ __forceinline__ int group_count(int bar_id, int nthreads, bool pred) {
+    int r;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.popc.u32 %0, %2, %3, p;\n\t}"
+        : "=r"(r)
+        : "r"(pred ? 1 : 0), "r"(bar_id), "r"(nthreads)
+        : "memory");
+    return r;
+}
+
+// Descending bitonic sort of one key per lane across a warp.
+__device__ __forceinline__ uint64_t warp_sort_desc(uint64_t v, int lane) {
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1)
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            const uint64_t o = __shfl_xor_sync(kFull, v, j);
+            const bool keep_max = ((lane & k) == 0) == ((lane & j) == 0);
+            v = keep_max ? (o > v ? o : v) : (o < v ? o : v);
+        }
+    return v;
+}
+
+// sigma_{F,C} of one draft row found in the streaming pass ([SSD] item 2): the
+// consumer group (kGT threads, named barrier bar_id) finds the row's top-F
+// keys from its raw 64-token group maxima gmax[0, G) (written in pass 1).
+// Each thread takes the largest of its groups' maxima; the F-th largest of
+// those (found bit by bit with barrier counts) bounds the F-th largest logit
+// from below; the groups at or above it are re-read from global memory (just
+// streamed, so they hit L2) by whole warps, and the tokens at or above it are
+// gathered and sorted (by one warp when at most 32 qualify, else by the group).
+// The reshaped normaliser comes from the row's plain statistics gD = (m, S) at
+// c: sum_t c_t 2^(x_t - m) = S - (1 - C) * (members' mass), whose rounding stays
+// within 8 ulps of S when C >= 1/8 or the result is at least S/8; otherwise the
+// non-members are summed afresh from the row (online, shifted by their own
+// maximum).  On return (every thread): the descriptor, and
+// q(t) = c_t 2^(z_t c - qm) / qS.
+struct SigResult {
+    DraftShape shape;
+    float qm, qS;
+};
 
 template <class D>
+__device__ __noinline__ SigResult sigma_fuse(const unsigned char *drow, const float *gmax, int G, int V,
+                                             int F, float C, float c, Stat gD, uint64_t *keys, int *cnt,
+                                             float *red, int t, int bar_id) {
+    constexpr int VEC = D::kVec, S = D::kBytes;
+    const auto bar = [bar_id]() { asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "r"(kGT) : "memory"); };
+    const int lane = t & 31, w = t >> 5;
+    float bm = -INFINITY;
+    for (int g = t; g < G; g += kGT) bm = fmaxf(bm, gmax[g]);
+    // F-th largest thread maximum, bit by bit over the upper 16 bits of the
+    // ordered value (all of a bf16 value's; for fp32 the bound is the bottom of
+    // its 2^-7-wide bucket), so T is at or below it
+    const uint32_t ob = ordered_bits_nz(bm);
+    uint32_t T = 0;
+    for (int bit = 31; bit >= 16; --bit) {
+        const uint32_t cand = T | (1u << bit);
+        if (group_count(bar_id, kGT, ob >= cand) >= F) T = cand;
+    }
+    // id V ranks below every token of that value: a lower bound on the F-th key
+    const uint64_t theta = (static_cast<uint64_t>(T) << 32) | static_cast<uint64_t>(0xFFFFFFFFu - static_cast<uint32_t>(V));
+    const float tv = value_of_ordered(T);
+    auto visit = [&](uint64_t th, float thv, auto emit) {
+        for (int g0 = w * 32; g0 < G; g0 += kGW * 32) {
+            const int g = g0 + lane;
+            uint32_t m = __ballot_sync(kFull, g < G && gmax[g] >= thv);
+            while (m) {
+                const int gg = g0 + __ffs(m) - 1;
+                m &= m - 1;
+                const int e = gg * kGTok + 2 * lane;  // the warp reads the group's 64 tokens
+                if (e < V) {
+                    const uint64_t k0 = make_key(load_logit<D>(drow, e), e);
+                    if (k0 >= th) emit(k0);
+                }
+                if (e + 1 < V) {
+                    const uint64_t k1 = make_key(load_logit<D>(drow, e + 1), e + 1);
+                    if (k1 >= th) emit(k1);
+                }
+            }
+        }
+    };
+    if (t == 0) *cnt = 0;
+    bar();
+    visit(theta, tv, [&](uint64_t key) {
+        const int idx = atomicAdd(cnt, 1);
+        if (idx < kCandCap) keys[idx] = key;
+    });
+    bar();
+    const int count = *cnt;
+    float top = 0.f;
+    if (count <= 32) {
+        // one warp sorts and sums the members (F <= count <= 32)
+        if (w == 0) {
+            uint64_t v = lane < count ? keys[lane] : 0;
+            v = warp_sort_desc(v, lane);
+            keys[lane] = v;
+            float sm = lane < F ? ex2(fmaf(key_value(v), c, -gD.m)) : 0.f;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) sm += __shfl_xor_sync(kFull, sm, o);
+            if (lane == 0) red[0] = sm;
+        }
+        bar();
+        top = red[0];
+    } else {
+        // many candidates (F above 32, or ties): the group's top-F selection
+        const uint64_t tb = make_key(bm, V);
+        group_topf(
+            F, tb,
+            [&](uint64_t th, auto emit) { visit(th, th ? key_value(th) : -INFINITY, emit); },
+            keys, cnt, t, bar);
+        float sm = t < F ? ex2(fmaf(key_value(keys[t]), c, -gD.m)) : 0.f;  // F <= kGT
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sm += __shfl_xor_sync(kFull, sm, o);
+        if (lane == 0) red[w] = sm;
+        bar();
+#pragma unroll
+        for (int i = 0; i < kGW; ++i) top += red[i];
+    }
+    const uint64_t thr = keys[F - 1];
+    bar();  // keys and red are free again
+    SigResult r;
+    r.shape.on = 1;
+    r.shape.thr = key_value(thr);
+    r.shape.thr_id = key_id(thr);
+    r.shape.l2C = C > 0.f ? (C == 1.f ? 0.f : lg2(C)) : -INFINITY;
+    const float Sp = gD.S - (1.f - C) * top;
+    if (C >= 0.125f || Sp >= 0.125f * gD.S) {
+        r.qm = gD.m;
+        r.qS = Sp;
+        return r;
+    }
+    // the members hold nearly all of the mass and C is small: sum the rest afresh
+    Stat sn{-INFINITY, 0.f};
+    const int nvec = static_cast<int>((static_cast<int64_t>(V) * S) / 16);
+    for (int v = t; v < nvec; v += kGT) {
+        float z[VEC];
+        decode_vec<D>(__ldg(reinterpret_cast<const uint4 *>(drow) + v), z);
+        float x[VEC];
+        float xm = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) {
+            const int e = v * VEC + i;
+            const bool mem = z[i] > r.shape.thr || (z[i] == r.shape.thr && e <= r.shape.thr_id);
+            x[i] = mem ? -INFINITY : z[i] * c;
+            xm = fmaxf(xm, x[i]);
+        }
+        stat_fold(sn, xm, [&](float mn) {
+            float a = 0.f;
+#pragma unroll
+            for (int i = 0; i < VEC; ++i) a += ex2(x[i] - mn);
+            return a;
+        });
+    }
+    const Stat ws = warp_stat(sn);
+    if (lane == 0) {
+        red[2 * w] = ws.m;
+        red[2 * w + 1] = ws.S;
+    }
+    bar();
+    Stat tot{-INFINITY, 0.f};
+#pragma unroll
+    for (int i = 0; i < kGW; ++i) tot = stat_merge_nan(tot, Stat{red[2 * i], red[2 * i + 1]});
+    bar();
+    // log2 of C * top * 2^m + S_non * 2^m_non, the larger term factored out
+    const float a = (C > 0.f && top > 0.f) ? gD.m + lg2(C * top) : -INFINITY;
+    const float bb = tot.S > 0.f ? tot.m + lg2(tot.S) : -INFINITY;
+    const float hi = fmaxf(a, bb), lo = fminf(a, bb);
+    r.qm = hi + lg2(1.f + ex2(lo - hi));
+    r.qS = 1.f;
+    return r;
+}
+
+}  // namespace
+
+template <class D, bool kSig>
 __global__ void __launch_bounds__(kStreamThreads, 1)
     ssd_stream_kernel(const __grid_constant__ UnitParams P) {
     constexpr int VEC = D::kVec, S = D::kBytes;
@@ -341,6 +519,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     constexpr int TPGS = kGT / GPS;        // single rows: threads per group
     constexpr int TPG2 = kGT / GPR;        // pass 2: threads per group
     constexpr int VPT1 = FULL_PAIR / (kGT / 2), VPTS = GV / TPGS, VPT2 = GV / TPG2;
+    constexpr int TPG1 = GV / VPT1;        // pass 1 of a pair: threads per group of one row
     static_assert(VPT1 == 4 && VPTS == 4 && VPT2 == 2, "stage geometry");
     constexpr int LPG = GV < 32 ? GV : 32;  // tail: lanes per group re-read (one vector each)
     constexpr int GPI = 32 / LPG;           // tail: groups per warp iteration
@@ -608,7 +787,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                 uint32_t m1 = 0, m2 = 0;
                 for (int i = 0; i < nstrip; ++i) {
                     const float4 v = gm4[32 * i];
-                    const uint32_t o[4] = {ordered_bits(v.x), ordered_bits(v.y), ordered_bits(v.z), ordered_bits(v.w)};
+                    const uint32_t o[4] = {ordered_bits_nz(v.x), ordered_bits_nz(v.y), ordered_bits_nz(v.z),
+                                           ordered_bits_nz(v.w)};
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         m2 = max(m2, min(m1, o[j]));
@@ -634,8 +814,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                         int cnt = 0;
                         for (int i = 0; i < nstrip; ++i) {
                             const float4 v = gm4[32 * i];
-                            cnt += (ordered_bits(v.x) >= mid) + (ordered_bits(v.y) >= mid) + (ordered_bits(v.z) >= mid) +
-                                   (ordered_bits(v.w) >= mid);
+                            cnt += (ordered_bits_nz(v.x) >= mid) + (ordered_bits_nz(v.y) >= mid) +
+                                   (ordered_bits_nz(v.z) >= mid) + (ordered_bits_nz(v.w) >= mid);
                         }
                         cnt = __reduce_add_sync(kFull, cnt);
                         if (cnt >= Fk)
@@ -652,8 +832,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                 for (int w = 0; w < kMaskWords; ++w) cm[w] = 0;
                 for (int i = 0; i < nstrip; ++i) {
                     const float4 v = gm4[32 * i];
-                    const uint32_t bits = (ordered_bits(v.x) >= th ? 1u : 0u) | (ordered_bits(v.y) >= th ? 2u : 0u) |
-                                          (ordered_bits(v.z) >= th ? 4u : 0u) | (ordered_bits(v.w) >= th ? 8u : 0u);
+                    const uint32_t bits = (ordered_bits_nz(v.x) >= th ? 1u : 0u) | (ordered_bits_nz(v.y) >= th ? 2u : 0u) |
+                                          (ordered_bits_nz(v.z) >= th ? 4u : 0u) | (ordered_bits_nz(v.w) >= th ? 8u : 0u);
 #pragma unroll
                     for (int w = 0; w < kMaskWords; ++w)
                         if ((i >> 3) == w) cm[w] |= bits << (4 * (i & 7));
@@ -896,7 +1076,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                                     if (e < V) s2 += ex2(fmaf(load_logit<D>(trow, e), c, -m * c));
                                 }
                             }
-                            gmax[g] = m;
+                            gmax[g] = canon_zero(m);
                             gsum[g] = s2;
                         }
                         __syncwarp();
@@ -907,7 +1087,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                 // argmax: the best group (lowest index on ties), then the lowest id in it
                 uint64_t gk = 0;
                 for (int g = g0; g < g1; ++g) {
-                    const uint64_t key = (static_cast<uint64_t>(ordered_bits(gmax[g])) << 32) |
+                    const uint64_t key = (static_cast<uint64_t>(ordered_bits_nz(gmax[g])) << 32) |
                                          static_cast<uint64_t>(0xFFFFFFFFu - static_cast<uint32_t>(g));
                     gk = key > gk ? key : gk;
                 }
@@ -1038,6 +1218,10 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     auto gbar = [&]() { asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "r"(kGT) : "memory"); };
     unsigned char *const ring = dyn_smem + grp * kRS * kSB;
     float *const arrays = reinterpret_cast<float *>(dyn_smem + kNG * kRS * kSB) + grp * kNBuf * 2 * Gp;
+    // fused sigma: candidate keys after the group arrays (present only when P.sig_on)
+    uint64_t *const sig_keys =
+        reinterpret_cast<uint64_t *>(dyn_smem + kNG * kRS * kSB + static_cast<size_t>(kNG) * kNBuf * 2 * Gp * 4) +
+        grp * kStreamSigKeys;
 
     // per-thread stage geometry (fixed for the whole launch)
     const int p1_row = t / (kGT / 2), p1_tr = t % (kGT / 2);
@@ -1051,7 +1235,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     uint32_t nho = 0;  // hand-offs to the tail warp
     int cur = -1;
     int b = 0, k = 0, flags = 0, xt = -1, xmask = -1;
-    bool sampled = false, pair = false, active = false, want_p2 = false;
+    bool sampled = false, pair = false, active = false, want_p2 = false, sig = false;
     float c = 0.f, LT = 0.f, LD = 0.f;
     DraftShape shape{0, 0.f, 0, 0.f};
     Stat st{-INFINITY, 0.f};
@@ -1130,6 +1314,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             want_p2 = pair && (do_verify || (do_cache && P.F[k] > 0));
             c = sampled ? kLog2e / tau : 0.f;
             shape = DraftShape{0, 0.f, 0, 0.f};
+            sig = kSig && pair && P.sig_F[k] > 0;
             if (pair && P.reshape) {
                 const ssd_reshape_desc dd = P.reshape[static_cast<int64_t>(b) * K + k];
                 shape.on = dd.F > 0;
@@ -1169,11 +1354,19 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         if (active) {
             if (pass == kPassStats && stage_pair) {
                 // online statistics: threads [0, 128) target, the rest draft
-                if (p1_row == 0 || !shape.on) {
-                    uint4 w[VPT1];
-                    load_vecs<D, VPT1>(stg + p1_row * HALF, p1_vbase, h.nvec, p1_rot, h.nvec == FULL_PAIR, w);
-                    const float xm = vecs_max<D, VPT1>(w) * c;
-                    stat_fold(st, xm, [&](float mn) { return vecs_expsum<D, VPT1>(w, c, mn); });
+                uint4 w[VPT1];
+                load_vecs<D, VPT1>(stg + p1_row * HALF, p1_vbase, h.nvec, p1_rot, h.nvec == FULL_PAIR, w);
+                const float rm = vecs_max<D, VPT1>(w);
+                // a reshaped draft row takes the plain path where none of the thread's
+                // tokens reaches the top-F threshold (all but a few threads of the row)
+                if (p1_row == 0 || !shape.on || !(rm >= shape.thr)) {
+                    stat_fold(st, rm * c, [&](float mn) { return vecs_expsum<D, VPT1>(w, c, mn); });
+                    if (sig && p1_row == 1) {
+                        // raw 64-token group maxima of the draft row for the fused sigma
+                        const float gm = tpg_max<TPG1>(rm);
+                        const int g = h.chunk * GPR + p1_tr / TPG1;
+                        if (p1_tr % TPG1 == 0 && g < G) gmax[g] = canon_zero(gm);
+                    }
                 } else {
                     st = reshaped_fold<D, VPT1>(st, stg + HALF, p1_vbase, h.nvec, p1_rot, h.nvec == FULL_PAIR, c,
                                                 shape, h.chunk * (FULL_PAIR * VEC) + p1_vbase * VEC);
@@ -1202,21 +1395,22 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                     const bool lead = s_part == 0 && gm != -INFINITY;
                     st = stat_merge_nan(st, Stat{lead ? gmc : -INFINITY, lead ? gsv : 0.f});
                     if (s_part == 0 && g < G) {
-                        gmax[g] = gm;
+                        gmax[g] = canon_zero(gm);
                         gsum[g] = gsv;
                     }
                 } else if (s_part == 0 && g < G) {
-                    gmax[g] = gm;
+                    gmax[g] = canon_zero(gm);
                 }
             } else {
                 // pass 2 (pair): residual masses and maxima per group
                 const bool full = h.nvec == FULL_PAIR;
                 float2 acc = make_float2(0.f, 0.f);
                 float mx = 0.f;
-                if (!shape.on) {
-                    uint4 wt[VPT2], wd[VPT2];
-                    load_vecs<D, VPT2>(stg, r_vbase, h.nvec, r_rot, full, wt);
-                    load_vecs<D, VPT2>(stg + HALF, r_vbase, h.nvec, r_rot, full, wd);
+                uint4 wt[VPT2], wd[VPT2];
+                load_vecs<D, VPT2>(stg, r_vbase, h.nvec, r_rot, full, wt);
+                load_vecs<D, VPT2>(stg + HALF, r_vbase, h.nvec, r_rot, full, wd);
+                // reshaped draft: only tokens at or above the top-F threshold carry a bias
+                if (!shape.on || !(vecs_max<D, VPT2>(wd) >= shape.thr)) {
                     const float2 cc = make_float2(c, c), nl = make_float2(-LT, -LD);
 #pragma unroll
                     for (int kk = 0; kk < VPT2; ++kk) {
@@ -1280,12 +1474,30 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                 continue;
             }
             LT = gT.m + lg2(gT.S);
-            LD = gD.m + lg2(gD.S);
+            float qm = gD.m, qS = gD.S;
+            if (sig) {
+                const unsigned char *drow = static_cast<const unsigned char *>(P.drf) +
+                                            (static_cast<int64_t>(b) * P.drf_seq_stride + static_cast<int64_t>(k) * V) * S;
+                const SigResult sr = sigma_fuse<D>(drow, gmax, G, V, P.sig_F[k], P.sig_C, c, gD, sig_keys, &gs.scnt,
+                                                   reinterpret_cast<float *>(gs.red), t, bar_id);
+                shape = sr.shape;
+                qm = sr.qm;
+                qS = sr.qS;
+            }
+            LD = qm + lg2(qS);
             if (t == 0) {
                 // the same operations for both, so identical rows give identical p and q
                 p_tok = ex2(fmaf(ztx, c, -gT.m)) / gT.S;
-                q_tok = ex2(fmaf(zdx, c, draft_bias(shape, zdx, xt) - gD.m)) / gD.S;
+                q_tok = ex2(fmaf(zdx, c, draft_bias(shape, zdx, xt) - qm)) / qS;
                 accept = (u_k * q_tok < p_tok) ? 1 : 0;
+                if (kSig && P.desc_out) {
+                    ssd_reshape_desc dd;
+                    dd.F = sig ? P.sig_F[k] : 0;
+                    dd.C = P.sig_C;
+                    dd.thr_val = sig ? shape.thr : INFINITY;
+                    dd.thr_id = sig ? shape.thr_id : -1;
+                    P.desc_out[static_cast<int64_t>(b) * K + k] = dd;
+                }
             }
             if (!want_p2) handoff(kKindPass, 1, 0.f, 0.f);
             continue;
@@ -1323,8 +1535,14 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
 
 int stream_setup(int dtype, size_t optin, size_t *max_dyn) {
     bool dummy = true;
-    return dtype == SSD_F32 ? setup_kernel(ssd_stream_kernel<F32Tag>, optin, max_dyn, &dummy)
-                            : setup_kernel(ssd_stream_kernel<BF16Tag>, optin, max_dyn, &dummy);
+    size_t with_sig = 0;
+    const int st = dtype == SSD_F32 ? setup_kernel(ssd_stream_kernel<F32Tag, true>, optin, &with_sig, &dummy)
+                                    : setup_kernel(ssd_stream_kernel<BF16Tag, true>, optin, &with_sig, &dummy);
+    if (st != SSD_OK) return st;
+    const int st2 = dtype == SSD_F32 ? setup_kernel(ssd_stream_kernel<F32Tag, false>, optin, max_dyn, &dummy)
+                                     : setup_kernel(ssd_stream_kernel<BF16Tag, false>, optin, max_dyn, &dummy);
+    if (with_sig < *max_dyn) *max_dyn = with_sig;  // one limit for both forms
+    return st2;
 }
 
 int stream_launch(int dtype, const UnitParams &P, int grid, size_t dyn, void *stream) {
@@ -1334,8 +1552,13 @@ int stream_launch(int dtype, const UnitParams &P, int grid, size_t dyn, void *st
     cfg.dynamicSmemBytes = dyn;
     cfg.stream = static_cast<cudaStream_t>(stream);
     cfg.numAttrs = 0;
-    const cudaError_t e = dtype == SSD_F32 ? cudaLaunchKernelEx(&cfg, ssd_stream_kernel<F32Tag>, P)
-                                           : cudaLaunchKernelEx(&cfg, ssd_stream_kernel<BF16Tag>, P);
+    cudaError_t e;
+    if (P.sig_on)
+        e = dtype == SSD_F32 ? cudaLaunchKernelEx(&cfg, ssd_stream_kernel<F32Tag, true>, P)
+                             : cudaLaunchKernelEx(&cfg, ssd_stream_kernel<BF16Tag, true>, P);
+    else
+        e = dtype == SSD_F32 ? cudaLaunchKernelEx(&cfg, ssd_stream_kernel<F32Tag, false>, P)
+                             : cudaLaunchKernelEx(&cfg, ssd_stream_kernel<BF16Tag, false>, P);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return SSD_ERR_CUDA;

@@ -19,12 +19,16 @@ constexpr int kStreamMaxGroups = 3 * 32 * 32;  // groups per row the tail warp's
 // Dynamic shared memory of the streaming kernel for a vocabulary of V tokens:
 // the stage rings plus, per consumer group, kStreamBuffers buffers of two float
 // arrays with one entry per 64-token group.
-inline size_t stream_dyn_bytes(int V) {
+// With sigma_{F,C} found in the pass (sig), each group also keeps a candidate-key
+// buffer of kStreamSigKeys 64-bit keys.
+constexpr int kStreamSigKeys = 512;
+inline size_t stream_dyn_bytes(int V, bool sig = false) {
     const size_t G = (static_cast<size_t>(V) + kGroupTokens - 1) / kGroupTokens;
     const size_t Gp = (G + 127) & ~static_cast<size_t>(127);  // padded to whole 4 x 32-group strips
     return static_cast<size_t>(kStreamGroups) *
            (static_cast<size_t>(kStreamRingStages) * kStreamStageBytes +
-            static_cast<size_t>(kStreamBuffers) * 2 * Gp * sizeof(float));
+            static_cast<size_t>(kStreamBuffers) * 2 * Gp * sizeof(float) +
+            (sig ? static_cast<size_t>(kStreamSigKeys) * sizeof(unsigned long long) : 0));
 }
 
 struct UnitParams;

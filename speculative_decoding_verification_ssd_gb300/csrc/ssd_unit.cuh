@@ -59,6 +59,12 @@ struct UnitParams {
     uint32_t *unit_counter;  // next unit to hand out (reset by the last CTA to exit)
     uint32_t *exit_counter;  // CTAs that have exited
     int perm_mul;            // unit u -> sequence ((u % B) * perm_mul) % B (coprime to B)
+    // sigma_{F,C} found in the pass over the draft rows (streaming kernel only):
+    // position k of a sampled sequence reshapes with F = sig_F[k] (0: none)
+    int sig_on;
+    int sig_F[SSD_MAX_K];
+    float sig_C;
+    ssd_reshape_desc *desc_out;  // [B, K] descriptors found (sampled sequences), or nullptr
 };
 
 // Workspace layout (each region 256-byte aligned).
