@@ -205,15 +205,20 @@ def cpu_baseline(inp, wl, off, sample_per_half: int = 128):
                           np.arange(g, min(B, g + sample_per_half))])
     sub = {k: inp[k][idx] for k in ("tgt", "drf", "tokens", "uniforms", "temperature")}
     threads = oracle.default_threads()
+    reps = 0
     t0 = time.perf_counter()
-    oracle.round_(sub["tgt"], sub["drf"], sub["tokens"], sub["uniforms"], sub["temperature"],
-                  wl.dtype, off, wl.budget, threads=threads)
-    dt = time.perf_counter() - t0
-    rounds = len(idx) / B
+    while True:  # repeat the sample until about 10 s of host time (at most 30 rounds)
+        oracle.round_(sub["tgt"], sub["drf"], sub["tokens"], sub["uniforms"], sub["temperature"],
+                      wl.dtype, off, wl.budget, threads=threads)
+        reps += 1
+        dt = time.perf_counter() - t0
+        if dt >= 10.0 or reps >= 30:
+            break
+    rounds = reps * len(idx) / B
     return {"value": rounds / dt, "unit": "rounds/s", "cores": threads, "kind": "oracle",
             "sample": f"{len(idx)} of {B} sequences of one round ({len(idx)//2} greedy, "
-                      f"{len(idx) - len(idx)//2} sampled), float64 C oracle, {threads} host threads; "
-                      f"{dt:.2f} s wall"}
+                      f"{len(idx) - len(idx)//2} sampled) x {reps} repetitions, float64 C oracle, "
+                      f"{threads} host threads; {dt:.2f} s wall"}
 
 
 def run_ours(args):

@@ -703,10 +703,13 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                     mbar_arrive_expect_tx(&gq.full_bar[s], 0);
                 } else {
                     const bool second = i >= nch;
-                    const int chunk = second ? i - nch : i;
+                    // the second pass runs from the row's end back to its start: the
+                    // chunks read last in the first pass are the likeliest still in L2
+                    const int chunk = second ? nch - 1 - (i - nch) : i;
                     const int64_t off = static_cast<int64_t>(chunk) * cb;
                     const uint32_t bytes = static_cast<uint32_t>(row_bytes - off < cb ? row_bytes - off : cb);
-                    const int code = (second ? kPassResid : kPassStats) | ((chunk == nch - 1) << 4) |
+                    const bool last = second ? chunk == 0 : chunk == nch - 1;
+                    const int code = (second ? kPassResid : kPassStats) | ((last ? 1 : 0) << 4) |
                                      ((pair ? 1 : 0) << 5);
                     gq.hdr[s] = Hdr{u, code, chunk, static_cast<int>(bytes / 16), b, k, 0, 0};
                     unsigned char *dst = ring + s * kSB;
