@@ -81,6 +81,28 @@ def dist_env():
     return world, rank, local
 
 
+def rank_seed(name: str, rank: int) -> int:
+    """Seed of a rank's batch: every rank draws its own batch of the workload (weak
+    scaling: the same per-GPU work on every rank, no data shared between ranks)."""
+    return synth.BENCH_SEED[name] + rank
+
+
+def max_over_ranks(x: float, pg, device) -> float:
+    """The slowest rank's value (a timed region bracketed by barriers ends when the
+    slowest rank does)."""
+    if pg is None:
+        return x
+    import torch
+    t = torch.tensor([x], device=device, dtype=torch.float64)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank: int, world: int, elapsed_ms: float) -> float:
+    """Whole-job throughput: the units all ranks processed over the (max-over-ranks) time."""
+    return world * units_per_rank / (elapsed_ms * 1e-3)
+
+
 def workload_config(wl) -> dict:
     return {"workload": f"{wl.name}: {wl.description}", "B": wl.B, "K": wl.K, "V": wl.V,
             "logits": wl.dtype, "mode": wl.mode, "greedy_sequences": min(wl.greedy_first, wl.B),
@@ -235,7 +257,7 @@ def run_ours(args):
     from speculative_decoding_verification_ssd_gb300 import _build
 
     wl = chosen_workload(args)
-    inp = synth.make_inputs(wl, synth.BENCH_SEED[wl.name] + rank)
+    inp = synth.make_inputs(wl, rank_seed(wl.name, rank))
     F, off = ssd.ssd_fanout(wl.K, max(wl.budget, 0), wl.a_p or 0.5, wl.r, wl.V) if wl.budget else (
         np.zeros(wl.K + 1, np.int32), np.zeros(wl.K + 2, np.int32))
     d = to_device(inp, torch, dev)
@@ -310,12 +332,8 @@ def run_ours(args):
         pg.barrier()
     time.sleep(0.05)
     sampler.stop()
-    elapsed_ms = start.elapsed_time(end)
+    elapsed_ms = max_over_ranks(start.elapsed_time(end), pg, dev)
     kernel_ms = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
-    if pg:
-        t = torch.tensor([elapsed_ms], device=dev, dtype=torch.float64)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
     clocks = sampler.summary(t_wall0, t_wall1)
 
     # end to end: pinned host inputs -> device, round, outputs -> host, every step
@@ -355,16 +373,12 @@ def run_ours(args):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = e0.elapsed_time(e1)
-    if pg:
-        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), pg, dev)
 
     peak, peak_kind = measured_peak()
     kmean = statistics.mean(kernel_ms)
     achieved = alg_bytes / (kmean * 1e-3) / 1e9
-    value = world * args.steps / (elapsed_ms * 1e-3)
+    value = job_rate(args.steps, world, elapsed_ms)
     line = {
         "metric": metric_name(), "value": value, "unit": "rounds/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps,
@@ -381,7 +395,7 @@ def run_ours(args):
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
                      "traffic": traffic_record(_build.stream_kernel_digest()),
                      "kernel": "ssd_stream_kernel<BF16Tag>"},
-        "e2e": {"value": world * args.e2e_steps / (e2e_ms * 1e-3), "unit": "rounds/s",
+        "e2e": {"value": job_rate(args.e2e_steps, world, e2e_ms), "unit": "rounds/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps * launches_per_step,
         "clocks": clocks,
