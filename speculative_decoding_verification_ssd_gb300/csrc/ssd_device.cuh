@@ -107,37 +107,6 @@ __device__ __forceinline__ bool mbar_wait_suspend(uint64_t *bar, uint32_t parity
     return done != 0;
 }
 
-// Waits for phase `parity` of `bar`, polling with try_wait and sleeping
-// SleepNs between polls (0: no sleep); gives up after kWaitLimitNs of
-// wall-clock time and returns false.  Roles that mostly idle (tail warps,
-// producers) sleep longer so that their polls take few issue slots from the
-// warps doing arithmetic.
-template <uint32_t SleepNs>
-__device__ __forceinline__ bool mbar_wait_sleep(uint64_t *bar, uint32_t parity) {
-    uint32_t done;
-    if (SleepNs == 0) return mbar_wait_suspend(bar, parity);
-    asm volatile(
-        "{\n\t"
-        ".reg .pred p;\n\t"
-        ".reg .u64 t0, t1;\n\t"
-        "mov.u64 t0, %%globaltimer;\n"
-        "SSD_SWAIT:\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "@p bra SSD_SDONE;\n\t"
-        "nanosleep.u32 %3;\n\t"
-        "mov.u64 t1, %%globaltimer;\n\t"
-        "sub.u64 t1, t1, t0;\n\t"
-        "setp.lt.u64 p, t1, %4;\n\t"
-        "@p bra SSD_SWAIT;\n"
-        "SSD_SDONE:\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t"
-        "}"
-        : "=r"(done)
-        : "r"(smem_addr(bar)), "r"(parity), "n"(SleepNs), "l"(kWaitLimitNs)
-        : "memory");
-    return done != 0;
-}
-
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
     for (uint32_t i = 0; i < kSpinLimit; ++i) {
         if (mbar_try_wait(bar, parity)) return true;

@@ -17,18 +17,21 @@
 //       between       a pair unit (sampled, k < K) reduces its two statistics
 //                     to the normalisers L_T, L_D and takes the accept test
 //                     ([SD] step 3);
-//       pass 2 (L2)   the pair's rows stream again (just read, so they hit L2):
-//                     per group the residual mass sum max(0, p - q) and the
-//                     largest residual;
+//       pass 2 (L2)   the pair's rows stream again, from the row's end back to
+//                     its start (just read, so mostly L2 hits): per group the
+//                     residual mass sum max(0, p - q) and the largest residual;
 //     then hands the unit's group arrays (double-buffered) to
 //   * tail warp g, which, without block barriers: selects the cache top-F_k
-//     (groups whose maximum reaches the F-th largest lane maximum are
-//     re-read and ranked as (value, id) keys), draws the bonus t_k at u_K by
+//     (groups whose maximum reaches the F-th largest of the lanes' two
+//     largest group maxima are re-read and ranked as (value, id) keys, with
+//     a bisection over the maxima for F_k above 64), draws the bonus t_k at u_K by
 //     inverse CDF over ascending token id (group prefix, then the crossing
 //     group re-read), takes the greedy argmax, publishes the unit's record,
 //     counts the sequence's finished units and, for the last one, runs the
 //     epilogue (scan -> a, bonus t_a, outputs, cache lookup).
-// The consumer groups never wait on a global-memory round trip.
+// The consumer groups never wait on a global-memory round trip, except in the
+// kernel form that finds sigma_{F,C} in the pass (kSig), where a pair's draft
+// top-F set is selected between its two passes (sigma_fuse).
 //
 // Operation sources: [SD] "Speculative decoding" (brentwoodlivery.com), "The
 // Algorithm (Step-by-Step)" and "Temperature and Sampling"; [WHY] "Why does
@@ -156,19 +159,6 @@ __device__ __forceinline__ void load_vecs(const unsigned char *row, int vbase, i
         else
             w[k] = v < nvec ? *reinterpret_cast<const uint4 *>(row + 16 * v) : neg_inf_vec<D>();
     }
-}
-
-// One 16-byte vector of a staged row, read afresh from shared memory (a second
-// sweep reloads instead of keeping the stage in registers); vectors at or past
-// nvec read as -inf unless the stage is full.
-template <class D>
-__device__ __forceinline__ uint4 lds_vec(const unsigned char *row, int v, int nvec, bool full) {
-    uint4 r = neg_inf_vec<D>();
-    if (full || v < nvec)
-        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                     : "r"(smem_addr(row + 16 * v)));
-    return r;
 }
 
 template <class D, int VPT>
