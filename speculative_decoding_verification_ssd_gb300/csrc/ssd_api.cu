@@ -223,6 +223,7 @@ int run_units(int mode, const void *tgt, const void *drf, int dtype, int B, int 
     uint32_t *sched = reinterpret_cast<uint32_t *>(ws + ssd::ws_rec_bytes(B, K) + 2 * ssd::ws_count_bytes(B));
     P.unit_counter = sched;
     P.exit_counter = sched + 1;
+    P.unit_ends = reinterpret_cast<unsigned long long *>(sched + 2);
     P.perm_mul = coprime_stride(B);
     if (streaming) {
         if (sig_F) {

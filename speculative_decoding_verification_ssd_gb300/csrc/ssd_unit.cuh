@@ -57,6 +57,8 @@ struct UnitParams {
     int32_t *dev_status;
     // persistent streaming kernel only
     uint32_t *unit_counter;  // next unit to hand out (reset by the last CTA to exit)
+    unsigned long long *unit_ends;  // streaming kernel: units taken from the front (low
+                                    // 32 bits) and from the back (high 32 bits) of the order
     uint32_t *exit_counter;  // CTAs that have exited
     int perm_mul;            // unit u -> sequence ((u % B) * perm_mul) % B (coprime to B)
     // sigma_{F,C} found in the pass over the draft rows (streaming kernel only):
