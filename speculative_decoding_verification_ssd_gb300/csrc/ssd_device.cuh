@@ -372,4 +372,49 @@ __device__ int block_topf(int F, uint64_t thread_best, Visit &&visit, uint64_t *
                       static_cast<int>(threadIdx.x), BlockBar{});
 }
 
+// Descending bitonic sort of one key per lane across a warp.
+__device__ __forceinline__ uint64_t warp_sort_desc(uint64_t v, int lane) {
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1)
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            const uint64_t o = __shfl_xor_sync(0xFFFFFFFFu, v, j);
+            const bool keep_max = ((lane & k) == 0) == ((lane & j) == 0);
+            v = keep_max ? (o > v ? o : v) : (o < v ? o : v);
+        }
+    return v;
+}
+
+// Top-F of a CTA (kThreads threads) when few keys reach the F-th largest thread
+// maximum: that maximum's ordered value is found bit by bit over its upper 16
+// bits with block-wide counts (a lower bound on the F-th largest key), the keys
+// at or above it are gathered, and one warp sorts them when at most 32 qualify;
+// otherwise the general block_topf runs.  Same contract as block_topf.
+template <class Visit>
+__device__ int block_topf_fast(int F, uint64_t thread_best, Visit &&visit, uint64_t *cand, int *cnt) {
+    if (F <= 0) return 0;
+    const uint32_t ob = static_cast<uint32_t>(thread_best >> 32);
+    uint32_t T = 0;
+    for (int bit = 31; bit >= 16; --bit) {
+        const uint32_t c = T | (1u << bit);
+        if (__syncthreads_count(ob >= c) >= F) T = c;
+    }
+    const uint64_t theta = static_cast<uint64_t>(T) << 32;
+    if (threadIdx.x == 0) *cnt = 0;
+    __syncthreads();
+    visit(theta, [&](uint64_t key) {
+        const int idx = atomicAdd(cnt, 1);
+        if (idx < kCandCap) cand[idx] = key;
+    });
+    __syncthreads();
+    const int count = *cnt;
+    if (count > 32) return block_topf(F, thread_best, visit, cand, cnt);
+    if (threadIdx.x < 32) {
+        const int l = static_cast<int>(threadIdx.x);
+        cand[l] = warp_sort_desc(l < count ? cand[l] : 0, l);
+    }
+    __syncthreads();
+    return count < F ? count : F;
+}
+
 }  // namespace ssd

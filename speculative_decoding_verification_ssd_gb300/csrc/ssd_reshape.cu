@@ -139,7 +139,7 @@ __global__ void __launch_bounds__(kThreads)
         }
     }
     const int Fsel = F + 1;
-    const int nlist = block_topf(
+    const int nlist = block_topf_fast(
         Fsel, tb,
         [&](uint64_t theta, auto emit) {
             const uint32_t tv = static_cast<uint32_t>(theta >> 32);

@@ -331,19 +331,6 @@ __device__ __forceinline__ int group_count(int bar_id, int nthreads, bool pred) 
     return r;
 }
 
-// Descending bitonic sort of one key per lane across a warp.
-__device__ __forceinline__ uint64_t warp_sort_desc(uint64_t v, int lane) {
-#pragma unroll
-    for (int k = 2; k <= 32; k <<= 1)
-#pragma unroll
-        for (int j = k >> 1; j > 0; j >>= 1) {
-            const uint64_t o = __shfl_xor_sync(kFull, v, j);
-            const bool keep_max = ((lane & k) == 0) == ((lane & j) == 0);
-            v = keep_max ? (o > v ? o : v) : (o < v ? o : v);
-        }
-    return v;
-}
-
 // sigma_{F,C} of one draft row found in the streaming pass ([SSD] item 2): the
 // consumer group (kGT threads, named barrier bar_id) finds the row's top-F
 // keys from its raw 64-token group maxima gmax[0, G) (written in pass 1).
