@@ -441,11 +441,15 @@ def ssd_draft_cache(drf, tokens, F, budget, C=1.0, *, cache=True, reshape=False,
         cache_tok = cache_tok if cache_tok is not None else torch.empty(
             (B, budget), dtype=torch.int32, device=dev)
         _dev(cache_tok, "cache_tok", torch.int32)
+        if tuple(cache_tok.shape) != (B, budget):
+            raise ValueError("cache_tok must be [B, budget]")
     else:
         cache_tok = None
     if reshape:
         desc = desc if desc is not None else torch.empty((B * K, 4), dtype=torch.int32, device=dev)
         _dev(desc, "desc", torch.int32)
+        if desc.numel() != B * K * 4:
+            raise ValueError("desc must hold B*K descriptors")
     else:
         desc = None
     _check(lib().ssd_draft_cache(
