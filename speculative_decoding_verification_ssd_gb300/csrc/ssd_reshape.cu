@@ -29,6 +29,7 @@
 #include "ssd_device.cuh"
 #include "ssd_launch.cuh"
 #include "ssd_reshape.cuh"
+#include "ssd_vec.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -125,31 +126,47 @@ __global__ void __launch_bounds__(kThreads)
     };
 
     // ---- local top-(F+1) by raw (value, id) --------------------------------
-    uint64_t tb = 0;
-    for (int v = tid; v < nv; v += kThreads) {
-        float z[VEC];
-        vec(v, z);
-#pragma unroll
-        for (int i = 0; i < VEC; ++i) {
-            const int e = ebase + v * VEC + i;
-            if (e >= lo && e < hi) {
-                const uint64_t key = make_key(z[i], e);
-                tb = key > tb ? key : tb;
-            }
-        }
-    }
-    const int Fsel = F + 1;
-    const int nlist = block_topf_fast(
-        Fsel, tb,
-        [&](uint64_t theta, auto emit) {
-            const uint32_t tv = static_cast<uint32_t>(theta >> 32);
-            for (int v = tid; v < nv; v += kThreads) {
+    // Vectors wholly inside [lo, hi) go through packed maxima and lane masks; the
+    // two boundary vectors of the slice element by element.
+    auto inside = [&](int v) { return ebase + v * VEC >= lo && ebase + v * VEC + VEC <= hi; };
+    float tmax = -INFINITY;
+    {
+        RawMax<D> rm;
+        for (int v = tid; v < nv; v += kThreads) {
+            if (inside(v)) {
+                rm.add(*reinterpret_cast<const uint4 *>(buf + 16 * v));
+            } else {
                 float z[VEC];
                 vec(v, z);
 #pragma unroll
                 for (int i = 0; i < VEC; ++i) {
                     const int e = ebase + v * VEC + i;
-                    if (e >= lo && e < hi && ordered_bits(z[i]) >= tv) {
+                    if (e >= lo && e < hi) tmax = fmax_nan(tmax, z[i]);
+                }
+            }
+        }
+        tmax = fmax_nan(tmax, rm.get());
+    }
+    // id V ranks below every token of value tmax: a lower bound on the thread's best key
+    const uint64_t tb = (tmax == -INFINITY) ? 0 : make_key(tmax, V);
+    const int Fsel = F + 1;
+    const int nlist = block_topf_fast(
+        Fsel, tb,
+        [&](uint64_t theta, auto emit) {
+            const uint32_t tv = static_cast<uint32_t>(theta >> 32);
+            // every token whose key reaches theta is at or above this storage value
+            const float tstore = tv ? round_down_storage<D>(value_of_ordered(tv)) : -INFINITY;
+            for (int v = tid; v < nv; v += kThreads) {
+                const uint4 w = *reinterpret_cast<const uint4 *>(buf + 16 * v);
+                const bool in = inside(v);
+                uint32_t m = in ? ge_lanes<D>(w, tstore) : ((1u << VEC) - 1u);
+                if (!m) continue;
+                float z[VEC];
+                decode_vec<D>(w, z);
+#pragma unroll
+                for (int i = 0; i < VEC; ++i) {
+                    const int e = ebase + v * VEC + i;
+                    if (((m >> i) & 1u) && e >= lo && e < hi && ordered_bits(z[i]) >= tv) {
                         const uint64_t key = make_key(z[i], e);
                         if (key >= theta) emit(key);
                     }
