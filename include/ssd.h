@@ -13,7 +13,9 @@
  *         acceptance and the residual (p - q)+).
  *   [SSD] "Speculative Speculative Decoding" notes (papernotes.org): "整体框架"
  *         (outcome v = (k, t*), speculation cache S_T, hit test), "关键设计" item 1
- *         (geometric fan-out F_k) and item 2 (SAGUARO sampling sigma_{F,C}).
+ *         (geometric and uniform fan-out F_k), item 2 (SAGUARO sampling
+ *         sigma_{F,C}; cache keys from the draft logits) and item 3 (batch-size
+ *         aware fallback; fast random-token backup).
  *
  * Conventions shared by every call
  * --------------------------------
@@ -25,8 +27,9 @@
  * - Shapes: B sequences, K drafted tokens per sequence, V vocabulary entries.
  *   Target logits  tgt [B, K+1, V]   (row i scores position i, row K is the
  *                                     extra row used when all K are accepted)
- *   Draft logits   drf [B, drf_rows, V], drf_rows in {K, K+1} (only rows 0..K-1
- *                                     are read)
+ *   Draft logits   drf [B, drf_rows, V], drf_rows in {K, K+1} (verification
+ *                                     reads rows 0..K-1; ssd_draft_cache takes
+ *                                     all K+1)
  *   Draft tokens   tokens [B, K] int32
  *   Uniforms       uniforms [B, K+1] fp32 in [0, 1): column i < K is the accept
  *                  draw of position i, column K draws the bonus token.
