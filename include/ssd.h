@@ -103,6 +103,19 @@ typedef struct ssd_reshape_desc {
     float C;
 } ssd_reshape_desc;
 
+/* Kernel choice for rows on the 16-byte grid (process-wide; rows off the grid
+ * always take the cluster kernel).  AUTO: the persistent streaming kernel when
+ * the batch has at least as many units (sequences x (K+1)) as the GPU has SMs,
+ * or when sigma_{F,C} is found in the pass, else the cluster kernel, which
+ * splits each row across a thread-block cluster.  STREAM / CLUSTER force one. */
+#define SSD_DISPATCH_AUTO 0
+#define SSD_DISPATCH_STREAM 1
+#define SSD_DISPATCH_CLUSTER 2
+
+/* Sets the kernel choice; returns the previous one, or -1 (and changes nothing)
+ * for an unknown policy.  Calls already enqueued are not affected. */
+int ssd_set_dispatch(int policy);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char *ssd_strerror(int status);
 

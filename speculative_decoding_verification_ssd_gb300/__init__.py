@@ -42,7 +42,8 @@ LIB_PATH = _build.LIB
 ABI_SYMBOLS = ("ssd_strerror", "ssd_version", "ssd_workspace_size", "ssd_verify", "ssd_fanout",
                "ssd_reshape_draft", "ssd_build_cache", "ssd_cache_lookup", "ssd_round",
                "ssd_noalloc_max_scratch", "ssd_round_noalloc", "ssd_fanout_uniform",
-               "ssd_backup_fill", "ssd_draft_cache", "ssd_verify_sigma", "ssd_round_sigma")
+               "ssd_backup_fill", "ssd_draft_cache", "ssd_verify_sigma", "ssd_round_sigma",
+               "ssd_set_dispatch")
 
 
 class SSDError(RuntimeError):
@@ -99,8 +100,21 @@ def lib() -> ctypes.CDLL:
         L.ssd_round_sigma.argtypes = [P, P, i, i, i, i, i, P, P, P, P, f, P, P, i, P, P, P, P, P, P,
                                       P, P, z, P, P]
         L.ssd_round_sigma.restype = i
+        L.ssd_set_dispatch.argtypes = [i]
+        L.ssd_set_dispatch.restype = i
         _lib = L
     return _lib
+
+
+SSD_DISPATCH_AUTO, SSD_DISPATCH_STREAM, SSD_DISPATCH_CLUSTER = 0, 1, 2
+
+
+def ssd_set_dispatch(policy: int) -> int:
+    """Kernel choice for aligned rows (process-wide); returns the previous policy."""
+    prev = int(lib().ssd_set_dispatch(int(policy)))
+    if prev < 0:
+        raise ValueError(f"unknown dispatch policy {policy}")
+    return prev
 
 
 def strerror(status: int) -> str:

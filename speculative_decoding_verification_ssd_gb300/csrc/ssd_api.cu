@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <climits>
 #include <cmath>
 #include <cstdint>
@@ -133,6 +134,9 @@ int check_fanout(const int32_t *F_host, int K, int V, int budget, int *off) {
     return SSD_OK;
 }
 
+// Kernel choice for aligned rows (ssd_set_dispatch).
+std::atomic<int> g_dispatch{SSD_DISPATCH_AUTO};
+
 // Shared driver of ssd_verify / ssd_build_cache / ssd_round.
 int run_units(int mode, const void *tgt, const void *drf, int dtype, int B, int K, int V,
               int drf_rows, const int32_t *tokens, const float *uniforms, const float *temperature,
@@ -180,10 +184,16 @@ int run_units(int mode, const void *tgt, const void *drf, int dtype, int B, int 
     // The persistent streaming kernel needs every row on a 16-byte boundary and
     // its per-group arrays within shared memory; other inputs take the cluster kernel.
     const size_t sdyn = ssd::stream_dyn_bytes(V, sig_F != nullptr);
-    const bool streaming = aligned(tgt, 16) && aligned(drf, 16) &&
+    const bool stream_ok = aligned(tgt, 16) && aligned(drf, 16) &&
                            (static_cast<long long>(V) * elem) % 16 == 0 &&
                            (V + ssd::kGroupTokens - 1) / ssd::kGroupTokens <= ssd::kStreamMaxGroups &&
                            sdyn <= dv->max_dyn[dtype == SSD_F32 ? 4 : 5];
+    // With fewer units than SMs the persistent kernel leaves SMs idle and each unit
+    // streams at one group's share of an SM; the cluster kernel splits every row
+    // across a cluster instead (c2: 8 sequences, K = 5: 38.5 us against 58.7).
+    const int policy = g_dispatch.load(std::memory_order_relaxed);
+    const bool streaming = stream_ok && policy != SSD_DISPATCH_CLUSTER &&
+                           (policy == SSD_DISPATCH_STREAM || sig_F != nullptr || units >= dv->sm_count);
     Geometry g;
     if (!streaming) {
         st = choose_geometry(V, elem, 2, units, *dv, dv->max_dyn[dtype == SSD_F32 ? 0 : 1], &g);
@@ -279,6 +289,12 @@ const char *ssd_strerror(int status) {
 }
 
 const char *ssd_version(void) { return "libssd 0.1 (sm_103a)"; }
+
+int ssd_set_dispatch(int policy) {
+    if (policy != SSD_DISPATCH_AUTO && policy != SSD_DISPATCH_STREAM && policy != SSD_DISPATCH_CLUSTER)
+        return -1;
+    return g_dispatch.exchange(policy);
+}
 
 size_t ssd_workspace_size(int B, int K) {
     if (B < 1 || K < 1 || K > SSD_MAX_K) return 0;

@@ -10,6 +10,7 @@ Tolerance rule (the stated parity bar for this path):
 """
 from __future__ import annotations
 
+from contextlib import contextmanager
 from dataclasses import dataclass, field
 
 import numpy as np
@@ -147,3 +148,13 @@ def lookup_from(cache: np.ndarray, off, a: np.ndarray, t: np.ndarray):
             hit[b] = 1
             slot[b] = off[a[b]] + w[0]
     return hit, slot
+
+
+@contextmanager
+def use_dispatch(ssd, policy):
+    """Runs the block with the library's kernel choice forced to `policy`."""
+    prev = ssd.ssd_set_dispatch(policy)
+    try:
+        yield
+    finally:
+        ssd.ssd_set_dispatch(prev)

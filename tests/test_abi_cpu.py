@@ -43,6 +43,16 @@ def test_strerror_and_version(ssd):
     assert "sm_103a" in ssd.version()
 
 
+def test_dispatch_policy(ssd):
+    assert ssd.ssd_set_dispatch(ssd.SSD_DISPATCH_STREAM) == ssd.SSD_DISPATCH_AUTO
+    assert ssd.ssd_set_dispatch(ssd.SSD_DISPATCH_CLUSTER) == ssd.SSD_DISPATCH_STREAM
+    assert ssd.ssd_set_dispatch(ssd.SSD_DISPATCH_AUTO) == ssd.SSD_DISPATCH_CLUSTER
+    with pytest.raises(ValueError):
+        ssd.ssd_set_dispatch(7)
+    assert ssd.lib().ssd_set_dispatch(-3) == -1
+    assert ssd.ssd_set_dispatch(ssd.SSD_DISPATCH_AUTO) == ssd.SSD_DISPATCH_AUTO
+
+
 def test_workspace_size(ssd):
     assert ssd.ssd_workspace_size(0, 4) == 0
     assert ssd.ssd_workspace_size(4, 0) == 0

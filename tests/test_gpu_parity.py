@@ -11,7 +11,8 @@ import pytest
 
 import oracle
 import synth
-from tests._parity import Tally, compare_cache, compare_verify, lookup_from, np_out, to_device
+from tests._parity import (Tally, compare_cache, compare_verify, lookup_from, np_out, to_device,
+                           use_dispatch)
 
 pytestmark = pytest.mark.gpu
 
@@ -47,12 +48,14 @@ def _run_verify(ssd, inp, reshape=None):
     return np_out(out)
 
 
+@pytest.mark.parametrize("policy", [1, 2])  # streaming kernel, cluster kernel
 @pytest.mark.parametrize("name,B,seed_off", [("c1", 1, 0), ("c1", 64, 1), ("c2", 8, 0),
                                              ("c2", 24, 1)])
-def test_verify_parity(ssd, name, B, seed_off):
+def test_verify_parity(ssd, name, B, seed_off, policy):
     wl = _reduced(name, B)
     inp = synth.make_inputs(wl, synth.PARITY_SEED[name] + 100 * seed_off)
-    g = _run_verify(ssd, inp)
+    with use_dispatch(ssd, policy):
+        g = _run_verify(ssd, inp)
     o = _oracle_verify(inp, wl)
     t = Tally()
     compare_verify(g, o, wl.K, t)
@@ -99,16 +102,18 @@ def test_verify_reshaped_parity(ssd):
     assert err <= 1e-5, err
 
 
+@pytest.mark.parametrize("policy", [1, 2])  # streaming kernel, cluster kernel
 @pytest.mark.parametrize("name,B", [("c4", 6), ("c5", 32)])
-def test_round_parity(ssd, name, B):
+def test_round_parity(ssd, name, B, policy):
     wl = _reduced(name, B)
     inp = synth.make_inputs(wl, synth.PARITY_SEED[name])
     F, off = ssd.ssd_fanout(wl.K, wl.budget, wl.a_p, wl.r, wl.V)
     Fo, offo, _ = oracle.fanout(wl.K, wl.budget, wl.a_p, wl.r, wl.V)
     np.testing.assert_array_equal(F, Fo)
     d = to_device(inp)
-    out = ssd.ssd_round(d["tgt"], d["drf"], d["tokens"], d["uniforms"], d["temperature"], F,
-                        wl.budget)
+    with use_dispatch(ssd, policy):
+        out = ssd.ssd_round(d["tgt"], d["drf"], d["tokens"], d["uniforms"], d["temperature"], F,
+                            wl.budget)
     torch.cuda.synchronize()
     g = np_out(out)
     o = oracle.round_(inp["tgt"], inp["drf"], inp["tokens"], inp["uniforms"],

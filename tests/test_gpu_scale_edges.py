@@ -8,7 +8,8 @@ import pytest
 
 import oracle
 import synth
-from tests._parity import Tally, compare_cache, compare_verify, lookup_from, np_out, to_device
+from tests._parity import (Tally, compare_cache, compare_verify, lookup_from, np_out, to_device,
+                           use_dispatch)
 
 pytestmark = pytest.mark.gpu
 
@@ -46,10 +47,12 @@ def _round(ssd, wl, seed, F=None):
     return g
 
 
-def test_largest_lookahead(ssd):
+@pytest.mark.parametrize("policy", [1, 2])  # streaming kernel, cluster kernel
+def test_largest_lookahead(ssd, policy):
     wl = synth.WORKLOADS["c5"].replace(B=6, K=32, V=8192, greedy_first=2, budget=100,
                                        sigma_n=0.3)
-    g = _round(ssd, wl, 5101)
+    with use_dispatch(ssd, policy):
+        g = _round(ssd, wl, 5101)
     assert (g["accept_len"] >= 0).all()
 
 
@@ -61,4 +64,5 @@ def test_batch_above_the_ordered_unit_list(ssd):
 @pytest.mark.parametrize("V", [160000, 200000])
 def test_vocabularies_at_the_group_array_limit(ssd, V):
     wl = synth.WORKLOADS["c5"].replace(B=4, K=2, V=V, greedy_first=2)
-    _round(ssd, wl, 5103 + V % 7)
+    with use_dispatch(ssd, ssd.SSD_DISPATCH_STREAM):  # 160000 streams, 200000 cannot
+        _round(ssd, wl, 5103 + V % 7)

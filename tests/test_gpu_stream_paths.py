@@ -15,7 +15,8 @@ import pytest
 
 import oracle
 import synth
-from tests._parity import Tally, compare_cache, compare_verify, lookup_from, np_out, to_device
+from tests._parity import (Tally, compare_cache, compare_verify, lookup_from, np_out, to_device,
+                           use_dispatch)
 
 pytestmark = pytest.mark.gpu
 
@@ -29,7 +30,9 @@ def ssd():
     import speculative_decoding_verification_ssd_gb300 as m
     from speculative_decoding_verification_ssd_gb300 import _build
     _build.build()
-    return m
+    # these batches are small: force the streaming kernel, whose paths they exercise
+    with use_dispatch(m, m.SSD_DISPATCH_STREAM):
+        yield m
 
 
 def _pack(zt, zd, tok, u, taus, dtype):
