@@ -116,6 +116,14 @@ typedef struct ssd_reshape_desc {
  * for an unknown policy.  Calls already enqueued are not affected. */
 int ssd_set_dispatch(int policy);
 
+/* Check of the bounded waits (no counterpart on the pages): one warp waits on a
+ * shared-memory mbarrier that nothing completes, with the same bounded wait
+ * every kernel here uses but a limit of limit_ms milliseconds (1..10000); when
+ * it gives up it ORs SSD_DEV_TIMEOUT into *dev_status (device int32, required)
+ * and the launch ends normally, leaving the context usable.  The kernels' own
+ * waits give up after 4 s. */
+int ssd_check_wait_timeout(int32_t *dev_status, int limit_ms, void *stream);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char *ssd_strerror(int status);
 

@@ -43,7 +43,7 @@ ABI_SYMBOLS = ("ssd_strerror", "ssd_version", "ssd_workspace_size", "ssd_verify"
                "ssd_reshape_draft", "ssd_build_cache", "ssd_cache_lookup", "ssd_round",
                "ssd_noalloc_max_scratch", "ssd_round_noalloc", "ssd_fanout_uniform",
                "ssd_backup_fill", "ssd_draft_cache", "ssd_verify_sigma", "ssd_round_sigma",
-               "ssd_set_dispatch")
+               "ssd_set_dispatch", "ssd_check_wait_timeout")
 
 
 class SSDError(RuntimeError):
@@ -102,6 +102,8 @@ def lib() -> ctypes.CDLL:
         L.ssd_round_sigma.restype = i
         L.ssd_set_dispatch.argtypes = [i]
         L.ssd_set_dispatch.restype = i
+        L.ssd_check_wait_timeout.argtypes = [P, i, P]
+        L.ssd_check_wait_timeout.restype = i
         _lib = L
     return _lib
 
@@ -115,6 +117,15 @@ def ssd_set_dispatch(policy: int) -> int:
     if prev < 0:
         raise ValueError(f"unknown dispatch policy {policy}")
     return prev
+
+
+def ssd_check_wait_timeout(dev_status, limit_ms: int, *, stream=None):
+    """Runs the bounded-wait check: a wait nothing completes gives up after limit_ms
+    and ORs SSD_DEV_TIMEOUT into dev_status (a device int32 tensor)."""
+    _dev(dev_status, "dev_status", torch.int32)
+    _check(lib().ssd_check_wait_timeout(_ptr(dev_status), int(limit_ms), _stream(stream)),
+           "ssd_check_wait_timeout")
+    return dev_status
 
 
 def strerror(status: int) -> str:

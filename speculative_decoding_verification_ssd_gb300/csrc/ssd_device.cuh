@@ -74,17 +74,15 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
-// Waits for phase `parity` of `bar` with a bounded number of polls.  Returns
-// false if the limit ran out (the caller records SSD_DEV_TIMEOUT).
 // Waits for phase `parity` of `bar`, polling with try_wait (each poll may
 // suspend the thread for up to kSuspendHintNs or until the phase completes);
-// gives up after kWaitLimitNs of wall-clock time (%globaltimer) and returns
-// false.  A time bound rather than a poll count keeps roles that legitimately
+// gives up after limit_ns of wall-clock time (%globaltimer; kWaitLimitNs for
+// mbar_wait_suspend) and returns false (the caller records SSD_DEV_TIMEOUT).  A time bound rather than a poll count keeps roles that legitimately
 // idle for a long stretch of a large launch from giving up early.  The loop
 // lives in one asm block, so the compiler sees no divergent branch around it.
 constexpr uint32_t kSuspendHintNs = 200000;
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
-__device__ __forceinline__ bool mbar_wait_suspend(uint64_t *bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait_suspend_for(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
     uint32_t done;
     asm volatile(
         "{\n\t"
@@ -102,11 +100,16 @@ __device__ __forceinline__ bool mbar_wait_suspend(uint64_t *bar, uint32_t parity
         "selp.u32 %0, 1, 0, p;\n\t"
         "}"
         : "=r"(done)
-        : "r"(smem_addr(bar)), "r"(parity), "r"(kSuspendHintNs), "l"(kWaitLimitNs)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(kSuspendHintNs), "l"(limit_ns)
         : "memory");
     return done != 0;
 }
+__device__ __forceinline__ bool mbar_wait_suspend(uint64_t *bar, uint32_t parity) {
+    return mbar_wait_suspend_for(bar, parity, kWaitLimitNs);
+}
 
+// Waits for phase `parity` of `bar` with a bounded number of polls.  Returns
+// false if the limit ran out (the caller records SSD_DEV_TIMEOUT).
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
     for (uint32_t i = 0; i < kSpinLimit; ++i) {
         if (mbar_try_wait(bar, parity)) return true;

@@ -173,6 +173,9 @@ def test_device_calls_validate_before_any_cuda_call(ssd):
     Fv = np.array([2, 101, 3], np.int32).ctypes.data_as(ctypes.c_void_p)
     assert dc(p, 0, 4, 2, 100, p, Fv, 106, c(1), p, None, None, None) == \
         ssd.SSD_ERR_INVALID_ARG  # F_k > V
+    assert L.ssd_check_wait_timeout(None, 20, None) == ssd.SSD_ERR_INVALID_ARG
+    assert L.ssd_check_wait_timeout(p, 0, None) == ssd.SSD_ERR_INVALID_ARG
+    assert L.ssd_check_wait_timeout(p, 10001, None) == ssd.SSD_ERR_INVALID_ARG
     bf = L.ssd_backup_fill
     assert bf(p, p, 0, 4, 100, p, None) == ssd.SSD_ERR_INVALID_ARG
     assert bf(p, p, 4, 0, 100, p, None) == ssd.SSD_ERR_INVALID_ARG

@@ -196,3 +196,29 @@ def test_zero_budget_and_empty_segments(ssd):
     g0 = np_out(ssd.ssd_round(d["tgt"], d["drf"], d["tokens"], d["uniforms"], d["temperature"], Fz,
                               0))
     assert (g0["hit"] == 0).all() and (g0["slot"] == -1).all()
+
+
+def test_bounded_wait_gives_up_and_context_stays_usable(ssd):
+    """A wait that nothing completes ends after its limit with SSD_DEV_TIMEOUT set,
+    and the next round on the same context is still correct."""
+    import time
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    ssd.ssd_check_wait_timeout(st, 50)
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    assert int(st.item()) == ssd.SSD_DEV_TIMEOUT
+    assert 0.04 < dt < 5.0
+    wl = synth.WORKLOADS["c4"].replace(B=4, V=4096)
+    inp = synth.make_inputs(wl, 7070)
+    F, off = ssd.ssd_fanout(wl.K, wl.budget, wl.a_p, wl.r, wl.V)
+    d = to_device(inp)
+    g = np_out(ssd.ssd_round(d["tgt"], d["drf"], d["tokens"], d["uniforms"], d["temperature"], F,
+                             wl.budget))
+    o = oracle.round_(inp["tgt"], inp["drf"], inp["tokens"], inp["uniforms"], inp["temperature"],
+                      wl.dtype, off, wl.budget)
+    t = Tally()
+    compare_verify(g, o, wl.K, t)
+    compare_cache(g["cache_tok"], o, off, wl.K, t)
+    t.check()
