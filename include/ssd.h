@@ -272,6 +272,28 @@ int ssd_round(const void *tgt, const void *drf, int dtype, int B, int K, int V, 
               size_t workspace_bytes, int32_t *dev_status, void *stream);
 
 /*
+ * ssd_verify_ld / ssd_round_ld -- ssd_verify / ssd_round on logit rows spaced
+ * ld >= V elements apart (tgt row (b, i) starts at element (b (K+1) + i) ld,
+ * drf row (b, i) at (b drf_rows + i) ld; both tensors share ld).  Entries V..ld-1
+ * of a row are never used as logits.  A vocabulary whose rows are not a whole
+ * number of 16-byte vectors (V * s not a multiple of 16) reaches the streaming
+ * kernel this way when ld * s is a multiple of 16 and ld >= V rounded up to
+ * 16 / s; other layouts take the cluster kernel.  ld = V is ssd_verify /
+ * ssd_round.  Errors as those calls, and SSD_ERR_INVALID_ARG for ld < V.
+ */
+int ssd_verify_ld(const void *tgt, const void *drf, int dtype, int B, int K, int V, int ld,
+                  int drf_rows, const int32_t *tokens, const float *uniforms, const float *temperature,
+                  const ssd_reshape_desc *reshape, int32_t *accept_len, int32_t *bonus, float *p_tok,
+                  float *q_tok, void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                  void *stream);
+int ssd_round_ld(const void *tgt, const void *drf, int dtype, int B, int K, int V, int ld,
+                 int drf_rows, const int32_t *tokens, const float *uniforms, const float *temperature,
+                 const ssd_reshape_desc *reshape, const int32_t *F_host, int budget,
+                 int32_t *accept_len, int32_t *bonus, float *p_tok, float *q_tok, int32_t *cache_tok,
+                 uint8_t *hit, int32_t *slot, void *workspace, size_t workspace_bytes,
+                 int32_t *dev_status, void *stream);
+
+/*
  * ssd_verify_sigma / ssd_round_sigma -- ssd_verify / ssd_round on the
  * sigma_{F_k,C}-reshaped draft ([SSD] item 2) without descriptors computed
  * beforehand: the top-F_k set of each sampled draft row is found while the

@@ -43,7 +43,7 @@ ABI_SYMBOLS = ("ssd_strerror", "ssd_version", "ssd_workspace_size", "ssd_verify"
                "ssd_reshape_draft", "ssd_build_cache", "ssd_cache_lookup", "ssd_round",
                "ssd_noalloc_max_scratch", "ssd_round_noalloc", "ssd_fanout_uniform",
                "ssd_backup_fill", "ssd_draft_cache", "ssd_verify_sigma", "ssd_round_sigma",
-               "ssd_set_dispatch", "ssd_check_wait_timeout")
+               "ssd_set_dispatch", "ssd_check_wait_timeout", "ssd_verify_ld", "ssd_round_ld")
 
 
 class SSDError(RuntimeError):
@@ -104,6 +104,11 @@ def lib() -> ctypes.CDLL:
         L.ssd_set_dispatch.restype = i
         L.ssd_check_wait_timeout.argtypes = [P, i, P]
         L.ssd_check_wait_timeout.restype = i
+        L.ssd_verify_ld.argtypes = [P, P, i, i, i, i, i, i, P, P, P, P, P, P, P, P, P, z, P, P]
+        L.ssd_verify_ld.restype = i
+        L.ssd_round_ld.argtypes = [P, P, i, i, i, i, i, i, P, P, P, P, P, i, P, P, P, P, P, P, P, P,
+                                   z, P, P]
+        L.ssd_round_ld.restype = i
         _lib = L
     return _lib
 
@@ -219,11 +224,36 @@ def _workspace(ws, B, K, device):
     return ws
 
 
-def _shapes(tgt, drf, tokens):
-    _dev(tgt, "tgt")
-    _dev(drf, "drf")
+def _row_stride(t, name):
+    """Elements between consecutive rows of a [B, R, V] logit tensor whose rows are
+    contiguous and evenly spaced (a contiguous tensor, or a [..., :V] view of one
+    with a longer row); raises for any other layout."""
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dim() != 3:
+        raise ValueError(f"{name} must be [B, rows, V]")
+    B, R, V = t.shape
+    ld = t.stride(1) if R > 1 else (t.stride(0) if B > 1 else V)
+    if t.stride(2) != 1 or ld < V or (R > 1 and B > 1 and t.stride(0) != R * ld):
+        raise ValueError(f"{name} rows must be contiguous and evenly spaced")
+    return int(ld)
+
+
+def _shapes(tgt, drf, tokens, allow_ld=False):
     if tgt.dim() != 3 or drf.dim() != 3:
         raise ValueError("tgt must be [B, K+1, V] and drf [B, K or K+1, V]")
+    if allow_ld:
+        ld_t, ld_d = _row_stride(tgt, "tgt"), _row_stride(drf, "drf")
+        if tgt.shape[1] == 1 and tgt.shape[0] == 1:
+            ld_t = ld_d
+        if drf.shape[1] == 1 and drf.shape[0] == 1:
+            ld_d = ld_t
+        if ld_t != ld_d:
+            raise ValueError("tgt and drf must share one row stride")
+    else:
+        _dev(tgt, "tgt")
+        _dev(drf, "drf")
+        ld_t = int(tgt.shape[2])
     B, K1, V = tgt.shape
     K = K1 - 1
     if drf.shape[0] != B or drf.shape[2] != V or drf.dtype != tgt.dtype:
@@ -231,6 +261,8 @@ def _shapes(tgt, drf, tokens):
     _dev(tokens, "tokens", torch.int32)
     if tuple(tokens.shape) != (B, K):
         raise ValueError("tokens must be [B, K]")
+    if allow_ld:
+        return B, K, V, int(drf.shape[1]), ld_t
     return B, K, V, int(drf.shape[1])
 
 
@@ -249,8 +281,9 @@ def _F_host(F):
 def ssd_verify(tgt, drf, tokens, uniforms, temperature, reshape=None, *, accept_len=None,
                bonus=None, p_tok=None, q_tok=None, probs=True, workspace=None, dev_status=None,
                stream=None):
-    """Verify one batch: returns dict(accept_len, bonus[, p_tok, q_tok])."""
-    B, K, V, drf_rows = _shapes(tgt, drf, tokens)
+    """Verify one batch: returns dict(accept_len, bonus[, p_tok, q_tok]).  The logit
+    tensors may be [..., :V] views of rows with a longer stride (same for both)."""
+    B, K, V, drf_rows, ld = _shapes(tgt, drf, tokens, allow_ld=True)
     dev = tgt.device
     _dev(uniforms, "uniforms", torch.float32)
     _dev(temperature, "temperature", torch.float32)
@@ -261,11 +294,11 @@ def ssd_verify(tgt, drf, tokens, uniforms, temperature, reshape=None, *, accept_
         q_tok = q_tok if q_tok is not None else torch.empty((B, K), dtype=torch.float32, device=dev)
     ws = _workspace(workspace, B, K, dev)
     _opt(reshape, "reshape", torch.int32)
-    _check(lib().ssd_verify(
-        _ptr(tgt), _ptr(drf), _logit_dtype(tgt), B, K, V, drf_rows, _ptr(tokens), _ptr(uniforms),
+    _check(lib().ssd_verify_ld(
+        _ptr(tgt), _ptr(drf), _logit_dtype(tgt), B, K, V, ld, drf_rows, _ptr(tokens), _ptr(uniforms),
         _ptr(temperature), _ptr(reshape), _ptr(accept_len), _ptr(bonus), _ptr(p_tok), _ptr(q_tok),
         _ptr(ws), ws.numel(), _ptr(_opt(dev_status, "dev_status", torch.int32)), _stream(stream)),
-        "ssd_verify")
+        "ssd_verify_ld")
     out = {"accept_len": accept_len, "bonus": bonus}
     if probs:
         out.update(p_tok=p_tok, q_tok=q_tok)
@@ -322,8 +355,9 @@ def ssd_backup_fill(hit, uniforms, V: int, next_tokens, *, stream=None):
 
 def ssd_round(tgt, drf, tokens, uniforms, temperature, F, budget, reshape=None, *, out=None,
               probs=True, workspace=None, dev_status=None, stream=None):
-    """One fused SSD round: verify + cache build + lookup.  Returns a dict of outputs."""
-    B, K, V, drf_rows = _shapes(tgt, drf, tokens)
+    """One fused SSD round: verify + cache build + lookup.  Returns a dict of outputs.
+    The logit tensors may be [..., :V] views of rows with a longer stride."""
+    B, K, V, drf_rows, ld = _shapes(tgt, drf, tokens, allow_ld=True)
     dev = tgt.device
     _dev(uniforms, "uniforms", torch.float32)
     _dev(temperature, "temperature", torch.float32)
@@ -348,12 +382,12 @@ def ssd_round(tgt, drf, tokens, uniforms, temperature, F, budget, reshape=None, 
     if "slot" not in o:
         o["slot"] = torch.empty(B, dtype=torch.int32, device=dev)
     ws = _workspace(workspace, B, K, dev)
-    _check(lib().ssd_round(
-        _ptr(tgt), _ptr(drf), _logit_dtype(tgt), B, K, V, drf_rows, _ptr(tokens), _ptr(uniforms),
+    _check(lib().ssd_round_ld(
+        _ptr(tgt), _ptr(drf), _logit_dtype(tgt), B, K, V, ld, drf_rows, _ptr(tokens), _ptr(uniforms),
         _ptr(temperature), _ptr(_opt(reshape, "reshape", torch.int32)), _ptr(Fh), int(budget),
         _ptr(o["accept_len"]), _ptr(o["bonus"]), _ptr(o.get("p_tok")), _ptr(o.get("q_tok")),
         _ptr(o["cache_tok"]), _ptr(o["hit"]), _ptr(o["slot"]), _ptr(ws), ws.numel(),
-        _ptr(_opt(dev_status, "dev_status", torch.int32)), _stream(stream)), "ssd_round")
+        _ptr(_opt(dev_status, "dev_status", torch.int32)), _stream(stream)), "ssd_round_ld")
     return o
 
 

@@ -144,10 +144,13 @@ int run_units(int mode, const void *tgt, const void *drf, int dtype, int B, int 
               int32_t *accept_len, int32_t *bonus, float *p_tok, float *q_tok, int32_t *cache_tok,
               uint8_t *hit, int32_t *slot, void *workspace, size_t workspace_bytes,
               int32_t *dev_status, void *stream, const int32_t *sig_F = nullptr, float sig_C = 1.f,
-              ssd_reshape_desc *desc_out = nullptr) {
+              ssd_reshape_desc *desc_out = nullptr, int64_t ld = -1) {
     if (dtype != SSD_F32 && dtype != SSD_BF16) return SSD_ERR_DTYPE;
     if (B < 1 || K < 1 || K > SSD_MAX_K || V < 2) return SSD_ERR_INVALID_ARG;
     if (drf_rows != K && drf_rows != K + 1) return SSD_ERR_INVALID_ARG;
+    if (ld < 0) ld = V;
+    if (ld < V) return SSD_ERR_INVALID_ARG;
+    if (sig_F && ld != V) return SSD_ERR_INVALID_ARG;  // descriptors are found on contiguous rows
     if (sig_F) {
         // sigma_{F_k,C} found in the pass: no descriptors in, descriptors out
         if (reshape || !desc_out) return SSD_ERR_INVALID_ARG;
@@ -184,8 +187,9 @@ int run_units(int mode, const void *tgt, const void *drf, int dtype, int B, int 
     // The persistent streaming kernel needs every row on a 16-byte boundary and
     // its per-group arrays within shared memory; other inputs take the cluster kernel.
     const size_t sdyn = ssd::stream_dyn_bytes(V, sig_F != nullptr);
-    const bool stream_ok = aligned(tgt, 16) && aligned(drf, 16) &&
-                           (static_cast<long long>(V) * elem) % 16 == 0 &&
+    // rows on the 16-byte grid, each row readable as whole 16-byte vectors
+    const bool stream_ok = aligned(tgt, 16) && aligned(drf, 16) && (ld * elem) % 16 == 0 &&
+                           ld >= round_up(V, 16 / elem) &&
                            (V + ssd::kGroupTokens - 1) / ssd::kGroupTokens <= ssd::kStreamMaxGroups &&
                            sdyn <= dv->max_dyn[dtype == SSD_F32 ? 4 : 5];
     // With fewer units than SMs the persistent kernel leaves SMs idle and each unit
@@ -202,8 +206,9 @@ int run_units(int mode, const void *tgt, const void *drf, int dtype, int B, int 
 
     P.tgt = tgt;
     P.drf = drf;
-    P.tgt_seq_stride = static_cast<int64_t>(K + 1) * V;
-    P.drf_seq_stride = static_cast<int64_t>(drf_rows) * V;
+    P.ld = ld;
+    P.tgt_seq_stride = static_cast<int64_t>(K + 1) * ld;
+    P.drf_seq_stride = static_cast<int64_t>(drf_rows) * ld;
     P.B = B;
     P.K = K;
     P.V = V;
@@ -331,6 +336,29 @@ int ssd_round(const void *tgt, const void *drf, int dtype, int B, int K, int V, 
                      V, drf_rows, tokens, uniforms, temperature, reshape, F_host, budget,
                      accept_len, bonus, p_tok, q_tok, cache_tok, hit, slot, workspace,
                      workspace_bytes, dev_status, stream);
+}
+
+int ssd_verify_ld(const void *tgt, const void *drf, int dtype, int B, int K, int V, int ld,
+                  int drf_rows, const int32_t *tokens, const float *uniforms, const float *temperature,
+                  const ssd_reshape_desc *reshape, int32_t *accept_len, int32_t *bonus, float *p_tok,
+                  float *q_tok, void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                  void *stream) {
+    return run_units(ssd::kModeVerify, tgt, drf, dtype, B, K, V, drf_rows, tokens, uniforms,
+                     temperature, reshape, nullptr, 0, accept_len, bonus, p_tok, q_tok, nullptr,
+                     nullptr, nullptr, workspace, workspace_bytes, dev_status, stream, nullptr, 1.f,
+                     nullptr, ld);
+}
+
+int ssd_round_ld(const void *tgt, const void *drf, int dtype, int B, int K, int V, int ld,
+                 int drf_rows, const int32_t *tokens, const float *uniforms, const float *temperature,
+                 const ssd_reshape_desc *reshape, const int32_t *F_host, int budget,
+                 int32_t *accept_len, int32_t *bonus, float *p_tok, float *q_tok, int32_t *cache_tok,
+                 uint8_t *hit, int32_t *slot, void *workspace, size_t workspace_bytes,
+                 int32_t *dev_status, void *stream) {
+    return run_units(ssd::kModeVerify | ssd::kModeCache | ssd::kModeLookup, tgt, drf, dtype, B, K,
+                     V, drf_rows, tokens, uniforms, temperature, reshape, F_host, budget,
+                     accept_len, bonus, p_tok, q_tok, cache_tok, hit, slot, workspace,
+                     workspace_bytes, dev_status, stream, nullptr, 1.f, nullptr, ld);
 }
 
 int ssd_verify_sigma(const void *tgt, const void *drf, int dtype, int B, int K, int V, int drf_rows,

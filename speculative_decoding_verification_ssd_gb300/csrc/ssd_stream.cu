@@ -37,6 +37,8 @@
 // Algorithm (Step-by-Step)" and "Temperature and Sampling"; [WHY] "Why does
 // speculative decoding exist?", "How it works"; [SSD] "Speculative Speculative
 // Decoding" notes (papernotes.org), "关键设计" items 1-2 and "整体框架".
+#include <algorithm>
+
 #include "ssd_device.cuh"
 #include "ssd_launch.cuh"
 #include "ssd_stream.cuh"
@@ -161,6 +163,29 @@ __device__ __forceinline__ void load_vecs(const unsigned char *row, int vbase, i
     }
 }
 
+// The row's last vector holds `valid` tokens when the row is not a whole number
+// of 16-byte vectors (a row stride longer than V): the rest read as -inf.
+template <class D>
+__device__ __forceinline__ uint4 mask_tail(uint4 w, int valid) {
+    uint32_t r[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        if (D::kBytes == 4) {
+            if (j >= valid) r[j] = 0xFF800000u;
+        } else {
+            if (2 * j >= valid) r[j] = (r[j] & 0xFFFF0000u) | 0x0000FF80u;
+            if (2 * j + 1 >= valid) r[j] = (r[j] & 0x0000FFFFu) | 0xFF800000u;
+        }
+    }
+    return make_uint4(r[0], r[1], r[2], r[3]);
+}
+template <class D, int VPT>
+__device__ __forceinline__ void mask_partial(uint4 (&w)[VPT], int vbase, int rot, int pv, int valid) {
+#pragma unroll
+    for (int k = 0; k < VPT; ++k)
+        if (vbase + ((k + rot) & (VPT - 1)) == pv) w[k] = mask_tail<D>(w[k], valid);
+}
+
 template <class D, int VPT>
 __device__ __forceinline__ float vecs_max(const uint4 (&w)[VPT]) {
     RawMax<D> rm;
@@ -263,10 +288,11 @@ __device__ __forceinline__ bool stat_ok(Stat s) {
 // st (kept out of line: the common path has no reshape).
 template <class D, int VPT>
 __device__ __noinline__ Stat reshaped_fold(Stat st, const unsigned char *row, int vbase, int nvec, int rot,
-                                           bool full, float c, DraftShape shape, int e0) {
+                                           bool full, float c, DraftShape shape, int e0, int pv, int valid) {
     constexpr int VEC = D::kVec;
     uint4 w[VPT];
     load_vecs<D, VPT>(row, vbase, nvec, rot, full, w);
+    if (pv >= 0) mask_partial<D, VPT>(w, vbase, rot, pv, valid);
     float x[VPT][VEC];
     float xm = -INFINITY;
 #pragma unroll
@@ -296,11 +322,15 @@ __device__ __noinline__ Stat reshaped_fold(Stat st, const unsigned char *row, in
 template <class D, int VPT>
 __device__ __noinline__ float2 reshaped_resid(const unsigned char *stg, int half, int vbase, int nvec,
                                               int rot, bool full, float c, float LT, float LD,
-                                              DraftShape shape, int e0) {
+                                              DraftShape shape, int e0, int pv, int valid) {
     constexpr int VEC = D::kVec;
     uint4 wt[VPT], wd[VPT];
     load_vecs<D, VPT>(stg, vbase, nvec, rot, full, wt);
     load_vecs<D, VPT>(stg + half, vbase, nvec, rot, full, wd);
+    if (pv >= 0) {
+        mask_partial<D, VPT>(wt, vbase, rot, pv, valid);
+        mask_partial<D, VPT>(wd, vbase, rot, pv, valid);
+    }
     float acc = 0.f, mx = 0.f;
 #pragma unroll
     for (int kk = 0; kk < VPT; ++kk) {
@@ -442,7 +472,7 @@ __device__ __noinline__ SigResult sigma_fuse(const unsigned char *drow, const fl
     }
     // the members hold nearly all of the mass and C is small: sum the rest afresh
     Stat sn{-INFINITY, 0.f};
-    const int nvec = static_cast<int>((static_cast<int64_t>(V) * S) / 16);
+    const int nvec = (V + VEC - 1) / VEC;
     for (int v = t; v < nvec; v += kGT) {
         float z[VEC];
         decode_vec<D>(__ldg(reinterpret_cast<const uint4 *>(drow) + v), z);
@@ -452,7 +482,7 @@ __device__ __noinline__ SigResult sigma_fuse(const unsigned char *drow, const fl
         for (int i = 0; i < VEC; ++i) {
             const int e = v * VEC + i;
             const bool mem = z[i] > r.shape.thr || (z[i] == r.shape.thr && e <= r.shape.thr_id);
-            x[i] = mem ? -INFINITY : z[i] * c;
+            x[i] = (mem || e >= V) ? -INFINITY : z[i] * c;
             xm = fmaxf(xm, x[i]);
         }
         stat_fold(sn, xm, [&](float mn) {
@@ -483,7 +513,10 @@ __device__ __noinline__ SigResult sigma_fuse(const unsigned char *drow, const fl
 
 }  // namespace
 
-template <class D, bool kSig>
+// kSig: sigma_{F,C} found in the pass.  kTail: rows are not whole 16-byte
+// vectors (a row stride longer than V), so each row's last vector is masked; the
+// common form carries none of that code.
+template <class D, bool kSig, bool kTail>
 __global__ void __launch_bounds__(kStreamThreads, 1)
     ssd_stream_kernel(const __grid_constant__ UnitParams P) {
     constexpr int VEC = D::kVec, S = D::kBytes;
@@ -520,7 +553,11 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     const bool do_verify = (P.mode & kModeVerify) != 0;
     const bool do_cache = (P.mode & kModeCache) != 0;
     const int nunits = B * (K + 1);
-    const int64_t row_bytes = static_cast<int64_t>(V) * S;
+    // a row is streamed as whole 16-byte vectors: with a row stride longer than V
+    // the last vector carries V % VEC tokens and the rest is masked on arrival
+    const int nvec_row = (V + VEC - 1) / VEC;
+    const int vtail = kTail ? V % VEC : 0;
+    const int64_t row_bytes = static_cast<int64_t>(nvec_row) * 16;
 
     if (tid == 0) {
         for (int g = 0; g < kNG; ++g) {
@@ -677,10 +714,10 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             const uint32_t mask = (k >= 32) ? 0xFFFFFFFFu : ((1u << k) - 1u);
             const bool skip = (P.mode & kModeEarlyExit) && k > 0 && (pf_rej & mask) != 0;
             const unsigned char *trow = static_cast<const unsigned char *>(P.tgt) +
-                                        (static_cast<int64_t>(b) * P.tgt_seq_stride + static_cast<int64_t>(k) * V) * S;
+                                        (static_cast<int64_t>(b) * P.tgt_seq_stride + static_cast<int64_t>(k) * P.ld) * S;
             const unsigned char *drow =
                 pair ? static_cast<const unsigned char *>(P.drf) +
-                           (static_cast<int64_t>(b) * P.drf_seq_stride + static_cast<int64_t>(k) * V) * S
+                           (static_cast<int64_t>(b) * P.drf_seq_stride + static_cast<int64_t>(k) * P.ld) * S
                      : nullptr;
             const int cb = pair ? HALF : kSB;
             const int nch = static_cast<int>((row_bytes + cb - 1) / cb);
@@ -753,9 +790,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             const int Fk = do_cache ? P.F[k] : 0;
             const float c = d.c;
             const unsigned char *trow = static_cast<const unsigned char *>(P.tgt) +
-                                        (static_cast<int64_t>(b) * P.tgt_seq_stride + static_cast<int64_t>(k) * V) * S;
+                                        (static_cast<int64_t>(b) * P.tgt_seq_stride + static_cast<int64_t>(k) * P.ld) * S;
             const unsigned char *drow = static_cast<const unsigned char *>(P.drf) +
-                                        (static_cast<int64_t>(b) * P.drf_seq_stride + static_cast<int64_t>(k) * V) * S;
+                                        (static_cast<int64_t>(b) * P.drf_seq_stride + static_cast<int64_t>(k) * P.ld) * S;
             const int xt = d.xt;
             const int xmask = (d.kind == kKindGreedy && k < K) ? xt : -1;
             const float nLT = -d.LT;
@@ -891,6 +928,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
 #pragma unroll
                             for (int i = 0; i < VEC; ++i) {
                                 const int e = e0[x] + i;
+                                if (e >= V) break;  // the row's partial last vector
                                 uint64_t key;
                                 if (resid)
                                     key = make_key(resid_e(zt[i], zd[i], e), e);
@@ -1328,11 +1366,11 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             ztx = 0.f;
             if (t == 0 && active && k < K) {
                 const unsigned char *trow = static_cast<const unsigned char *>(P.tgt) +
-                                            (static_cast<int64_t>(b) * P.tgt_seq_stride + static_cast<int64_t>(k) * V) * S;
+                                            (static_cast<int64_t>(b) * P.tgt_seq_stride + static_cast<int64_t>(k) * P.ld) * S;
                 ztx = load_logit<D>(trow, xt);
                 if (pair) {
                     const unsigned char *drow = static_cast<const unsigned char *>(P.drf) +
-                                                (static_cast<int64_t>(b) * P.drf_seq_stride + static_cast<int64_t>(k) * V) * S;
+                                                (static_cast<int64_t>(b) * P.drf_seq_stride + static_cast<int64_t>(k) * P.ld) * S;
                     zdx = load_logit<D>(drow, xt);
                     u_k = P.uniforms ? P.uniforms[static_cast<int64_t>(b) * (K + 1) + k] : 0.f;
                 }
@@ -1347,12 +1385,16 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         }
         const unsigned char *stg = ring + s * kSB;
         const bool stage_pair = (h.code >> 5) & 1;
+        // the stage holding a row's partial last vector (row stride longer than V)
+        const bool part = vtail != 0 && h.chunk * (stage_pair ? FULL_PAIR : FULL_ONE) + h.nvec == nvec_row;
+        const int pv = part ? h.nvec - 1 : -1;
         // ---- stage processing -----------------------------------------------
         if (active) {
             if (pass == kPassStats && stage_pair) {
                 // online statistics: threads [0, 128) target, the rest draft
                 uint4 w[VPT1];
-                load_vecs<D, VPT1>(stg + p1_row * HALF, p1_vbase, h.nvec, p1_rot, h.nvec == FULL_PAIR, w);
+                load_vecs<D, VPT1>(stg + p1_row * HALF, p1_vbase, h.nvec, p1_rot, h.nvec == FULL_PAIR && !part, w);
+                if (part) mask_partial<D, VPT1>(w, p1_vbase, p1_rot, pv, vtail);
                 const float rm = vecs_max<D, VPT1>(w);
                 // a reshaped draft row takes the plain path where none of the thread's
                 // tokens reaches the top-F threshold (all but a few threads of the row)
@@ -1365,14 +1407,15 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                         if (p1_tr % TPG1 == 0 && g < G) gmax[g] = canon_zero(gm);
                     }
                 } else {
-                    st = reshaped_fold<D, VPT1>(st, stg + HALF, p1_vbase, h.nvec, p1_rot, h.nvec == FULL_PAIR, c,
-                                                shape, h.chunk * (FULL_PAIR * VEC) + p1_vbase * VEC);
+                    st = reshaped_fold<D, VPT1>(st, stg + HALF, p1_vbase, h.nvec, p1_rot, h.nvec == FULL_PAIR && !part,
+                                                c, shape, h.chunk * (FULL_PAIR * VEC) + p1_vbase * VEC, pv, vtail);
                 }
             } else if (pass == kPassStats) {
                 // one row: sampled row K (maxima, masses, statistics) or greedy (maxima,
                 // drafted token excluded)
                 uint4 w[VPTS];
-                load_vecs<D, VPTS>(stg, s_vbase, h.nvec, s_rot, h.nvec == FULL_ONE, w);
+                load_vecs<D, VPTS>(stg, s_vbase, h.nvec, s_rot, h.nvec == FULL_ONE && !part, w);
+                if (part) mask_partial<D, VPTS>(w, s_vbase, s_rot, pv, vtail);
                 const int e0 = h.chunk * (FULL_ONE * VEC) + s_vbase * VEC;
                 if (static_cast<unsigned>(xmask - e0) < static_cast<unsigned>(VPTS * VEC)) {
 #pragma unroll
@@ -1400,12 +1443,16 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                 }
             } else {
                 // pass 2 (pair): residual masses and maxima per group
-                const bool full = h.nvec == FULL_PAIR;
+                const bool full = h.nvec == FULL_PAIR && !part;
                 float2 acc = make_float2(0.f, 0.f);
                 float mx = 0.f;
                 uint4 wt[VPT2], wd[VPT2];
                 load_vecs<D, VPT2>(stg, r_vbase, h.nvec, r_rot, full, wt);
                 load_vecs<D, VPT2>(stg + HALF, r_vbase, h.nvec, r_rot, full, wd);
+                if (part) {
+                    mask_partial<D, VPT2>(wt, r_vbase, r_rot, pv, vtail);
+                    mask_partial<D, VPT2>(wd, r_vbase, r_rot, pv, vtail);
+                }
                 // reshaped draft: only tokens at or above the top-F threshold carry a bias
                 if (!shape.on || !(vecs_max<D, VPT2>(wd) >= shape.thr)) {
                     const float2 cc = make_float2(c, c), nl = make_float2(-LT, -LD);
@@ -1428,7 +1475,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                     }
                 } else {
                     const float2 r2 = reshaped_resid<D, VPT2>(stg, HALF, r_vbase, h.nvec, r_rot, full, c, LT, LD, shape,
-                                                              h.chunk * (FULL_PAIR * VEC) + r_vbase * VEC);
+                                                              h.chunk * (FULL_PAIR * VEC) + r_vbase * VEC, pv, vtail);
                     acc.x = r2.x;
                     mx = r2.y;
                 }
@@ -1474,7 +1521,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             float qm = gD.m, qS = gD.S;
             if (sig) {
                 const unsigned char *drow = static_cast<const unsigned char *>(P.drf) +
-                                            (static_cast<int64_t>(b) * P.drf_seq_stride + static_cast<int64_t>(k) * V) * S;
+                                            (static_cast<int64_t>(b) * P.drf_seq_stride + static_cast<int64_t>(k) * P.ld) * S;
                 const SigResult sr = sigma_fuse<D>(drow, gmax, G, V, P.sig_F[k], P.sig_C, c, gD, sig_keys, &gs.scnt,
                                                    reinterpret_cast<float *>(gs.red), t, bar_id);
                 shape = sr.shape;
@@ -1530,16 +1577,27 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     handoff(kKindStop, 0, 0.f, 0.f);
 }
 
-int stream_setup(int dtype, size_t optin, size_t *max_dyn) {
+template <class D>
+int stream_setup_d(size_t optin, size_t *max_dyn) {
     bool dummy = true;
-    size_t with_sig = 0;
-    const int st = dtype == SSD_F32 ? setup_kernel(ssd_stream_kernel<F32Tag, true>, optin, &with_sig, &dummy)
-                                    : setup_kernel(ssd_stream_kernel<BF16Tag, true>, optin, &with_sig, &dummy);
+    size_t lim[4];
+    int st = setup_kernel(ssd_stream_kernel<D, true, false>, optin, &lim[0], &dummy);
+    if (st == SSD_OK) st = setup_kernel(ssd_stream_kernel<D, false, true>, optin, &lim[1], &dummy);
+    if (st == SSD_OK) st = setup_kernel(ssd_stream_kernel<D, false, false>, optin, &lim[2], &dummy);
     if (st != SSD_OK) return st;
-    const int st2 = dtype == SSD_F32 ? setup_kernel(ssd_stream_kernel<F32Tag, false>, optin, max_dyn, &dummy)
-                                     : setup_kernel(ssd_stream_kernel<BF16Tag, false>, optin, max_dyn, &dummy);
-    if (with_sig < *max_dyn) *max_dyn = with_sig;  // one limit for both forms
-    return st2;
+    *max_dyn = std::min(lim[0], std::min(lim[1], lim[2]));  // one limit for every form
+    return SSD_OK;
+}
+
+int stream_setup(int dtype, size_t optin, size_t *max_dyn) {
+    return dtype == SSD_F32 ? stream_setup_d<F32Tag>(optin, max_dyn) : stream_setup_d<BF16Tag>(optin, max_dyn);
+}
+
+template <class D>
+cudaError_t stream_launch_d(const cudaLaunchConfig_t &cfg, const UnitParams &P) {
+    if (P.sig_on) return cudaLaunchKernelEx(&cfg, ssd_stream_kernel<D, true, false>, P);
+    if (P.V % D::kVec != 0) return cudaLaunchKernelEx(&cfg, ssd_stream_kernel<D, false, true>, P);
+    return cudaLaunchKernelEx(&cfg, ssd_stream_kernel<D, false, false>, P);
 }
 
 int stream_launch(int dtype, const UnitParams &P, int grid, size_t dyn, void *stream) {
@@ -1549,13 +1607,7 @@ int stream_launch(int dtype, const UnitParams &P, int grid, size_t dyn, void *st
     cfg.dynamicSmemBytes = dyn;
     cfg.stream = static_cast<cudaStream_t>(stream);
     cfg.numAttrs = 0;
-    cudaError_t e;
-    if (P.sig_on)
-        e = dtype == SSD_F32 ? cudaLaunchKernelEx(&cfg, ssd_stream_kernel<F32Tag, true>, P)
-                             : cudaLaunchKernelEx(&cfg, ssd_stream_kernel<BF16Tag, true>, P);
-    else
-        e = dtype == SSD_F32 ? cudaLaunchKernelEx(&cfg, ssd_stream_kernel<F32Tag, false>, P)
-                             : cudaLaunchKernelEx(&cfg, ssd_stream_kernel<BF16Tag, false>, P);
+    const cudaError_t e = dtype == SSD_F32 ? stream_launch_d<F32Tag>(cfg, P) : stream_launch_d<BF16Tag>(cfg, P);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return SSD_ERR_CUDA;

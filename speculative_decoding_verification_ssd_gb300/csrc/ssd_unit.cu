@@ -311,10 +311,10 @@ __global__ void __launch_bounds__(kThreads, 3) ssd_unit_kernel(const __grid_cons
     unsigned char *buf_d = dyn_smem + P.row_buf_bytes;
     const unsigned char *tgt_row = static_cast<const unsigned char *>(P.tgt) +
                                    (static_cast<int64_t>(b) * P.tgt_seq_stride +
-                                    static_cast<int64_t>(k) * V) * D::kBytes;
+                                    static_cast<int64_t>(k) * P.ld) * D::kBytes;
     const unsigned char *drf_row =
         pair ? static_cast<const unsigned char *>(P.drf) +
-                   (static_cast<int64_t>(b) * P.drf_seq_stride + static_cast<int64_t>(k) * V) *
+                   (static_cast<int64_t>(b) * P.drf_seq_stride + static_cast<int64_t>(k) * P.ld) *
                        D::kBytes
              : nullptr;
     if (tid == 0) {

@@ -30,8 +30,9 @@ static_assert(sizeof(UnitRecord) == 32, "record layout");
 struct UnitParams {
     const void *tgt;
     const void *drf;
-    int64_t tgt_seq_stride;  // elements between sequences of tgt ((K+1) V)
-    int64_t drf_seq_stride;  // elements between sequences of drf (drf_rows V)
+    int64_t ld;              // elements between consecutive rows (>= V)
+    int64_t tgt_seq_stride;  // elements between sequences of tgt ((K+1) ld)
+    int64_t drf_seq_stride;  // elements between sequences of drf (drf_rows ld)
     int B, K, V;
     int CL;              // CTAs per unit (thread-block cluster size)
     int slice;           // vocabulary entries per CTA (multiple of the 16-byte vector)

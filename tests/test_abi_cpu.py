@@ -176,6 +176,10 @@ def test_device_calls_validate_before_any_cuda_call(ssd):
     assert L.ssd_check_wait_timeout(None, 20, None) == ssd.SSD_ERR_INVALID_ARG
     assert L.ssd_check_wait_timeout(p, 0, None) == ssd.SSD_ERR_INVALID_ARG
     assert L.ssd_check_wait_timeout(p, 10001, None) == ssd.SSD_ERR_INVALID_ARG
+    assert L.ssd_verify_ld(p, p, 0, 4, 2, 100, 99, 2, p, p, p, None, p, p, None, None, p, ws_ok, None,
+                           None) == ssd.SSD_ERR_INVALID_ARG  # ld < V
+    assert L.ssd_round_ld(p, p, 0, 4, 2, 100, 99, 2, p, p, p, None, Fp, 6, p, p, None, None, p, p, p,
+                          p, ws_ok, None, None) == ssd.SSD_ERR_INVALID_ARG
     bf = L.ssd_backup_fill
     assert bf(p, p, 0, 4, 100, p, None) == ssd.SSD_ERR_INVALID_ARG
     assert bf(p, p, 4, 0, 100, p, None) == ssd.SSD_ERR_INVALID_ARG
