@@ -1,8 +1,8 @@
 """Rarely taken paths of the streaming kernel (rows on the 16-byte grid), each
 compared with the float64 oracle:
 
-* a draft row equal to its target row: no residual mass, so the bonus prepared
-  for each position is drawn from p;
+* a draft row equal to its target row, rejected at a token both give
+  probability 0: no residual mass, so the bonus is drawn from p;
 * a fan-out with F_k above 64, where the top-F threshold is found by bisection
   over the group maxima instead of from the lanes' two largest maxima;
 * rows whose logits are all equal, where every group reaches the threshold
@@ -65,44 +65,34 @@ def _round_and_compare(ssd, inp, budget, a_p, r):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_draft_equal_to_target_prepares_bonus_from_p(ssd, dtype):
-    """q = p: every position accepts (u < 1), and the bonus the round would draw had it
-    stopped at k -- prepared for every k and kept in the workspace record -- comes from
-    p_k, since the residual has no mass."""
+def test_draft_equal_to_target_draws_bonus_from_p(ssd, dtype):
+    """q = p, and the drafted token at position a = b mod K has logit -inf in both
+    rows: positions before a accept (u < 1), a rejects (u * 0 < 0 fails), and the
+    residual at a has no mass, so the bonus is drawn from p_a."""
     rng = np.random.default_rng(31)
     B, K, V = 8, 3, 20000
     zt = (rng.standard_normal((B, K + 1, V)) * 2.5).astype(np.float32)
-    zd = zt[:, :K].copy()
     tok = rng.integers(0, V, (B, K))
+    want_a = np.arange(B) % K
+    for b in range(B):
+        zt[b, want_a[b], tok[b, want_a[b]]] = -np.inf
+    zd = zt[:, :K].copy()
     u = rng.random((B, K + 1))
     inp = _pack(zt, zd, tok, u, [1.0] * B, dtype)
-    budget, a_p, r = 24, 0.7, 0.5
-    F, off = ssd.ssd_fanout(K, budget, a_p, r, V)
-    d = to_device(inp)
-    ws = ssd.workspace(B, K)
-    g = np_out(ssd.ssd_round(d["tgt"], d["drf"], d["tokens"], d["uniforms"], d["temperature"], F,
-                             budget, workspace=ws))
-    rec = ws[: B * (K + 1) * 32].view(torch.int32).reshape(B, K + 1, 8).cpu().numpy()
-    o = oracle.round_(inp["tgt"], inp["drf"], inp["tokens"], inp["uniforms"], inp["temperature"],
-                      dtype, off, budget)
-    t = Tally()
-    compare_verify(g, o, K, t)
-    compare_cache(g["cache_tok"], o, off, K, t)
-    t.check()
-    assert (g["accept_len"] == K).all()
+    g, o, F = _round_and_compare(ssd, inp, 24, 0.7, 0.5)
+    np.testing.assert_array_equal(g["accept_len"], want_a)
     zs = synth.stored_to_f32(inp["tgt"], dtype)
     checked = 0
     for b in range(B):
-        for k in range(K):
-            p = oracle.softmax(zs[b, k].astype(np.float64), 1.0)
-            cum = np.cumsum(p)
-            T = float(inp["uniforms"][b, K]) * cum[-1]
-            want = int(np.searchsorted(cum, T, side="right"))
-            if abs(cum[min(want, V - 1)] - T) < 1e-6 or (want > 0 and abs(cum[want - 1] - T) < 1e-6):
-                continue  # too close to a boundary to be a clean decision
-            assert rec[b, k, 3] == want, (b, k, rec[b, k, 3], want)
-            checked += 1
-    assert checked >= B * K - 2
+        p = oracle.softmax(zs[b, want_a[b]].astype(np.float64), 1.0)
+        cum = np.cumsum(p)
+        T = float(inp["uniforms"][b, K]) * cum[-1]
+        want = int(np.searchsorted(cum, T, side="right"))
+        if abs(cum[min(want, V - 1)] - T) < 1e-6 or (want > 0 and abs(cum[want - 1] - T) < 1e-6):
+            continue  # too close to a boundary to be a clean decision
+        assert g["bonus"][b] == want, (b, g["bonus"][b], want)
+        checked += 1
+    assert checked >= B - 1
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
