@@ -338,29 +338,37 @@ def run_ours(args):
 
     # end to end: pinned host inputs -> device, round, outputs -> host, every step
     host = {k: v.cpu().pin_memory() for k, v in d.items()}
-    dev_in = {k: torch.empty_like(v) for k, v in d.items()}
-    h2d = sum(v.numel() * v.element_size() for v in host.values())
     res_keys = ["accept_len", "bonus"] + (["cache_tok", "hit", "slot"] if wl.mode == "round" else [])
     host_out = {k: torch.empty(out[k].shape, dtype=out[k].dtype).pin_memory() for k in res_keys}
     d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+    if wl.mode == "round":
+        # the library's host-buffer round: it copies the target logits and only the
+        # sampled sequences' draft rows, runs the round and copies the results back
+        staging = torch.empty(ssd.ssd_host_staging_size(ssd._logit_dtype(d["tgt"]), wl.B, wl.K, wl.V,
+                                                        wl.budget), dtype=torch.uint8, device=dev)
+        h2d_box = [0]
 
-    def e2e_step():
-        for k in dev_in:
-            dev_in[k].copy_(host[k], non_blocking=True)
-        if wl.mode == "round":
-            o = ssd.ssd_round(dev_in["tgt"], dev_in["drf"], dev_in["tokens"], dev_in["uniforms"],
-                              dev_in["temperature"], F, wl.budget, out=out, probs=False,
-                              workspace=ws, stream=stream)
-        elif sig:
-            o = ssd.ssd_verify_sigma(dev_in["tgt"], dev_in["drf"], dev_in["tokens"],
-                                     dev_in["uniforms"], dev_in["temperature"], sig_F,
-                                     wl.reshape_C, desc_out=desc, probs=False, workspace=ws,
-                                     stream=stream)
-        else:
-            o = ssd.ssd_verify(dev_in["tgt"], dev_in["drf"], dev_in["tokens"], dev_in["uniforms"],
-                               dev_in["temperature"], probs=False, workspace=ws, stream=stream)
-        for k in res_keys:
-            host_out[k].copy_(o[k], non_blocking=True)
+        def e2e_step():
+            _, h2d_box[0] = ssd.ssd_round_host(host["tgt"], host["drf"], host["tokens"], host["uniforms"],
+                                               host["temperature"], F, wl.budget, out=host_out,
+                                               staging=staging, workspace=ws, stream=stream)
+    else:
+        dev_in = {k: torch.empty_like(v) for k, v in d.items()}
+        h2d_box = [sum(v.numel() * v.element_size() for v in host.values())]
+
+        def e2e_step():
+            for k in dev_in:
+                dev_in[k].copy_(host[k], non_blocking=True)
+            if sig:
+                o = ssd.ssd_verify_sigma(dev_in["tgt"], dev_in["drf"], dev_in["tokens"],
+                                         dev_in["uniforms"], dev_in["temperature"], sig_F,
+                                         wl.reshape_C, desc_out=desc, probs=False, workspace=ws,
+                                         stream=stream)
+            else:
+                o = ssd.ssd_verify(dev_in["tgt"], dev_in["drf"], dev_in["tokens"], dev_in["uniforms"],
+                                   dev_in["temperature"], probs=False, workspace=ws, stream=stream)
+            for k in res_keys:
+                host_out[k].copy_(o[k], non_blocking=True)
 
     for _ in range(3):
         e2e_step()
@@ -396,7 +404,7 @@ def run_ours(args):
                      "traffic": traffic_record(_build.stream_kernel_digest()),
                      "kernel": "ssd_stream_kernel<BF16Tag>"},
         "e2e": {"value": job_rate(args.e2e_steps, world, e2e_ms), "unit": "rounds/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d_box[0], "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps * launches_per_step,
         "clocks": clocks,
         "accept_mean": float(np.mean(acc[acc >= 0])) if (acc >= 0).any() else None,

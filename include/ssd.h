@@ -348,6 +348,39 @@ int ssd_round_noalloc(const void *tgt, const void *drf, int dtype, int B, int K,
                       float *p_tok, float *q_tok, int32_t *cache_tok, uint8_t *hit,
                       int32_t *slot, int32_t *dev_status, void *stream);
 
+/*
+ * ssd_round_host -- ssd_round on inputs and outputs in host memory (no
+ * counterpart on the pages: the transfer plumbing around [SSD] "整体框架").
+ * Enqueues on `stream`: the copies of the inputs into `staging`, the round
+ * (ssd_round with drf_rows = K, no reshape, no p/q outputs) and the copies of
+ * its results back.  A sequence that does not sample (tau == 0 decides by the
+ * target argmax, [WHY] Fix 2; an invalid tau is reported) never has its draft
+ * logits read, so only the sampled sequences' draft rows are copied, each run
+ * of consecutive sampled sequences as one copy: the host-to-device traffic is
+ * the target logits, those draft rows, tokens, uniforms and temperatures.
+ * Inputs (host memory; page-locked for the copies to run asynchronously):
+ *   tgt [B, K+1, V] and drf [B, K, V] of `dtype`, contiguous; tokens [B, K];
+ *   uniforms [B, K+1]; temperature [B] (also read by the host during the
+ *   call); F_host [K+1] and budget as in ssd_build_cache.
+ * Outputs (host memory, valid once `stream` has completed): accept_len [B],
+ *   bonus [B], cache_tok [B, budget], hit [B], slot [B] as in ssd_round.
+ * staging: device memory of at least ssd_host_staging_size(dtype, B, K, V,
+ *   budget) bytes, owned by the caller, 256-byte aligned; workspace as in
+ *   ssd_round.  h2d_bytes (host, may be NULL) receives the bytes copied to
+ *   the device by this call.
+ * Errors (before anything is enqueued): SSD_ERR_DTYPE for an unknown dtype;
+ * SSD_ERR_INVALID_ARG for a NULL pointer, a size out of range, a fan-out that
+ * ssd_build_cache would reject or a staging buffer that is too small.  Later:
+ * SSD_ERR_CUDA when a copy cannot be enqueued; otherwise as ssd_round.
+ */
+size_t ssd_host_staging_size(int dtype, int B, int K, int V, int budget);
+int ssd_round_host(const void *tgt, const void *drf, int dtype, int B, int K, int V,
+                   const int32_t *tokens, const float *uniforms, const float *temperature,
+                   const int32_t *F_host, int budget, int32_t *accept_len, int32_t *bonus,
+                   int32_t *cache_tok, uint8_t *hit, int32_t *slot, void *staging,
+                   size_t staging_bytes, void *workspace, size_t workspace_bytes,
+                   int32_t *dev_status, size_t *h2d_bytes, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -43,7 +43,8 @@ ABI_SYMBOLS = ("ssd_strerror", "ssd_version", "ssd_workspace_size", "ssd_verify"
                "ssd_reshape_draft", "ssd_build_cache", "ssd_cache_lookup", "ssd_round",
                "ssd_noalloc_max_scratch", "ssd_round_noalloc", "ssd_fanout_uniform",
                "ssd_backup_fill", "ssd_draft_cache", "ssd_verify_sigma", "ssd_round_sigma",
-               "ssd_set_dispatch", "ssd_check_wait_timeout", "ssd_verify_ld", "ssd_round_ld")
+               "ssd_set_dispatch", "ssd_check_wait_timeout", "ssd_verify_ld", "ssd_round_ld",
+               "ssd_host_staging_size", "ssd_round_host")
 
 
 class SSDError(RuntimeError):
@@ -109,6 +110,11 @@ def lib() -> ctypes.CDLL:
         L.ssd_round_ld.argtypes = [P, P, i, i, i, i, i, i, P, P, P, P, P, i, P, P, P, P, P, P, P, P,
                                    z, P, P]
         L.ssd_round_ld.restype = i
+        L.ssd_host_staging_size.argtypes = [i, i, i, i, i]
+        L.ssd_host_staging_size.restype = z
+        L.ssd_round_host.argtypes = [P, P, i, i, i, i, P, P, P, P, i, P, P, P, P, P, P, z, P, z, P, P,
+                                     P]
+        L.ssd_round_host.restype = i
         _lib = L
     return _lib
 
@@ -389,6 +395,69 @@ def ssd_round(tgt, drf, tokens, uniforms, temperature, F, budget, reshape=None, 
         _ptr(o["cache_tok"]), _ptr(o["hit"]), _ptr(o["slot"]), _ptr(ws), ws.numel(),
         _ptr(_opt(dev_status, "dev_status", torch.int32)), _stream(stream)), "ssd_round_ld")
     return o
+
+
+def _host(t, name: str, dtype=None) -> torch.Tensor:
+    if not isinstance(t, torch.Tensor) or t.device.type != "cpu":
+        raise TypeError(f"{name} must be a host (CPU) tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def ssd_host_staging_size(dtype: int, B: int, K: int, V: int, budget: int) -> int:
+    """Device bytes ssd_round_host needs for its copies of one round's inputs and outputs."""
+    return int(lib().ssd_host_staging_size(int(dtype), int(B), int(K), int(V), int(budget)))
+
+
+def ssd_round_host(tgt, drf, tokens, uniforms, temperature, F, budget, *, out=None, staging=None,
+                   workspace=None, dev_status=None, stream=None, device=None):
+    """ssd_round on host tensors (page-locked ones copy asynchronously): the inputs
+    are copied to the device (the draft rows of sampled sequences only), the round
+    runs and its results are copied back, all on `stream`.  Returns (outputs, h2d):
+    a dict of host tensors accept_len, bonus, cache_tok, hit, slot -- valid once the
+    stream has completed -- and the bytes copied to the device."""
+    _host(tgt, "tgt")
+    _host(drf, "drf", tgt.dtype)
+    if tgt.dim() != 3 or drf.dim() != 3:
+        raise ValueError("tgt must be [B, K+1, V] and drf [B, K, V]")
+    B, K1, V = tgt.shape
+    K = K1 - 1
+    if tuple(drf.shape) != (B, K, V):
+        raise ValueError("drf must be [B, K, V]")
+    _host(tokens, "tokens", torch.int32)
+    _host(uniforms, "uniforms", torch.float32)
+    _host(temperature, "temperature", torch.float32)
+    if tuple(tokens.shape) != (B, K) or tuple(uniforms.shape) != (B, K + 1) or tuple(temperature.shape) != (B,):
+        raise ValueError("tokens [B, K], uniforms [B, K+1] and temperature [B] expected")
+    dt = _logit_dtype(tgt)
+    Fh = _F_host(F)
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    o = dict(out) if out is not None else {}
+    shapes = {"accept_len": ((B,), torch.int32), "bonus": ((B,), torch.int32),
+              "cache_tok": ((B, int(budget)), torch.int32), "hit": ((B,), torch.uint8),
+              "slot": ((B,), torch.int32)}
+    for k, (shp, dty) in shapes.items():
+        if k not in o:
+            o[k] = torch.empty(shp, dtype=dty).pin_memory()
+        _host(o[k], k, dty)
+    need = ssd_host_staging_size(dt, B, K, V, budget)
+    if need == 0:
+        raise ValueError("invalid sizes for ssd_round_host")
+    if staging is None:
+        staging = torch.empty(need, dtype=torch.uint8, device=dev)
+    _dev(staging, "staging", torch.uint8)
+    ws = _workspace(workspace, B, K, dev)
+    moved = ctypes.c_size_t(0)
+    _check(lib().ssd_round_host(
+        _ptr(tgt), _ptr(drf), dt, B, K, V, _ptr(tokens), _ptr(uniforms), _ptr(temperature), _ptr(Fh),
+        int(budget), _ptr(o["accept_len"]), _ptr(o["bonus"]), _ptr(o["cache_tok"]), _ptr(o["hit"]),
+        _ptr(o["slot"]), _ptr(staging), staging.numel(), _ptr(ws), ws.numel(),
+        _ptr(_opt(dev_status, "dev_status", torch.int32)), ctypes.c_void_p(ctypes.addressof(moved)),
+        _stream(stream)), "ssd_round_host")
+    return o, int(moved.value)
 
 
 def _sigma_args(sigma_F, K, B, desc_out, dev):

@@ -559,3 +559,142 @@ int ssd_round_noalloc(const void *tgt, const void *drf, int dtype, int B, int K,
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Rounds from host buffers: the staging layout in device memory (every part on
+// a 256-byte boundary) and the copies around the round.
+namespace {
+
+struct HostStaging {
+    size_t tgt, drf, tok, uni, tau, acc, bon, cache, hit, slot, total;
+};
+
+HostStaging host_staging_layout(int dtype, int B, int K, int V, int budget) {
+    const auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+    const size_t s = dtype == SSD_F32 ? 4 : 2;
+    const size_t b = static_cast<size_t>(B);
+    HostStaging L;
+    size_t o = 0;
+    L.tgt = o;
+    o = up(o + b * (K + 1) * V * s);
+    L.drf = o;
+    o = up(o + b * K * V * s);
+    L.tok = o;
+    o = up(o + b * K * 4);
+    L.uni = o;
+    o = up(o + b * (K + 1) * 4);
+    L.tau = o;
+    o = up(o + b * 4);
+    L.acc = o;
+    o = up(o + b * 4);
+    L.bon = o;
+    o = up(o + b * 4);
+    L.cache = o;
+    o = up(o + b * static_cast<size_t>(budget) * 4);
+    L.hit = o;
+    o = up(o + b);
+    L.slot = o;
+    o = up(o + b * 4);
+    L.total = o;
+    return L;
+}
+
+bool host_staging_args_ok(int dtype, int B, int K, int V, int budget) {
+    return B >= 1 && K >= 1 && K <= SSD_MAX_K && V >= 2 && budget >= 0 &&
+           (dtype == SSD_F32 || dtype == SSD_BF16);
+}
+
+// The fan-out checks of the round, taken before any copy is enqueued.
+bool host_fanout_ok(const int32_t *F_host, int K, int V, int budget) {
+    int64_t sum = 0;
+    for (int k = 0; k <= K; ++k) {
+        if (F_host[k] < 0 || F_host[k] > V || F_host[k] > SSD_MAX_F) return false;
+        sum += F_host[k];
+    }
+    return sum <= budget;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t ssd_host_staging_size(int dtype, int B, int K, int V, int budget) {
+    if (!host_staging_args_ok(dtype, B, K, V, budget)) return 0;
+    return host_staging_layout(dtype, B, K, V, budget).total;
+}
+
+int ssd_round_host(const void *tgt, const void *drf, int dtype, int B, int K, int V,
+                   const int32_t *tokens, const float *uniforms, const float *temperature,
+                   const int32_t *F_host, int budget, int32_t *accept_len, int32_t *bonus,
+                   int32_t *cache_tok, uint8_t *hit, int32_t *slot, void *staging,
+                   size_t staging_bytes, void *workspace, size_t workspace_bytes,
+                   int32_t *dev_status, size_t *h2d_bytes, void *stream) {
+    if (dtype != SSD_F32 && dtype != SSD_BF16) return SSD_ERR_DTYPE;
+    if (!host_staging_args_ok(dtype, B, K, V, budget)) return SSD_ERR_INVALID_ARG;
+    if (!tgt || !drf || !tokens || !uniforms || !temperature || !F_host || !accept_len || !bonus ||
+        !cache_tok || !hit || !slot || !staging)
+        return SSD_ERR_INVALID_ARG;
+    if (!host_fanout_ok(F_host, K, V, budget)) return SSD_ERR_INVALID_ARG;
+    const HostStaging L = host_staging_layout(dtype, B, K, V, budget);
+    if (staging_bytes < L.total) return SSD_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    unsigned char *base = static_cast<unsigned char *>(staging);
+    size_t moved = 0;
+    bool ok = true;
+    const auto h2d = [&](size_t off, const void *src, size_t n) {
+        if (!ok || n == 0) return;
+        moved += n;
+        ok = cudaMemcpyAsync(base + off, src, n, cudaMemcpyHostToDevice, st) == cudaSuccess;
+    };
+    const auto d2h = [&](void *dst, size_t off, size_t n) {
+        if (!ok || n == 0) return;
+        ok = cudaMemcpyAsync(dst, base + off, n, cudaMemcpyDeviceToHost, st) == cudaSuccess;
+    };
+    const size_t row = static_cast<size_t>(V) * (dtype == SSD_F32 ? 4 : 2);
+    const size_t seq_d = static_cast<size_t>(K) * row;
+    h2d(L.tgt, tgt, static_cast<size_t>(B) * (K + 1) * row);
+    // Draft rows of the sampled sequences only (a run of consecutive ones in one
+    // copy): a greedy or invalid sequence's draft logits are never read.
+    for (int b = 0; b < B;) {
+        const auto sampled = [&](int i) { return temperature[i] > 0.f && temperature[i] < INFINITY; };
+        if (!sampled(b)) {
+            ++b;
+            continue;
+        }
+        int e = b + 1;
+        while (e < B && sampled(e)) ++e;
+        h2d(L.drf + static_cast<size_t>(b) * seq_d,
+            static_cast<const unsigned char *>(drf) + static_cast<size_t>(b) * seq_d,
+            static_cast<size_t>(e - b) * seq_d);
+        b = e;
+    }
+    h2d(L.tok, tokens, static_cast<size_t>(B) * K * 4);
+    h2d(L.uni, uniforms, static_cast<size_t>(B) * (K + 1) * 4);
+    h2d(L.tau, temperature, static_cast<size_t>(B) * 4);
+    if (!ok) {
+        cudaGetLastError();
+        return SSD_ERR_CUDA;
+    }
+    const int rc = ssd_round(base + L.tgt, base + L.drf, dtype, B, K, V, K,
+                             reinterpret_cast<const int32_t *>(base + L.tok),
+                             reinterpret_cast<const float *>(base + L.uni),
+                             reinterpret_cast<const float *>(base + L.tau), nullptr, F_host, budget,
+                             reinterpret_cast<int32_t *>(base + L.acc), reinterpret_cast<int32_t *>(base + L.bon),
+                             nullptr, nullptr, reinterpret_cast<int32_t *>(base + L.cache),
+                             reinterpret_cast<uint8_t *>(base + L.hit), reinterpret_cast<int32_t *>(base + L.slot),
+                             workspace, workspace_bytes, dev_status, stream);
+    if (rc != SSD_OK) return rc;
+    d2h(accept_len, L.acc, static_cast<size_t>(B) * 4);
+    d2h(bonus, L.bon, static_cast<size_t>(B) * 4);
+    d2h(cache_tok, L.cache, static_cast<size_t>(B) * budget * 4);
+    d2h(hit, L.hit, static_cast<size_t>(B));
+    d2h(slot, L.slot, static_cast<size_t>(B) * 4);
+    if (!ok) {
+        cudaGetLastError();
+        return SSD_ERR_CUDA;
+    }
+    if (h2d_bytes) *h2d_bytes = moved;
+    return SSD_OK;
+}
+
+}  // extern "C"

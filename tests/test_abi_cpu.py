@@ -114,6 +114,21 @@ def _fake(addr=0x10000):
     return ctypes.c_void_p(addr)
 
 
+def test_host_staging_size(ssd):
+    bf, f32 = ssd.SSD_BF16, ssd.SSD_F32
+    assert ssd.ssd_host_staging_size(bf, 0, 4, 100, 8) == 0
+    assert ssd.ssd_host_staging_size(bf, 4, 0, 100, 8) == 0
+    assert ssd.ssd_host_staging_size(bf, 4, 33, 100, 8) == 0
+    assert ssd.ssd_host_staging_size(bf, 4, 2, 1, 8) == 0
+    assert ssd.ssd_host_staging_size(bf, 4, 2, 100, -1) == 0
+    assert ssd.ssd_host_staging_size(9, 4, 2, 100, 8) == 0
+    for dt, s in ((bf, 2), (f32, 4)):
+        B, K, V, budget = 256, 4, 128256, 32
+        raw = B * (2 * K + 1) * V * s + B * K * 4 + B * (K + 1) * 4 + 4 * B * 4 + B * budget * 4 + B
+        n = ssd.ssd_host_staging_size(dt, B, K, V, budget)
+        assert raw <= n < raw + 10 * 256 and n % 256 == 0
+
+
 def test_device_calls_validate_before_any_cuda_call(ssd):
     L = ssd.lib()
     p = _fake()
@@ -173,6 +188,20 @@ def test_device_calls_validate_before_any_cuda_call(ssd):
     Fv = np.array([2, 101, 3], np.int32).ctypes.data_as(ctypes.c_void_p)
     assert dc(p, 0, 4, 2, 100, p, Fv, 106, c(1), p, None, None, None) == \
         ssd.SSD_ERR_INVALID_ARG  # F_k > V
+    need = ssd.ssd_host_staging_size(0, 4, 2, 100, 6)
+
+    def rhost(dtype=0, B=4, K=2, V=100, F=Fp, budget=6, tgt=p, staging=p, staging_bytes=need):
+        return L.ssd_round_host(tgt, p, dtype, B, K, V, p, p, p, F, budget, p, p, p, p, p, staging,
+                                staging_bytes, p, ws_ok, None, None, None)
+
+    assert rhost(dtype=5) == ssd.SSD_ERR_DTYPE
+    assert rhost(B=0) == ssd.SSD_ERR_INVALID_ARG
+    assert rhost(tgt=None) == ssd.SSD_ERR_INVALID_ARG
+    assert rhost(staging=None) == ssd.SSD_ERR_INVALID_ARG
+    assert rhost(F=None) == ssd.SSD_ERR_INVALID_ARG
+    assert rhost(budget=5) == ssd.SSD_ERR_INVALID_ARG  # budget < sum F
+    assert rhost(F=Fneg.ctypes.data_as(ctypes.c_void_p), budget=10) == ssd.SSD_ERR_INVALID_ARG
+    assert rhost(staging_bytes=need - 1) == ssd.SSD_ERR_INVALID_ARG
     assert L.ssd_check_wait_timeout(None, 20, None) == ssd.SSD_ERR_INVALID_ARG
     assert L.ssd_check_wait_timeout(p, 0, None) == ssd.SSD_ERR_INVALID_ARG
     assert L.ssd_check_wait_timeout(p, 10001, None) == ssd.SSD_ERR_INVALID_ARG
