@@ -559,6 +559,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     const int vtail = kTail ? V % VEC : 0;
     const int64_t row_bytes = static_cast<int64_t>(nvec_row) * 16;
 
+    // the next launch on the stream may be scheduled now (it waits below for this one)
+    asm volatile("griddepcontrol.launch_dependents;");
     if (tid == 0) {
         for (int g = 0; g < kNG; ++g) {
             for (int i = 0; i < kRS; ++i) {
@@ -624,6 +626,11 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         }
     }
     __syncthreads();
+    // Launched right behind another round (programmatic dependent launch), this
+    // grid may get here while that round's last blocks still drain: the lines
+    // above read only inputs, and the workspace, which the previous round's
+    // last block resets, is touched only once that grid has completed.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     // =========================== producers ==================================
     if (warp >= kProducerWarp0 && warp < kTailWarp0) {
@@ -1606,7 +1613,12 @@ int stream_launch(int dtype, const UnitParams &P, int grid, size_t dyn, void *st
     cfg.blockDim = dim3(kStreamThreads, 1, 1);
     cfg.dynamicSmemBytes = dyn;
     cfg.stream = static_cast<cudaStream_t>(stream);
-    cfg.numAttrs = 0;
+    // may start while the previous kernel on the stream drains (see griddepcontrol.wait)
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     const cudaError_t e = dtype == SSD_F32 ? stream_launch_d<F32Tag>(cfg, P) : stream_launch_d<BF16Tag>(cfg, P);
     if (e != cudaSuccess) {
         cudaGetLastError();
