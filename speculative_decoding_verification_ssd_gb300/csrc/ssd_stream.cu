@@ -14,17 +14,27 @@
 //                     c = log2 e / tau); single rows also store per 64-token
 //                     group the raw maximum (greedy rows: drafted token
 //                     excluded) and, when sampled, the mass 2^(z c - gmax c);
-//       between       a pair unit (sampled, k < K) reduces its two statistics
-//                     to the normalisers L_T, L_D and takes the accept test
-//                     ([SD] step 3);
+//                     A pair unit that builds a cache also keeps the raw
+//                     64-token group maxima of both rows;
+//       between       a pair unit reduces its two statistics to the
+//                     normalisers L_T, L_D and takes the accept test ([SD]
+//                     step 3).  Only a rejected position's residual can be
+//                     sampled; at an accepted one the residual serves the
+//                     cache top-F_k alone, and a group can hold one of those
+//                     only if its upper bound p(max z_p) reaches the F-th
+//                     largest lower bound p(max z_p) - q(max z_q) (found with
+//                     barrier counts over the threads' largest bounds);
 //       pass 2 (L2)   the pair's rows stream again, from the row's end back to
 //                     its start (just read, so mostly L2 hits): per group the
-//                     residual mass sum max(0, p - q) and the largest residual;
+//                     residual mass sum max(0, p - q) and the largest residual,
+//                     at an accepted position for those groups only (the rest
+//                     read as 0);
 //     then hands the unit's group arrays (double-buffered) to
 //   * tail warp g, which, without block barriers: selects the cache top-F_k
 //     (groups whose maximum reaches the F-th largest of the lanes' two
 //     largest group maxima are re-read and ranked as (value, id) keys, with
-//     a bisection over the maxima for F_k above 64), draws the bonus t_k at u_K by
+//     a bisection over the maxima for F_k above 64), draws the bonus t_k (at a
+//     rejected position, or from p_K) at u_K by
 //     inverse CDF over ascending token id (group prefix, then the crossing
 //     group re-read), takes the greedy argmax, publishes the unit's record,
 //     counts the sequence's finished units and, for the last one, runs the
@@ -107,6 +117,7 @@ struct TailDesc {
     float LT, LD;  // pair: normalisers (base 2)
     float p_tok, q_tok;
     float ztx;  // target logit of the drafted token (k < K)
+    float tlo;  // pair: a score at least F_k tokens reach (-inf when none is known)
     DraftShape shape;
 };
 
@@ -865,6 +876,10 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                     }
                     th = lo;
                 }
+                // a pair whose second pass covered only the groups that can hold its
+                // top-F (the rest read as 0) brings a score at least F tokens reach:
+                // the threshold is at least that, so those zeros never become candidates
+                if (d.tlo > 0.f) th = max(th, ordered_bits_nz(d.tlo));
                 // candidate groups (maximum reaches th): per-lane bit masks (bit 4i + j:
                 // group 128 i + 4 lane + j), then a warp prefix places each lane's groups
                 uint32_t cm[kMaskWords];
@@ -1095,11 +1110,13 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             };
 
             if (d.kind == kKindPair) {
-                float zs = 0.f;
-                for (int g = g0; g < g1; ++g) zs += gsum[g];
-                const float Z = warp_sum(zs);
                 if (Fk > 0) top_f(true);
-                if (do_verify) {
+                // the bonus at k is drawn only where k rejected (the second pass left
+                // every residual mass only there)
+                if (do_verify && !d.accept) {
+                    float zs = 0.f;
+                    for (int g = g0; g < g1; ++g) zs += gsum[g];
+                    const float Z = warp_sum(zs);
                     if (Z > 0.f) {
                         crossing(false, 0.f);
                     } else {
@@ -1278,6 +1295,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     int cur = -1;
     int b = 0, k = 0, flags = 0, xt = -1, xmask = -1;
     bool sampled = false, pair = false, active = false, want_p2 = false, sig = false;
+    bool bnd = false;      // a pair that builds a cache: pass 1 keeps both rows' group maxima
+    float cthr = -INFINITY;  // pass 2: residuals of the groups whose upper bound reaches this only
     float c = 0.f, LT = 0.f, LD = 0.f;
     DraftShape shape{0, 0.f, 0, 0.f};
     Stat st{-INFINITY, 0.f};
@@ -1313,6 +1332,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             D0.q_tok = q_tok;
             D0.ztx = ztx;
             D0.shape = shape;
+            D0.tlo = (hk == kKindPair && cthr > 0.f && cthr < INFINITY) ? cthr : -INFINITY;
             mbar_arrive(&gs.tail_full[nho % kNBuf]);
         }
         ++nho;
@@ -1354,6 +1374,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             xmask = (greedy && k < K) ? xt : -1;
             active = flags == 0;
             want_p2 = pair && (do_verify || (do_cache && P.F[k] > 0));
+            bnd = pair && do_cache && P.F[k] > 0;
+            cthr = -INFINITY;
             c = sampled ? kLog2e / tau : 0.f;
             shape = DraftShape{0, 0.f, 0, 0.f};
             sig = kSig && pair && P.sig_F[k] > 0;
@@ -1371,7 +1393,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             q_tok = NAN;
             accept = 0;
             ztx = 0.f;
-            if (t == 0 && active && k < K) {
+            if (active && k < K) {
                 const unsigned char *trow = static_cast<const unsigned char *>(P.tgt) +
                                             (static_cast<int64_t>(b) * P.tgt_seq_stride + static_cast<int64_t>(k) * P.ld) * S;
                 ztx = load_logit<D>(trow, xt);
@@ -1403,16 +1425,17 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                 load_vecs<D, VPT1>(stg + p1_row * HALF, p1_vbase, h.nvec, p1_rot, h.nvec == FULL_PAIR && !part, w);
                 if (part) mask_partial<D, VPT1>(w, p1_vbase, p1_rot, pv, vtail);
                 const float rm = vecs_max<D, VPT1>(w);
+                if (sig || bnd) {
+                    // raw 64-token group maxima: the draft's to gmax (the fused sigma's
+                    // candidates, the bound on q), the target's to gsum (the bound on p)
+                    const float gm = tpg_max<TPG1>(rm);
+                    const int g = h.chunk * GPR + p1_tr / TPG1;
+                    if (p1_tr % TPG1 == 0 && g < G) (p1_row ? gmax : gsum)[g] = canon_zero(gm);
+                }
                 // a reshaped draft row takes the plain path where none of the thread's
                 // tokens reaches the top-F threshold (all but a few threads of the row)
                 if (p1_row == 0 || !shape.on || !(rm >= shape.thr)) {
                     stat_fold(st, rm * c, [&](float mn) { return vecs_expsum<D, VPT1>(w, c, mn); });
-                    if (sig && p1_row == 1) {
-                        // raw 64-token group maxima of the draft row for the fused sigma
-                        const float gm = tpg_max<TPG1>(rm);
-                        const int g = h.chunk * GPR + p1_tr / TPG1;
-                        if (p1_tr % TPG1 == 0 && g < G) gmax[g] = canon_zero(gm);
-                    }
                 } else {
                     st = reshaped_fold<D, VPT1>(st, stg + HALF, p1_vbase, h.nvec, p1_rot, h.nvec == FULL_PAIR && !part,
                                                 c, shape, h.chunk * (FULL_PAIR * VEC) + p1_vbase * VEC, pv, vtail);
@@ -1453,15 +1476,23 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                 const bool full = h.nvec == FULL_PAIR && !part;
                 float2 acc = make_float2(0.f, 0.f);
                 float mx = 0.f;
+                const int g = h.chunk * GPR + r_gl;
+                // at an accepted position only the groups whose bound reaches cthr
+                const bool cand =
+                    cthr == -INFINITY ||
+                    (cthr < INFINITY && g < G && ex2(fmaf(gsum[g], c, -LT)) * (1.f + 0x1p-20f) >= cthr);
                 uint4 wt[VPT2], wd[VPT2];
-                load_vecs<D, VPT2>(stg, r_vbase, h.nvec, r_rot, full, wt);
-                load_vecs<D, VPT2>(stg + HALF, r_vbase, h.nvec, r_rot, full, wd);
-                if (part) {
-                    mask_partial<D, VPT2>(wt, r_vbase, r_rot, pv, vtail);
-                    mask_partial<D, VPT2>(wd, r_vbase, r_rot, pv, vtail);
+                if (cand) {
+                    load_vecs<D, VPT2>(stg, r_vbase, h.nvec, r_rot, full, wt);
+                    load_vecs<D, VPT2>(stg + HALF, r_vbase, h.nvec, r_rot, full, wd);
+                    if (part) {
+                        mask_partial<D, VPT2>(wt, r_vbase, r_rot, pv, vtail);
+                        mask_partial<D, VPT2>(wd, r_vbase, r_rot, pv, vtail);
+                    }
                 }
                 // reshaped draft: only tokens at or above the top-F threshold carry a bias
-                if (!shape.on || !(vecs_max<D, VPT2>(wd) >= shape.thr)) {
+                if (!cand) {
+                } else if (!shape.on || !(vecs_max<D, VPT2>(wd) >= shape.thr)) {
                     const float2 cc = make_float2(c, c), nl = make_float2(-LT, -LD);
 #pragma unroll
                     for (int kk = 0; kk < VPT2; ++kk) {
@@ -1488,7 +1519,6 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                 }
                 const float gsv = tpg_sum<TPG2>(acc.x + acc.y);
                 const float gmx = tpg_max<TPG2>(mx);
-                const int g = h.chunk * GPR + r_gl;
                 if (r_part == 0 && g < G) {
                     gmax[g] = gmx;
                     gsum[g] = gsv;
@@ -1536,11 +1566,38 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                 qS = sr.qS;
             }
             LD = qm + lg2(qS);
+            // the same operations for both, so identical rows give identical p and q
+            // (every thread: the accept bit decides the second pass's extent)
+            p_tok = ex2(fmaf(ztx, c, -gT.m)) / gT.S;
+            q_tok = ex2(fmaf(zdx, c, draft_bias(shape, zdx, xt) - qm)) / qS;
+            accept = (u_k * q_tok < p_tok) ? 1 : 0;
+            if (!(do_verify && !accept)) {
+                // the residual is not sampled here: it ranks the cache top-F alone (or
+                // nothing).  For t* the target maximum of group g, r(t*) >= p(max z_p) -
+                // q(max z_q), and no token of g exceeds p(max z_p) (a reshaped draft only
+                // lowers q); both widened by 2^-20 relative against ex2's rounding.  The
+                // threads' largest lower bounds (groups t, t + kGT, ...) give, bit by bit
+                // over their upper 16 ordered bits, a value that at least F tokens reach.
+                cthr = INFINITY;
+                if (bnd) {
+                    const int F = P.F[k];
+                    float lbm = -INFINITY;
+                    for (int gg = t; gg < G; gg += kGT) {
+                        const float ub = ex2(fmaf(gsum[gg], c, -LT));
+                        const float qb = ex2(fmaf(gmax[gg], c, -LD));
+                        lbm = fmaxf(lbm, fmaf(-qb, 1.f + 0x1p-20f, ub));
+                    }
+                    const uint32_t ob = ordered_bits_nz(lbm);
+                    uint32_t T = 0;
+                    for (int bit = 31; bit >= 16; --bit) {
+                        const uint32_t cand = T | (1u << bit);
+                        if (group_count(bar_id, kGT, ob >= cand) >= F) T = cand;
+                    }
+                    const float tv = value_of_ordered(T);
+                    cthr = tv > 0.f ? tv : -INFINITY;  // no positive bound: every group
+                }
+            }
             if (t == 0) {
-                // the same operations for both, so identical rows give identical p and q
-                p_tok = ex2(fmaf(ztx, c, -gT.m)) / gT.S;
-                q_tok = ex2(fmaf(zdx, c, draft_bias(shape, zdx, xt) - qm)) / qS;
-                accept = (u_k * q_tok < p_tok) ? 1 : 0;
                 if (kSig && P.desc_out) {
                     ssd_reshape_desc dd;
                     dd.F = sig ? P.sig_F[k] : 0;

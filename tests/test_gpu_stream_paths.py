@@ -3,6 +3,10 @@ compared with the float64 oracle:
 
 * a draft row equal to its target row, rejected at a token both give
   probability 0: no residual mass, so the bonus is drawn from p;
+* accepted positions, whose second pass computes residuals only for the groups
+  that can hold the cache top-F (bounded from the first pass's group maxima),
+  with those groups clustered at the lowest ids (a few tail lanes) or with no
+  residual at all (draft equal to target: every group is computed);
 * a fan-out with F_k above 64, where the top-F threshold is found by bisection
   over the group maxima instead of from the lanes' two largest maxima;
 * rows whose logits are all equal, where every group reaches the threshold
@@ -142,3 +146,24 @@ def test_signed_zeros_tie(ssd, dtype):
     tok[:, 1] = 5001               # not the argmax (101): rejected, greedy bonus 101
     u = rng.random((B, K + 1))
     _round_and_compare(ssd, _pack(zt, zd, tok, u, [0.0, 1.0, 0.0, 0.5], dtype), 12, 0.7, 0.5)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("same", [False, True])
+def test_accepted_pairs_bound_the_groups_they_compute(ssd, dtype, same):
+    """u = 0 accepts every drafted token with p > 0, so each pair's residual only ranks
+    its cache top-F: the second pass computes the groups whose bound p(max z_p) reaches
+    the F-th largest lower bound p(max z_p) - q(max z_q).  The large logits sit in
+    groups 0-7 (the first two tail lanes), or the draft equals the target (no positive
+    bound: every group is computed)."""
+    rng = np.random.default_rng(35)
+    B, K, V = 6, 3, 24000
+    zd = (rng.standard_normal((B, K + 1, V)) * 2.5).astype(np.float32)
+    zd[:, :, :512] += 6.0
+    zt = zd if same else (zd + rng.standard_normal((B, K + 1, V)) * 0.8).astype(np.float32)
+    tok = rng.integers(0, 512, (B, K))
+    u = rng.random((B, K + 1))
+    u[:, :K] = 0.0
+    inp = _pack(zt, zd[:, :K].copy(), tok, u, [1.0] * B, dtype)
+    g, o, F = _round_and_compare(ssd, inp, 28, 0.75, 0.5)
+    assert (g["accept_len"] == K).all()
