@@ -70,6 +70,7 @@ constexpr int kTailWarp0 = kProducerWarp0 + kNG;
 constexpr unsigned kFull = 0xFFFFFFFFu;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kCandGroupsCap = 512;
+constexpr int kDecWords = 4;  // chunk bitmap of a second pass (128 chunks)
 constexpr int kSchedCap = 2048;  // largest batch ordered by unit kind
 static_assert(kStreamSigKeys == kCandCap && kGT == kThreads, "fused sigma selection geometry");
 
@@ -126,6 +127,8 @@ struct GroupShared {
     uint64_t empty_bar[kRS];
     uint64_t tail_full[kNBuf];
     uint64_t tail_empty[kNBuf];
+    uint64_t dec_bar;         // consumer thread 0 -> producer: the chunks a second pass needs
+    uint32_t dec_mask[kDecWords];
     Hdr hdr[kRS];
     TailDesc desc[kNBuf];
     Stat red[kGW];
@@ -542,6 +545,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     constexpr int VPT1 = FULL_PAIR / (kGT / 2), VPTS = GV / TPGS, VPT2 = GV / TPG2;
     constexpr int TPG1 = GV / VPT1;        // pass 1 of a pair: threads per group of one row
     static_assert(VPT1 == 4 && VPTS == 4 && VPT2 == 2, "stage geometry");
+    static_assert((kStreamMaxGroups + GPR - 1) / GPR <= kDecWords * 32, "second-pass chunk list");
     constexpr int LPG = GV < 32 ? GV : 32;  // tail: lanes per group re-read (one vector each)
     constexpr int GPI = 32 / LPG;           // tail: groups per warp iteration
     constexpr int VPL = GV / LPG;           // tail: vectors per lane per group
@@ -582,6 +586,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                 mbar_init(&gsh[g].tail_full[i], 1);
                 mbar_init(&gsh[g].tail_empty[i], 1);
             }
+            mbar_init(&gsh[g].dec_bar, 1);
         }
         s_abort = 0;
         s_nS = 0;
@@ -708,7 +713,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                 pf_state = 2;
             }
         };
-        uint32_t n = 0;  // stages pushed
+        uint32_t n = 0;     // stages pushed
+        uint32_t ndec = 0;  // second-pass chunk lists received
         bool ok = true;
         for (;;) {
             while (pf_state < 2) pf_step();
@@ -740,7 +746,36 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             const int cb = pair ? HALF : kSB;
             const int nch = static_cast<int>((row_bytes + cb - 1) / cb);
             const int total = skip ? 1 : nch * (p2 ? 2 : 1);
+            // A second pass longer than the ring streams its first kRS stages unasked;
+            // the rest follows the consumers' chunk list, which they publish once the
+            // accept test and the top-F bound are known (before those stages are used).
+            const bool gated = p2 && !skip && nch > kRS;
+            int lowest = 0;  // gated: the smallest listed chunk (streamed last), -1 for none
             for (int i = 0; i < total; ++i) {
+                bool empty_end = false, listed_last = false;
+                if (gated && i >= nch + kRS) {
+                    if (i == nch + kRS) {
+                        if (!mbar_wait_suspend(&gq.dec_bar, ndec & 1)) {
+                            ok = false;
+                            break;
+                        }
+                        ++ndec;
+                        lowest = -1;
+                        for (int c = 0; c < nch - kRS && lowest < 0; ++c)
+                            if ((reinterpret_cast<volatile uint32_t *>(gq.dec_mask)[c >> 5] >> (c & 31)) & 1u)
+                                lowest = c;
+                    }
+                    const int chunk = nch - 1 - (i - nch);
+                    if (lowest < 0) {
+                        empty_end = true;  // nothing listed: a header-only stage ends the pass
+                        i = total - 1;
+                    } else if (!((reinterpret_cast<volatile uint32_t *>(gq.dec_mask)[chunk >> 5] >> (chunk & 31)) & 1u)) {
+                        if (total - i <= 3) pf_step();
+                        continue;
+                    } else {
+                        listed_last = chunk == lowest;
+                    }
+                }
                 const int s = static_cast<int>(n % kRS);
                 if (!mbar_wait_suspend(&gq.empty_bar[s], ((n / kRS) & 1) ^ 1)) {
                     ok = false;
@@ -749,6 +784,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                 if (skip) {
                     gq.hdr[s] = Hdr{u, kPassSkip | (1 << 4), 0, 0, b, k, 0, 0};
                     mbar_arrive_expect_tx(&gq.full_bar[s], 0);
+                } else if (empty_end) {
+                    gq.hdr[s] = Hdr{u, kPassResid | (1 << 4) | (1 << 5), -1, 0, b, k, 0, 0};
+                    mbar_arrive_expect_tx(&gq.full_bar[s], 0);
                 } else {
                     const bool second = i >= nch;
                     // the second pass runs from the row's end back to its start: the
@@ -756,7 +794,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                     const int chunk = second ? nch - 1 - (i - nch) : i;
                     const int64_t off = static_cast<int64_t>(chunk) * cb;
                     const uint32_t bytes = static_cast<uint32_t>(row_bytes - off < cb ? row_bytes - off : cb);
-                    const bool last = second ? chunk == 0 : chunk == nch - 1;
+                    const bool last = second ? (gated && i >= nch + kRS ? listed_last : chunk == 0)
+                                             : chunk == nch - 1;
                     const int code = (second ? kPassResid : kPassStats) | ((last ? 1 : 0) << 4) |
                                      ((pair ? 1 : 0) << 5);
                     gq.hdr[s] = Hdr{u, code, chunk, static_cast<int>(bytes / 16), b, k, 0, 0};
@@ -1297,6 +1336,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     bool sampled = false, pair = false, active = false, want_p2 = false, sig = false;
     bool bnd = false;      // a pair that builds a cache: pass 1 keeps both rows' group maxima
     float cthr = -INFINITY;  // pass 2: residuals of the groups whose upper bound reaches this only
+    const int nch_pair = static_cast<int>((row_bytes + HALF - 1) / HALF);  // chunks of a pair pass
     float c = 0.f, LT = 0.f, LD = 0.f;
     DraftShape shape{0, 0.f, 0, 0.f};
     Stat st{-INFINITY, 0.f};
@@ -1471,7 +1511,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                 } else if (s_part == 0 && g < G) {
                     gmax[g] = canon_zero(gm);
                 }
-            } else {
+            } else if (h.nvec > 0) {  // (a header-only stage just ends a shortened pass)
                 // pass 2 (pair): residual masses and maxima per group
                 const bool full = h.nvec == FULL_PAIR && !part;
                 float2 acc = make_float2(0.f, 0.f);
@@ -1531,8 +1571,26 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         if (!((h.code >> 4) & 1)) continue;
 
         // ---- end of a pass ------------------------------------------------------
+        // A second pass longer than the ring continues after its first kRS stages
+        // only with the chunks thread 0 lists here (dec_mask, then dec_bar).
+        const bool gated = pass == kPassStats && want_p2 && nch_pair > kRS;
+        auto list_chunks = [&](uint32_t all) {
+            if (gated && t == 0) {
+                if (all != 0u)
+#pragma unroll
+                    for (int w = 0; w < kDecWords; ++w) gs.dec_mask[w] = all;
+                mbar_arrive(&gs.dec_bar);
+            }
+        };
         if (!active) {
-            // an inactive pair still receives its second pass; hand off after it
+            // an inactive pair still receives (the unasked part of) its second pass;
+            // hand off after it
+            if (pass == kPassStats && pair) {
+                if (gated && t == 0)
+#pragma unroll
+                    for (int w = 0; w < kDecWords; ++w) gs.dec_mask[w] = 0u;
+                list_chunks(0u);
+            }
             if (pass == kPassResid || !want_p2) handoff(kKindPass, 1, 0.f, 0.f);
             continue;
         }
@@ -1551,6 +1609,10 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             if (!stat_ok(gT) || !stat_ok(gD)) {
                 flags |= SSD_DEV_NONFINITE;
                 active = false;
+                if (gated && t == 0)
+#pragma unroll
+                    for (int w = 0; w < kDecWords; ++w) gs.dec_mask[w] = 0u;
+                list_chunks(0u);
                 if (!want_p2) handoff(kKindPass, 1, 0.f, 0.f);
                 continue;
             }
@@ -1595,6 +1657,28 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                     }
                     const float tv = value_of_ordered(T);
                     cthr = tv > 0.f ? tv : -INFINITY;  // no positive bound: every group
+                }
+            }
+            if (gated) {
+                if (cthr == -INFINITY) {
+                    list_chunks(0xFFFFFFFFu);  // every chunk
+                } else {
+                    // the chunks holding a group whose bound reaches cthr; every other
+                    // group's largest residual reads as 0 (its chunk may not be streamed)
+                    if (t == 0)
+#pragma unroll
+                        for (int w = 0; w < kDecWords; ++w) gs.dec_mask[w] = 0u;
+                    gbar();
+                    for (int gg = t; gg < G; gg += kGT) {
+                        const bool cg = cthr < INFINITY &&
+                                        ex2(fmaf(gsum[gg], c, -LT)) * (1.f + 0x1p-20f) >= cthr;
+                        if (cg)
+                            atomicOr(&gs.dec_mask[(gg / GPR) >> 5], 1u << ((gg / GPR) & 31));
+                        else
+                            gmax[gg] = 0.f;
+                    }
+                    gbar();
+                    list_chunks(0u);
                 }
             }
             if (t == 0) {
