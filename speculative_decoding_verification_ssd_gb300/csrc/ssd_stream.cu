@@ -801,13 +801,10 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                     gq.hdr[s] = Hdr{u, code, chunk, static_cast<int>(bytes / 16), b, k, 0, 0};
                     unsigned char *dst = ring + s * kSB;
                     mbar_arrive_expect_tx(&gq.full_bar[s], bytes * (pair ? 2u : 1u));
-                    if (!pair || second) {  // not read again
-                        bulk_copy_hint(dst, trow + off, bytes, &gq.full_bar[s], pol);
-                        if (pair) bulk_copy_hint(dst + HALF, drow + off, bytes, &gq.full_bar[s], pol);
-                    } else {
-                        bulk_copy_g2s(dst, trow + off, bytes, &gq.full_bar[s]);
-                        bulk_copy_g2s(dst + HALF, drow + off, bytes, &gq.full_bar[s]);
-                    }
+                    // evict_first throughout: most second passes are cut to a few chunks,
+                    // so holding first-pass rows in L2 for them costs more than it saves
+                    bulk_copy_hint(dst, trow + off, bytes, &gq.full_bar[s], pol);
+                    if (pair) bulk_copy_hint(dst + HALF, drow + off, bytes, &gq.full_bar[s], pol);
                 }
                 ++n;
                 if (total - i <= 3) pf_step();
