@@ -24,11 +24,13 @@
 //                     only if its upper bound p(max z_p) reaches the F-th
 //                     largest lower bound p(max z_p) - q(max z_q) (found with
 //                     barrier counts over the threads' largest bounds);
-//       pass 2 (L2)   the pair's rows stream again, from the row's end back to
-//                     its start (just read, so mostly L2 hits): per group the
-//                     residual mass sum max(0, p - q) and the largest residual,
-//                     at an accepted position for those groups only (the rest
-//                     read as 0);
+//       pass 2        the pair's rows stream again, from the row's end back to
+//                     its start (the chunks read last are still in L2): per
+//                     group the residual mass sum max(0, p - q) and the largest
+//                     residual, at an accepted position for those groups only
+//                     (the rest read as 0).  The producer streams the first
+//                     kRS stages of the pass unasked and the rest only for the
+//                     chunks the consumers list after the accept test;
 //     then hands the unit's group arrays (double-buffered) to
 //   * tail warp g, which, without block barriers: selects the cache top-F_k
 //     (groups whose maximum reaches the F-th largest of the lanes' two
