@@ -400,7 +400,7 @@ template <class D>
 __device__ __noinline__ SigResult sigma_fuse(const unsigned char *drow, const float *gmax, int G, int V,
                                              int F, float C, float c, Stat gD, uint64_t *keys, int *cnt,
                                              float *red, int t, int bar_id) {
-    constexpr int VEC = D::kVec, S = D::kBytes;
+    constexpr int VEC = D::kVec;
     const auto bar = [bar_id]() { asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "r"(kGT) : "memory"); };
     const int lane = t & 31, w = t >> 5;
     float bm = -INFINITY;
