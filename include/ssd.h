@@ -351,9 +351,14 @@ int ssd_round_noalloc(const void *tgt, const void *drf, int dtype, int B, int K,
 /*
  * ssd_round_host -- ssd_round on inputs and outputs in host memory (no
  * counterpart on the pages: the transfer plumbing around [SSD] "整体框架").
- * Enqueues on `stream`: the copies of the inputs into `staging`, the round
- * (ssd_round with drf_rows = K, no reshape, no p/q outputs) and the copies of
- * its results back.  A sequence that does not sample (tau == 0 decides by the
+ * Enqueues the copies of the inputs into `staging`, the round (ssd_round with
+ * drf_rows = K, no reshape, no p/q outputs) and the copies of its results back.
+ * A batch of B >= 128 runs in min(4, B / 64) chunks of consecutive sequences:
+ * the input copies go on a copy stream the library keeps per device (made to
+ * wait for the work already on `stream`), and each chunk's round and result
+ * copies go on `stream` once that chunk's inputs have landed, so a round runs
+ * while the next chunk is copied.  Everything is ordered before the work
+ * enqueued on `stream` afterwards.  A sequence that does not sample (tau == 0 decides by the
  * target argmax, [WHY] Fix 2; an invalid tau is reported) never has its draft
  * logits read, so only the sampled sequences' draft rows are copied, each run
  * of consecutive sampled sequences as one copy: the host-to-device traffic is

@@ -604,6 +604,28 @@ bool host_staging_args_ok(int dtype, int B, int K, int V, int budget) {
            (dtype == SSD_F32 || dtype == SSD_BF16);
 }
 
+// One stream per device for the host-to-device copies of ssd_round_host, so that a
+// chunk's round overlaps the copies of the next chunk (created on first use, kept
+// until the process exits).
+std::mutex g_copy_mu;
+cudaStream_t g_copy_stream[kMaxDevices] = {};
+
+int copy_stream(cudaStream_t *out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SSD_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_copy_mu);
+    if (!g_copy_stream[dev]) {
+        cudaStream_t s = nullptr;
+        if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) {
+            cudaGetLastError();
+            return SSD_ERR_CUDA;
+        }
+        g_copy_stream[dev] = s;
+    }
+    *out = g_copy_stream[dev];
+    return SSD_OK;
+}
+
 // The fan-out checks of the round, taken before any copy is enqueued.
 bool host_fanout_ok(const int32_t *F_host, int K, int V, int budget) {
     int64_t sum = 0;
@@ -638,57 +660,100 @@ int ssd_round_host(const void *tgt, const void *drf, int dtype, int B, int K, in
     const HostStaging L = host_staging_layout(dtype, B, K, V, budget);
     if (staging_bytes < L.total) return SSD_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaStream_t cs = nullptr;  // the copies run here, each chunk's round on `stream`
+    const int cst = copy_stream(&cs);
+    if (cst != SSD_OK) return cst;
+    // Consecutive sequences in up to 4 chunks of at least 64: the round on chunk c
+    // runs while the next chunk is copied (sequences are independent).
+    const int nchunk = std::max(1, std::min(4, B / 64));
+    cudaEvent_t ev[5] = {};
+    for (int i = 0; i <= nchunk; ++i) {
+        if (cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) != cudaSuccess) {
+            cudaGetLastError();
+            for (int j = 0; j < i; ++j) cudaEventDestroy(ev[j]);
+            return SSD_ERR_CUDA;
+        }
+    }
+    const auto release = [&]() {
+        for (int i = 0; i <= nchunk; ++i) cudaEventDestroy(ev[i]);  // freed once complete
+    };
     unsigned char *base = static_cast<unsigned char *>(staging);
     size_t moved = 0;
     bool ok = true;
     const auto h2d = [&](size_t off, const void *src, size_t n) {
         if (!ok || n == 0) return;
         moved += n;
-        ok = cudaMemcpyAsync(base + off, src, n, cudaMemcpyHostToDevice, st) == cudaSuccess;
+        ok = cudaMemcpyAsync(base + off, src, n, cudaMemcpyHostToDevice, cs) == cudaSuccess;
     };
     const auto d2h = [&](void *dst, size_t off, size_t n) {
         if (!ok || n == 0) return;
         ok = cudaMemcpyAsync(dst, base + off, n, cudaMemcpyDeviceToHost, st) == cudaSuccess;
     };
     const size_t row = static_cast<size_t>(V) * (dtype == SSD_F32 ? 4 : 2);
+    const size_t seq_t = static_cast<size_t>(K + 1) * row;
     const size_t seq_d = static_cast<size_t>(K) * row;
-    h2d(L.tgt, tgt, static_cast<size_t>(B) * (K + 1) * row);
-    // Draft rows of the sampled sequences only (a run of consecutive ones in one
-    // copy): a greedy or invalid sequence's draft logits are never read.
-    for (int b = 0; b < B;) {
-        const auto sampled = [&](int i) { return temperature[i] > 0.f && temperature[i] < INFINITY; };
-        if (!sampled(b)) {
-            ++b;
-            continue;
-        }
-        int e = b + 1;
-        while (e < B && sampled(e)) ++e;
-        h2d(L.drf + static_cast<size_t>(b) * seq_d,
-            static_cast<const unsigned char *>(drf) + static_cast<size_t>(b) * seq_d,
-            static_cast<size_t>(e - b) * seq_d);
-        b = e;
-    }
+    // the copies start after the work already on `stream` (an earlier round reading staging)
+    ok = cudaEventRecord(ev[0], st) == cudaSuccess && cudaStreamWaitEvent(cs, ev[0], 0) == cudaSuccess;
     h2d(L.tok, tokens, static_cast<size_t>(B) * K * 4);
     h2d(L.uni, uniforms, static_cast<size_t>(B) * (K + 1) * 4);
     h2d(L.tau, temperature, static_cast<size_t>(B) * 4);
+    const auto sampled = [&](int i) { return temperature[i] > 0.f && temperature[i] < INFINITY; };
+    for (int c = 0; c < nchunk; ++c) {
+        const int c0 = static_cast<int>(static_cast<int64_t>(B) * c / nchunk);
+        const int c1 = static_cast<int>(static_cast<int64_t>(B) * (c + 1) / nchunk);
+        h2d(L.tgt + c0 * seq_t, static_cast<const unsigned char *>(tgt) + c0 * seq_t,
+            static_cast<size_t>(c1 - c0) * seq_t);
+        // Draft rows of the sampled sequences only (a run of consecutive ones in one
+        // copy): a greedy or invalid sequence's draft logits are never read.
+        for (int b = c0; b < c1;) {
+            if (!sampled(b)) {
+                ++b;
+                continue;
+            }
+            int e = b + 1;
+            while (e < c1 && sampled(e)) ++e;
+            h2d(L.drf + static_cast<size_t>(b) * seq_d,
+                static_cast<const unsigned char *>(drf) + static_cast<size_t>(b) * seq_d,
+                static_cast<size_t>(e - b) * seq_d);
+            b = e;
+        }
+        if (ok) ok = cudaEventRecord(ev[c + 1], cs) == cudaSuccess;
+    }
     if (!ok) {
         cudaGetLastError();
+        release();
         return SSD_ERR_CUDA;
     }
-    const int rc = ssd_round(base + L.tgt, base + L.drf, dtype, B, K, V, K,
-                             reinterpret_cast<const int32_t *>(base + L.tok),
-                             reinterpret_cast<const float *>(base + L.uni),
-                             reinterpret_cast<const float *>(base + L.tau), nullptr, F_host, budget,
-                             reinterpret_cast<int32_t *>(base + L.acc), reinterpret_cast<int32_t *>(base + L.bon),
-                             nullptr, nullptr, reinterpret_cast<int32_t *>(base + L.cache),
-                             reinterpret_cast<uint8_t *>(base + L.hit), reinterpret_cast<int32_t *>(base + L.slot),
-                             workspace, workspace_bytes, dev_status, stream);
-    if (rc != SSD_OK) return rc;
-    d2h(accept_len, L.acc, static_cast<size_t>(B) * 4);
-    d2h(bonus, L.bon, static_cast<size_t>(B) * 4);
-    d2h(cache_tok, L.cache, static_cast<size_t>(B) * budget * 4);
-    d2h(hit, L.hit, static_cast<size_t>(B));
-    d2h(slot, L.slot, static_cast<size_t>(B) * 4);
+    for (int c = 0; c < nchunk; ++c) {
+        const int c0 = static_cast<int>(static_cast<int64_t>(B) * c / nchunk);
+        const int c1 = static_cast<int>(static_cast<int64_t>(B) * (c + 1) / nchunk);
+        const int nb = c1 - c0;
+        if (cudaStreamWaitEvent(st, ev[c + 1], 0) != cudaSuccess) {
+            cudaGetLastError();
+            release();
+            return SSD_ERR_CUDA;
+        }
+        const int rc = ssd_round(
+            base + L.tgt + c0 * seq_t, base + L.drf + c0 * seq_d, dtype, nb, K, V, K,
+            reinterpret_cast<const int32_t *>(base + L.tok) + static_cast<size_t>(c0) * K,
+            reinterpret_cast<const float *>(base + L.uni) + static_cast<size_t>(c0) * (K + 1),
+            reinterpret_cast<const float *>(base + L.tau) + c0, nullptr, F_host, budget,
+            reinterpret_cast<int32_t *>(base + L.acc) + c0, reinterpret_cast<int32_t *>(base + L.bon) + c0,
+            nullptr, nullptr, reinterpret_cast<int32_t *>(base + L.cache) + static_cast<size_t>(c0) * budget,
+            reinterpret_cast<uint8_t *>(base + L.hit) + c0, reinterpret_cast<int32_t *>(base + L.slot) + c0,
+            workspace, workspace_bytes, dev_status, stream);
+        if (rc != SSD_OK) {
+            release();
+            return rc;
+        }
+        d2h(accept_len + c0, L.acc + static_cast<size_t>(c0) * 4, static_cast<size_t>(nb) * 4);
+        d2h(bonus + c0, L.bon + static_cast<size_t>(c0) * 4, static_cast<size_t>(nb) * 4);
+        d2h(cache_tok + static_cast<size_t>(c0) * budget, L.cache + static_cast<size_t>(c0) * budget * 4,
+            static_cast<size_t>(nb) * budget * 4);
+        d2h(hit + c0, L.hit + static_cast<size_t>(c0), static_cast<size_t>(nb));
+        d2h(slot + c0, L.slot + static_cast<size_t>(c0) * 4, static_cast<size_t>(nb) * 4);
+    }
+    release();
     if (!ok) {
         cudaGetLastError();
         return SSD_ERR_CUDA;

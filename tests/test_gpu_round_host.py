@@ -1,6 +1,7 @@
 """ssd_round_host: the round on host buffers gives exactly the device round's
 outputs, copies only the sampled sequences' draft rows (a greedy sequence's draft
-logits are NaN here and must not matter), and agrees with the float64 oracle."""
+logits are NaN here and must not matter), and agrees with the float64 oracle --
+also when the batch is copied and run in chunks that overlap."""
 import numpy as np
 import pytest
 
@@ -30,7 +31,12 @@ def _host_logits(a, dtype):
 
 @pytest.mark.parametrize("dtype,B,K,V,greedy", [("bf16", 24, 3, 20480, [0, 1, 2, 9, 10, 23]),
                                                  ("f32", 12, 2, 4096, [5]),
-                                                 ("bf16", 8, 4, 8192, list(range(8)))])
+                                                 ("bf16", 8, 4, 8192, list(range(8))),
+                                                 # copied and run in chunks (64 sequences or
+                                                 # more each); greedy runs cross the boundaries
+                                                 ("bf16", 160, 2, 4096,
+                                                  list(range(10)) + list(range(75, 91)) + [150, 159]),
+                                                 ("f32", 300, 2, 2048, list(range(60, 170)))])
 def test_round_host_matches_device_round_and_oracle(ssd, dtype, B, K, V, greedy):
     wl = synth.WORKLOADS["c5"].replace(B=B, K=K, V=V, dtype=dtype, greedy_first=0, budget=24)
     inp = synth.make_inputs(wl, 6100 + B)
