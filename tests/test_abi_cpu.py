@@ -224,3 +224,24 @@ def test_device_calls_validate_before_any_cuda_call(ssd):
         ssd.SSD_ERR_INVALID_ARG
     assert rs(p, 0, 4, 8, p, 8, ctypes.c_float(0.0), p, None, None, None) == ssd.SSD_ERR_INVALID_ARG
     assert rs(p, 0, 4, 100, None, 8, ctypes.c_float(0.5), p, p, None, None) == ssd.SSD_ERR_INVALID_ARG
+
+
+def test_round_host_binding_validates_before_any_device_use(ssd):
+    torch = pytest.importorskip("torch")
+    B, K, V = 4, 2, 64
+    tgt = torch.zeros((B, K + 1, V), dtype=torch.float32)
+    drf = torch.zeros((B, K, V), dtype=torch.float32)
+    tok = torch.zeros((B, K), dtype=torch.int32)
+    u = torch.zeros((B, K + 1), dtype=torch.float32)
+    tau = torch.ones(B, dtype=torch.float32)
+    F = [1, 1, 1]
+    with pytest.raises(ValueError):
+        ssd.ssd_round_host(tgt, drf[:, :1], tok, u, tau, F, 3)  # drf not [B, K, V]
+    with pytest.raises(TypeError):
+        ssd.ssd_round_host(tgt, drf.to(torch.bfloat16), tok, u, tau, F, 3)  # dtypes differ
+    with pytest.raises(TypeError):
+        ssd.ssd_round_host(tgt, drf, tok.to(torch.int64), u, tau, F, 3)
+    with pytest.raises(ValueError):
+        ssd.ssd_round_host(tgt, drf, tok, u[:, :K], tau, F, 3)  # uniforms not [B, K+1]
+    with pytest.raises(ValueError):
+        ssd.ssd_round_host(tgt.transpose(0, 1), drf, tok, u, tau, F, 3)  # not contiguous
