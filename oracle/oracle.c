@@ -35,6 +35,9 @@
  *     logits with the drafted token excluded (tau == 0);
  *   - draft-only cache keys: raw draft logits of row k (of K+1 draft rows), the
  *     drafted token left out for k < K; the reshape at position k uses F = F_k.
+ * Parity unpinned: the pages print no value that fixes which uniform draws the
+ * bonus, the CDF order and boundary, or the Z == 0 fallback; for those three
+ * readings the pins can only check internal consistency.
  */
 #include <math.h>
 #include <stdint.h>
