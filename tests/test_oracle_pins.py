@@ -286,6 +286,76 @@ def test_bonus_on_rejection_is_inverse_cdf_of_residual():
     np.testing.assert_allclose(o["Z"], w.sum(), rtol=1e-12)
 
 
+def _z0_rows(rng, K, V, reject_at):
+    """Target = draft at every position (p_i == q_i, so the residual is zero
+    everywhere), with the drafted token at -inf in both rows at `reject_at`: that
+    token has p = q = 0, u * 0 < 0 fails for every u, so the draft is rejected there
+    with Z = 0.  Earlier positions draft a finite token with p == q > 0, accepted for
+    every u < 1.  Each position has its own row, so a draw from the wrong row shows."""
+    z = (rng.standard_normal((K + 1, V)) * 2).astype(np.float32)
+    x = np.array([int(np.argmax(z[i])) for i in range(K)], np.int32)
+    x[reject_at] = (x[reject_at] + 3) % V
+    z[reject_at, x[reject_at]] = -np.inf
+    return z, x
+
+
+@pytest.mark.parametrize("reject_at", [0, 1, 2])
+def test_bonus_when_residual_is_zero_is_drawn_from_p(reject_at):
+    """Z = 0 at the rejected row (p_a == q_a): the reading draws the bonus from p_a,
+    the residual's limit.  Pinned against numpy's inverse CDF of the library softmax
+    of row a, so drawing from the all-zero residual, from another row or with another
+    uniform fails."""
+    rng = np.random.default_rng(17 + reject_at)
+    V, K, n = 40, 3, 400
+    z, x = _z0_rows(rng, K, V, reject_at)
+    p = scipy.special.softmax(z[reject_at].astype(np.float64))
+    assert p[x[reject_at]] == 0.0
+    c = np.cumsum(p)
+    u = rng.random((n, K + 1), dtype=np.float32)
+    T = u[:, K].astype(np.float64) * c[-1]
+    keep = np.min(np.abs(T[:, None] - c[None, :]), axis=1) > 1e-9   # away from CDF steps
+    o = oracle.verify(_batch(z, n), _batch(z[:K], n), _batch(x, n), u, np.ones(n, np.float32),
+                      "f32")
+    assert (o["accept_len"] == reject_at).all()
+    want = np.searchsorted(c, T, side="right")
+    np.testing.assert_array_equal(o["bonus"][keep], want[keep])
+    assert keep.mean() > 0.95
+    # the draw covers the support of p_a, never the rejected token
+    assert x[reject_at] not in set(o["bonus"].tolist())
+    assert len(set(o["bonus"].tolist())) > 5
+
+
+@pytest.mark.parametrize("reject_at", [0, 2])
+def test_p_hit_when_residual_is_zero_is_the_cached_mass_of_p(reject_at):
+    """With every draft before `reject_at` accepted for sure and the one at
+    `reject_at` rejected for sure with Z = 0, the outcome length is fixed and
+    P_hit = sum_{t in S_a} p_a(t) (closed form from the library softmax); the hit
+    frequency of the oracle's own rounds agrees within Monte Carlo error."""
+    rng = np.random.default_rng(31 + reject_at)
+    V, K, n = 40, 3, 100_000
+    z, x = _z0_rows(rng, K, V, reject_at)
+    F = [5, 4, 6, 3]
+    off = np.concatenate([[0], np.cumsum(F)]).astype(np.int32)
+    budget = int(off[-1])
+    # segment a holds some likely and some unlikely tokens of p_a; other segments hold
+    # the tokens p_a favours most, so a wrong segment changes the answer
+    order = np.argsort(-z[reject_at], kind="stable")
+    cache = np.zeros((1, budget), np.int32)
+    for k in range(K + 1):
+        cache[0, off[k]:off[k + 1]] = order[:F[k]] if k != reject_at else order[[1, 3, 7, 12, 20, 25]][:F[k]]
+    p = scipy.special.softmax(z[reject_at].astype(np.float64))
+    want = p[cache[0, off[reject_at]:off[reject_at + 1]]].sum()
+    got = oracle.p_hit(z[None], z[None, :K], x[None], np.ones(1, np.float32), "f32", off,
+                       budget, cache)[0]
+    assert got == pytest.approx(want, abs=1e-12)
+    u = rng.random((n, K + 1), dtype=np.float32)
+    v = oracle.verify(_batch(z, n), _batch(z[:K], n), _batch(x, n), u, np.ones(n, np.float32),
+                      "f32")
+    h = oracle.lookup(_batch(cache[0], n), off, v["accept_len"], v["bonus"])["hit"]
+    se = np.sqrt(want * (1 - want) / n)
+    assert abs(h.mean() - want) < 4 * se, (h.mean(), want)
+
+
 def test_invalid_inputs_are_flagged():
     rng = np.random.default_rng(10)
     B, K, V = 4, 2, 16
