@@ -209,6 +209,7 @@ def build_cache(tgt, drf, tokens, temperature, dtype, off, budget: int, reshape_
             _ptr(out["cache_score"]), _ptr(out["cache_margin"]))
 
     out["invalid"] = _parallel(run, B, threads)
+    out["temperature"] = tau.copy()      # which scores are raw logits (tau == 0)
     return out
 
 
@@ -269,7 +270,7 @@ def round_(tgt, drf, tokens, uniforms, temperature, dtype, off, budget: int,
                     threads)
     h = lookup(c["cache_tok"], off, v["accept_len"], v["bonus"])
     out = dict(v)
-    out.update({k: c[k] for k in ("cache_tok", "cache_score", "cache_margin")})
+    out.update({k: c[k] for k in ("cache_tok", "cache_score", "cache_margin", "temperature")})
     out.update(h)
     out["invalid"] = v["invalid"] + c["invalid"]
     return out

@@ -110,7 +110,14 @@ def compare_verify(g: dict, o: dict, K: int, tally: Tally, probs: bool = True):
 
 
 def compare_cache(g_cache: np.ndarray, o: dict, off, K: int, tally: Tally, skip_rows=()):
+    """Cache segments in rank order.  A segment is a near-tie decision when the oracle's
+    boundary margin or a gap between consecutive kept scores lies in (0, 1e-6).  Exact
+    ties (gap 0) are decided by the lowest id on both sides, so they must match bit for
+    bit; the one exception is a sampled sequence whose kept scores reach 0, the clamp of
+    (p - q)^+, which hides how close the clamped residuals are to 0 (the order among
+    them, and the boundary, then counts as near)."""
     oc = o["cache_tok"]
+    tau = np.asarray(o.get("temperature", np.ones(oc.shape[0], np.float32)))
     for b in range(oc.shape[0]):
         if b in skip_rows:
             continue
@@ -122,7 +129,8 @@ def compare_cache(g_cache: np.ndarray, o: dict, off, K: int, tally: Tally, skip_
             sg, so = g_cache[b, lo:hi], oc[b, lo:hi]
             sc = o["cache_score"][b, lo:hi]
             gaps = -np.diff(sc) if hi - lo > 1 else np.array([np.inf])
-            near = o["cache_margin"][b, k] < MARGIN or bool(np.any(gaps < MARGIN))
+            near = (o["cache_margin"][b, k] < MARGIN or bool(np.any((gaps > 0) & (gaps < MARGIN)))
+                    or (tau[b] > 0 and sc[-1] == 0.0))
             if near:
                 tally.near_margin += 1
             if np.array_equal(sg, so):
