@@ -594,6 +594,12 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         s_nS = 0;
         fence_mbar_init();
     }
+    // Launched right behind another kernel (programmatic dependent launch), this
+    // grid may get here while that kernel still runs: only shared memory is set
+    // up above.  Global memory -- the inputs, which the previous kernel may have
+    // written, and the workspace, which the previous round's last block resets --
+    // is read only after that grid has completed and its writes are visible.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     __syncthreads();
     // Unit order: pair units (sampled sequence, k < K) first, then the sampled
     // rows K, then the other sequences' rows.  Every CTA maps the shared unit
@@ -644,11 +650,6 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         }
     }
     __syncthreads();
-    // Launched right behind another round (programmatic dependent launch), this
-    // grid may get here while that round's last blocks still drain: the lines
-    // above read only inputs, and the workspace, which the previous round's
-    // last block resets, is touched only once that grid has completed.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     // =========================== producers ==================================
     if (warp >= kProducerWarp0 && warp < kTailWarp0) {

@@ -167,3 +167,42 @@ def test_accepted_pairs_bound_the_groups_they_compute(ssd, dtype, same):
     inp = _pack(zt, zd[:, :K].copy(), tok, u, [1.0] * B, dtype)
     g, o, F = _round_and_compare(ssd, inp, 28, 0.75, 0.5)
     assert (g["accept_len"] == K).all()
+
+
+def test_round_reads_inputs_written_just_before_it(ssd):
+    """The streaming kernel is launched so that it may start while the kernel before
+    it on the stream drains; it must still see what that kernel wrote.  Temperatures
+    and uniforms are rewritten by torch kernels right before each round (the greedy
+    and sampled halves swapped, fresh uniforms), and every round is compared with the
+    oracle on the values written last."""
+    wl = synth.WORKLOADS["c5"].replace(B=64, greedy_first=32)
+    inp = synth.make_inputs(wl, synth.PARITY_SEED["c5"] + 31)
+    F, off = ssd.ssd_fanout(wl.K, wl.budget, wl.a_p, wl.r, wl.V)
+    d = to_device(inp)
+    tau_a = inp["temperature"]
+    tau_b = np.where(tau_a > 0, 0.0, 1.0).astype(np.float32)
+    rng = np.random.default_rng(5)
+    tau_dev = torch.empty_like(d["temperature"])
+    u_dev = torch.empty_like(d["uniforms"])
+    ws = ssd.workspace(wl.B, wl.K)
+    outs, cases = [], []
+    for tau_np in (tau_a, tau_b, tau_a):
+        u_np = rng.random((wl.B, wl.K + 1), dtype=np.float32)
+        tau_src = torch.from_numpy(tau_np).cuda()
+        u_src = torch.from_numpy(u_np).cuda()
+        torch.cuda.synchronize()
+        tau_dev.copy_(tau_src)          # written by a torch kernel right before the round
+        u_dev.copy_(u_src)
+        out = ssd.ssd_round(d["tgt"], d["drf"], d["tokens"], u_dev, tau_dev, F, wl.budget,
+                            workspace=ws)
+        outs.append({k: v.clone() for k, v in out.items()})
+        cases.append((tau_np, u_np))
+    torch.cuda.synchronize()
+    for out, (tau_np, u_np) in zip(outs, cases):
+        g = np_out(out)
+        o = oracle.round_(inp["tgt"], inp["drf"], inp["tokens"], u_np, tau_np, wl.dtype, off,
+                          wl.budget)
+        t = Tally()
+        compare_verify(g, o, wl.K, t)
+        compare_cache(g["cache_tok"], o, off, wl.K, t)
+        t.check()
