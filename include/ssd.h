@@ -116,6 +116,14 @@ typedef struct ssd_reshape_desc {
  * for an unknown policy.  Calls already enqueued are not affected. */
 int ssd_set_dispatch(int policy);
 
+/* Name of the kernel that the most recent verify / cache / round call made on
+ * the calling host thread launched ("stream" -- the persistent streaming kernel,
+ * "cluster" -- the cluster kernel, "reshape+cluster" -- the reshape kernel and
+ * then the cluster kernel for sigma found before the pass), or "none" before any
+ * such call.  Plumbing for reporting (no counterpart on the pages); the string is
+ * static, owned by the library. */
+const char *ssd_last_kernel(void);
+
 /* Check of the bounded waits (no counterpart on the pages): one warp waits on a
  * shared-memory mbarrier that nothing completes, with the same bounded wait
  * every kernel here uses but a limit of limit_ms milliseconds (1..10000); when

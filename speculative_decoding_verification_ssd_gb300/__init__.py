@@ -44,7 +44,7 @@ ABI_SYMBOLS = ("ssd_strerror", "ssd_version", "ssd_workspace_size", "ssd_verify"
                "ssd_noalloc_max_scratch", "ssd_round_noalloc", "ssd_fanout_uniform",
                "ssd_backup_fill", "ssd_draft_cache", "ssd_verify_sigma", "ssd_round_sigma",
                "ssd_set_dispatch", "ssd_check_wait_timeout", "ssd_verify_ld", "ssd_round_ld",
-               "ssd_host_staging_size", "ssd_round_host")
+               "ssd_host_staging_size", "ssd_round_host", "ssd_last_kernel")
 
 
 class SSDError(RuntimeError):
@@ -70,6 +70,8 @@ def lib() -> ctypes.CDLL:
         L.ssd_strerror.restype = ctypes.c_char_p
         L.ssd_version.argtypes = []
         L.ssd_version.restype = ctypes.c_char_p
+        L.ssd_last_kernel.argtypes = []
+        L.ssd_last_kernel.restype = ctypes.c_char_p
         L.ssd_workspace_size.argtypes = [i, i]
         L.ssd_workspace_size.restype = z
         L.ssd_verify.argtypes = [P, P, i, i, i, i, i, P, P, P, P, P, P, P, P, P, z, P, P]
@@ -144,6 +146,11 @@ def strerror(status: int) -> str:
         return lib().ssd_strerror(int(status)).decode()
     except RuntimeError:
         return f"status {status}"
+
+
+def ssd_last_kernel() -> str:
+    """The kernel the calling thread's last verify / cache / round call launched."""
+    return lib().ssd_last_kernel().decode()
 
 
 def version() -> str:

@@ -136,6 +136,8 @@ int check_fanout(const int32_t *F_host, int K, int V, int budget, int *off) {
 
 // Kernel choice for aligned rows (ssd_set_dispatch).
 std::atomic<int> g_dispatch{SSD_DISPATCH_AUTO};
+// The kernel the calling thread's last verify / cache / round call launched.
+thread_local const char *t_last_kernel = "none";
 
 // Shared driver of ssd_verify / ssd_build_cache / ssd_round.
 int run_units(int mode, const void *tgt, const void *drf, int dtype, int B, int K, int V,
@@ -248,6 +250,7 @@ int run_units(int mode, const void *tgt, const void *drf, int dtype, int B, int 
             P.desc_out = desc_out;
         }
         const int grid = std::min(dv->sm_count, units);
+        t_last_kernel = "stream";
         return ssd::stream_launch(dtype, P, grid, sdyn, stream);
     }
     if (sig_F) {
@@ -274,6 +277,7 @@ int run_units(int mode, const void *tgt, const void *drf, int dtype, int B, int 
         P.reshape = desc_out;
     }
     const int grid = units * g.CL;
+    t_last_kernel = sig_F ? "reshape+cluster" : "cluster";
     return ssd::unit_launch(dtype, P, grid, g.CL, g.dyn, stream);
 }
 
@@ -293,7 +297,9 @@ const char *ssd_strerror(int status) {
     }
 }
 
-const char *ssd_version(void) { return "libssd 0.1 (sm_103a)"; }
+const char *ssd_version(void) { return "libssd 0.2 (sm_103a)"; }
+
+const char *ssd_last_kernel(void) { return t_last_kernel; }
 
 int ssd_set_dispatch(int policy) {
     if (policy != SSD_DISPATCH_AUTO && policy != SSD_DISPATCH_STREAM && policy != SSD_DISPATCH_CLUSTER)
@@ -545,8 +551,13 @@ int ssd_round_noalloc(const void *tgt, const void *drf, int dtype, int B, int K,
     void *scratch = nullptr;
     const int st = noalloc_scratch(&scratch);
     if (st != SSD_OK) return st;
-    // The array keeps the previous call's contents: the per-sequence counters
-    // and the scheduler counters must start at zero.
+    // The array keeps the previous call's contents.  A round that completes leaves
+    // its per-sequence and scheduler counters at zero (the last unit of a sequence
+    // and the grid's last tail warp reset them), but one that gave up early (a
+    // device timeout) or a different batch shape would not: clearing them here
+    // makes every call start from zero.  This clear sits between back-to-back
+    // calls, so these rounds do not overlap one another through programmatic
+    // dependent launch.
     unsigned char *base = static_cast<unsigned char *>(scratch);
     const size_t rec = ssd::ws_rec_bytes(B, K);
     if (cudaMemsetAsync(base + rec, 0, need - rec, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
@@ -604,25 +615,45 @@ bool host_staging_args_ok(int dtype, int B, int K, int V, int budget) {
            (dtype == SSD_F32 || dtype == SSD_BF16);
 }
 
-// One stream per device for the host-to-device copies of ssd_round_host, so that a
-// chunk's round overlaps the copies of the next chunk (created on first use, kept
-// until the process exits).
-std::mutex g_copy_mu;
-cudaStream_t g_copy_stream[kMaxDevices] = {};
+// Per device, for ssd_round_host: one stream for the host-to-device copies, so that
+// a chunk's round overlaps the copies of the next chunk, and the events that order
+// the copies and the rounds (created on first use, kept until the process exits).
+// A call holds its device's lock while it enqueues: an event is re-recorded only by
+// the next call, and a stream wait binds to the record made before it, so reuse
+// across calls is safe.
+constexpr int kHostChunks = 4;
 
-int copy_stream(cudaStream_t *out) {
+struct HostRoundRes {
+    std::mutex mu;
+    cudaStream_t copy = nullptr;
+    cudaEvent_t ev[kHostChunks + 1] = {};
+    bool ready = false;
+};
+
+std::mutex g_copy_mu;
+HostRoundRes g_host_res[kMaxDevices];
+
+int host_round_res(HostRoundRes **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SSD_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_copy_mu);
-    if (!g_copy_stream[dev]) {
-        cudaStream_t s = nullptr;
-        if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) {
+    HostRoundRes &r = g_host_res[dev];
+    if (!r.ready) {
+        if (!r.copy && cudaStreamCreateWithFlags(&r.copy, cudaStreamNonBlocking) != cudaSuccess) {
+            r.copy = nullptr;
             cudaGetLastError();
             return SSD_ERR_CUDA;
         }
-        g_copy_stream[dev] = s;
+        for (int i = 0; i <= kHostChunks; ++i) {
+            if (!r.ev[i] && cudaEventCreateWithFlags(&r.ev[i], cudaEventDisableTiming) != cudaSuccess) {
+                r.ev[i] = nullptr;
+                cudaGetLastError();
+                return SSD_ERR_CUDA;
+            }
+        }
+        r.ready = true;
     }
-    *out = g_copy_stream[dev];
+    *out = &r;
     return SSD_OK;
 }
 
@@ -660,23 +691,15 @@ int ssd_round_host(const void *tgt, const void *drf, int dtype, int B, int K, in
     const HostStaging L = host_staging_layout(dtype, B, K, V, budget);
     if (staging_bytes < L.total) return SSD_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    cudaStream_t cs = nullptr;  // the copies run here, each chunk's round on `stream`
-    const int cst = copy_stream(&cs);
-    if (cst != SSD_OK) return cst;
+    HostRoundRes *res = nullptr;
+    const int rst = host_round_res(&res);
+    if (rst != SSD_OK) return rst;
+    std::lock_guard<std::mutex> enqueue_lock(res->mu);
+    cudaStream_t cs = res->copy;  // the copies run here, each chunk's round on `stream`
+    cudaEvent_t *ev = res->ev;
     // Consecutive sequences in up to 4 chunks of at least 64: the round on chunk c
     // runs while the next chunk is copied (sequences are independent).
-    const int nchunk = std::max(1, std::min(4, B / 64));
-    cudaEvent_t ev[5] = {};
-    for (int i = 0; i <= nchunk; ++i) {
-        if (cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) != cudaSuccess) {
-            cudaGetLastError();
-            for (int j = 0; j < i; ++j) cudaEventDestroy(ev[j]);
-            return SSD_ERR_CUDA;
-        }
-    }
-    const auto release = [&]() {
-        for (int i = 0; i <= nchunk; ++i) cudaEventDestroy(ev[i]);  // freed once complete
-    };
+    const int nchunk = std::max(1, std::min(kHostChunks, B / 64));
     unsigned char *base = static_cast<unsigned char *>(staging);
     size_t moved = 0;
     bool ok = true;
@@ -721,7 +744,6 @@ int ssd_round_host(const void *tgt, const void *drf, int dtype, int B, int K, in
     }
     if (!ok) {
         cudaGetLastError();
-        release();
         return SSD_ERR_CUDA;
     }
     for (int c = 0; c < nchunk; ++c) {
@@ -730,7 +752,6 @@ int ssd_round_host(const void *tgt, const void *drf, int dtype, int B, int K, in
         const int nb = c1 - c0;
         if (cudaStreamWaitEvent(st, ev[c + 1], 0) != cudaSuccess) {
             cudaGetLastError();
-            release();
             return SSD_ERR_CUDA;
         }
         const int rc = ssd_round(
@@ -742,10 +763,7 @@ int ssd_round_host(const void *tgt, const void *drf, int dtype, int B, int K, in
             nullptr, nullptr, reinterpret_cast<int32_t *>(base + L.cache) + static_cast<size_t>(c0) * budget,
             reinterpret_cast<uint8_t *>(base + L.hit) + c0, reinterpret_cast<int32_t *>(base + L.slot) + c0,
             workspace, workspace_bytes, dev_status, stream);
-        if (rc != SSD_OK) {
-            release();
-            return rc;
-        }
+        if (rc != SSD_OK) return rc;
         d2h(accept_len + c0, L.acc + static_cast<size_t>(c0) * 4, static_cast<size_t>(nb) * 4);
         d2h(bonus + c0, L.bon + static_cast<size_t>(c0) * 4, static_cast<size_t>(nb) * 4);
         d2h(cache_tok + static_cast<size_t>(c0) * budget, L.cache + static_cast<size_t>(c0) * budget * 4,
@@ -753,7 +771,6 @@ int ssd_round_host(const void *tgt, const void *drf, int dtype, int B, int K, in
         d2h(hit + c0, L.hit + static_cast<size_t>(c0), static_cast<size_t>(nb));
         d2h(slot + c0, L.slot + static_cast<size_t>(c0) * 4, static_cast<size_t>(nb) * 4);
     }
-    release();
     if (!ok) {
         cudaGetLastError();
         return SSD_ERR_CUDA;

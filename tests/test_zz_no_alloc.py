@@ -67,16 +67,25 @@ def _noalloc_round(ssd, tgt, drf, tok, u, tau, F, budget):
     return {k: v.cpu().numpy() for k, v in out.items()}
 
 
-def test_noalloc_round_matches_round_on_two_calls(ssd):
-    wl = synth.WORKLOADS["c5"].replace(B=48, greedy_first=24)
-    inp = synth.make_inputs(wl, 777)
+@pytest.mark.parametrize("B,policy", [(48, "auto"), (48, "cluster"), (8, "auto")])
+def test_noalloc_round_matches_round_on_two_calls(ssd, B, policy):
+    """B = 48 (240 units) runs the persistent streaming kernel unless the cluster
+    kernel is forced; B = 8 (40 units, fewer than the SMs) takes the cluster kernel
+    by itself.  Both kernels use the same counters and records in the array."""
+    wl = synth.WORKLOADS["c5"].replace(B=B, greedy_first=B // 2)
+    inp = synth.make_inputs(wl, 777 + B)
     tgt, drf, tok, u, tau = _device_inputs(inp)
     F, off = ssd.ssd_fanout(wl.K, wl.budget, wl.a_p, wl.r, wl.V)
-    ref = ssd.ssd_round(tgt, drf, tok, u, tau, F, wl.budget)
-    torch.cuda.synchronize()
-    ref = {k: v.cpu().numpy() for k, v in ref.items()}
-    for _ in range(2):
-        got = _noalloc_round(ssd, tgt, drf, tok, u, tau, F, wl.budget)
+    pol = {"auto": ssd.SSD_DISPATCH_AUTO, "cluster": ssd.SSD_DISPATCH_CLUSTER}[policy]
+    prev = ssd.ssd_set_dispatch(pol)
+    try:
+        ref = ssd.ssd_round(tgt, drf, tok, u, tau, F, wl.budget)
+        torch.cuda.synchronize()
+        ref = {k: v.cpu().numpy() for k, v in ref.items()}
+        gots = [_noalloc_round(ssd, tgt, drf, tok, u, tau, F, wl.budget) for _ in range(2)]
+    finally:
+        ssd.ssd_set_dispatch(prev)
+    for got in gots:
         for key in ("accept_len", "bonus", "cache_tok", "hit", "slot"):
             np.testing.assert_array_equal(got[key], ref[key], err_msg=key)
         for key in ("p_tok", "q_tok"):
