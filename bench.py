@@ -49,6 +49,9 @@ def parse():
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--workloads", default="c1,c2,c3,c4",
+                    help="further workloads timed after the headline one (one GPU only), "
+                         "comma-separated, or 'none'")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch (greedy share scaled); for profiling")
     ap.add_argument("--two-pass-sigma", action="store_true",
@@ -101,6 +104,12 @@ def max_over_ranks(x: float, pg, device) -> float:
 def job_rate(units_per_rank: int, world: int, elapsed_ms: float) -> float:
     """Whole-job throughput: the units all ranks processed over the (max-over-ranks) time."""
     return world * units_per_rank / (elapsed_ms * 1e-3)
+
+
+def kernel_label(kind: str, wl) -> str:
+    tag = "F32Tag" if wl.dtype == synth.F32 else "BF16Tag"
+    return {"stream": f"ssd_stream_kernel<{tag}>", "cluster": f"ssd_unit_kernel<{tag}>",
+            "reshape+cluster": f"ssd_reshape_kernel<{tag}> + ssd_unit_kernel<{tag}>"}.get(kind, kind)
 
 
 def workload_config(wl) -> dict:
@@ -243,6 +252,133 @@ def cpu_baseline(inp, wl, off, sample_per_half: int = 128):
                       f"{threads} host threads; {dt:.2f} s wall"}
 
 
+def prepare(wl, seed: int, ssd, torch, dev, two_pass_sigma: bool = False) -> dict:
+    """Inputs of one workload on the device and its step (one call of the path over
+    the whole batch).  Workloads with a sigma_{F,C} draft redraw their drafted tokens
+    from sigma_{F,C} on the device (input synthesis, not a step of the method)."""
+    inp = synth.make_inputs(wl, seed)
+    F, off = ssd.ssd_fanout(wl.K, max(wl.budget, 0), wl.a_p or 0.5, wl.r, wl.V) if wl.budget else (
+        np.zeros(wl.K + 1, np.int32), np.zeros(wl.K + 2, np.int32))
+    d = to_device(inp, torch, dev)
+    ws = ssd.workspace(wl.B, wl.K, dev)
+    stream = torch.cuda.current_stream(dev)
+    sig = wl.reshape_F > 0
+    sig_F = [wl.reshape_F] * wl.K
+    desc = torch.zeros((wl.B * wl.K, 4), dtype=torch.int32, device=dev)
+    if sig:
+        ssd.ssd_reshape_draft(d["drf"], wl.reshape_F, wl.reshape_C, desc=desc)
+        thr_val, thr_id, _, _ = ssd.desc_fields(desc)
+        zd = d["drf"].float()
+        ids = torch.arange(wl.V, device=dev).view(1, 1, wl.V)
+        mem = (zd > thr_val.view(wl.B, wl.K, 1)) | ((zd == thr_val.view(wl.B, wl.K, 1)) &
+                                                     (ids <= thr_id.view(wl.B, wl.K, 1)))
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(seed + 7)
+        gum = -torch.log(-torch.log(torch.rand(zd.shape, generator=gen, device=dev).clamp_min(1e-30)))
+        tau = d["temperature"].view(wl.B, 1, 1)
+        score = zd / tau.clamp_min(1e-30) + mem.float() * float(np.log(wl.reshape_C)) + gum
+        d["tokens"] = torch.where(tau.view(wl.B, 1) > 0, torch.argmax(score, dim=-1),
+                                  torch.argmax(zd, dim=-1)).to(torch.int32).contiguous()
+        del zd, mem, gum, score
+    box = {"out": None}
+
+    def step():
+        out = box["out"]
+        if wl.mode == "round":
+            r = ssd.ssd_round(d["tgt"], d["drf"], d["tokens"], d["uniforms"], d["temperature"], F,
+                              wl.budget, out=out, probs=False, workspace=ws, stream=stream)
+        elif sig and two_pass_sigma:
+            ssd.ssd_reshape_draft(d["drf"], wl.reshape_F, wl.reshape_C, desc=desc, stream=stream)
+            r = ssd.ssd_verify(d["tgt"], d["drf"], d["tokens"], d["uniforms"], d["temperature"],
+                               reshape=desc, probs=False, workspace=ws, stream=stream)
+        elif sig:
+            r = ssd.ssd_verify_sigma(d["tgt"], d["drf"], d["tokens"], d["uniforms"],
+                                     d["temperature"], sig_F, wl.reshape_C, desc_out=desc,
+                                     probs=False, workspace=ws, stream=stream)
+        else:
+            r = ssd.ssd_verify(d["tgt"], d["drf"], d["tokens"], d["uniforms"], d["temperature"],
+                               probs=False, workspace=ws, stream=stream)
+        box["out"] = r if wl.mode == "round" else None
+        return r
+
+    return {"wl": wl, "inp": inp, "F": F, "off": off, "d": d, "ws": ws, "stream": stream,
+            "sig": sig, "sig_F": sig_F, "desc": desc, "step": step,
+            "launches_per_step": 2 if (sig and two_pass_sigma) else 1}
+
+
+def back_to_back_ms(step, stream, torch, dev, n: int) -> float:
+    """Device time of n launches issued back to back (CUDA events on the launching
+    stream around them, none between: the streaming kernel may start while the
+    previous launch drains)."""
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    a.record(stream)
+    for _ in range(n):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    return a.elapsed_time(b)
+
+
+def isolated_ms(step, stream, torch, dev, n: int) -> list:
+    """Per-launch device time with an event on each side of every launch."""
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    for i in range(n):
+        ev0[i].record(stream)
+        step()
+        ev1[i].record(stream)
+    torch.cuda.synchronize(dev)
+    return [x.elapsed_time(y) for x, y in zip(ev0, ev1)]
+
+
+def measure_workload(name: str, ssd, torch, dev, peak: float) -> dict:
+    """One line per further workload: the whole path over its batch, timed with CUDA
+    events over back-to-back launches (at least 200; 2000 for the single-sequence
+    one), isolated launch times, algorithmic bytes from the actual accepted lengths
+    and the fraction of the measured copy bandwidth."""
+    wl = synth.WORKLOADS[name]
+    pr = prepare(wl, synth.BENCH_SEED[name], ssd, torch, dev)
+    out = pr["step"]()
+    torch.cuda.synchronize(dev)
+    kernel = ssd.ssd_last_kernel()
+    acc = out["accept_len"].cpu().numpy()
+    tau = pr["inp"]["temperature"]
+    alg = synth.algorithmic_bytes(wl, tau, acc)
+    # a sigma draft: the bytes of the rows the verification needs (the pass finds each
+    # row's descriptor while it reads it; rows after the first rejection are not needed)
+    rows_bytes = synth.algorithmic_bytes(wl.replace(reshape_F=0), tau, acc)
+    n = 2000 if wl.B == 1 else 300
+    for _ in range(20):
+        pr["step"]()
+    ms = back_to_back_ms(pr["step"], pr["stream"], torch, dev, n) / n
+    iso = isolated_ms(pr["step"], pr["stream"], torch, dev, 200)
+    basis = rows_bytes if pr["sig"] else alg
+    achieved = basis / (ms * 1e-3) / 1e9
+    entry = {
+        "workload": f"{wl.name}: {wl.description}", "B": wl.B, "K": wl.K, "V": wl.V,
+        "logits": wl.dtype, "call": ("ssd_round" if wl.mode == "round" else
+                                     "ssd_verify_sigma" if pr["sig"] else "ssd_verify"),
+        "kernel": kernel, "launches_timed": n,
+        "us_per_round": ms * 1e3, "rounds_per_s": 1e3 / ms, "sequence_rounds_per_s": wl.B * 1e3 / ms,
+        "isolated_us": {"mean": statistics.mean(iso) * 1e3, "p10": float(np.percentile(iso, 10)) * 1e3,
+                        "p90": float(np.percentile(iso, 90)) * 1e3},
+        "algorithmic_bytes_per_round": alg,
+        "hbm_gbs": achieved, "frac": achieved / peak,
+        "accept_mean": float(np.mean(acc[acc >= 0])) if (acc >= 0).any() else None,
+    }
+    if pr["sig"]:
+        entry["bytes_basis"] = ("rows the verification reads (2(a+1) rows per sequence below a "
+                                "full accept); algorithmic_bytes_per_round adds the separate "
+                                "reshape pass over every draft row")
+        entry["verify_row_bytes_per_round"] = rows_bytes
+    if wl.mode == "round":
+        entry["hit_rate"] = float(out["hit"].float().mean().item())
+    del pr, out
+    torch.cuda.empty_cache()
+    return entry
+
+
 def run_ours(args):
     import torch
     world, rank, local = dist_env()
@@ -257,54 +393,18 @@ def run_ours(args):
     from speculative_decoding_verification_ssd_gb300 import _build
 
     wl = chosen_workload(args)
-    inp = synth.make_inputs(wl, rank_seed(wl.name, rank))
-    F, off = ssd.ssd_fanout(wl.K, max(wl.budget, 0), wl.a_p or 0.5, wl.r, wl.V) if wl.budget else (
-        np.zeros(wl.K + 1, np.int32), np.zeros(wl.K + 2, np.int32))
-    d = to_device(inp, torch, dev)
-    ws = ssd.workspace(wl.B, wl.K, dev)
-    stream = torch.cuda.current_stream(dev)
-    out = None
-    sig = wl.reshape_F > 0
-    sig_F = [wl.reshape_F] * wl.K
-    launches_per_step = 2 if (sig and args.two_pass_sigma) else 1
-    desc = torch.zeros((wl.B * wl.K, 4), dtype=torch.int32, device=dev)
-    if sig:
-        # the draft samples from sigma_{F,C}: redraw the drafted tokens from it (input
-        # synthesis on the device: Gumbel-max over the reshaped draft logits)
-        ssd.ssd_reshape_draft(d["drf"], wl.reshape_F, wl.reshape_C, desc=desc)
-        thr_val, thr_id, _, _ = ssd.desc_fields(desc)
-        zd = d["drf"].float()
-        ids = torch.arange(wl.V, device=dev).view(1, 1, wl.V)
-        mem = (zd > thr_val.view(wl.B, wl.K, 1)) | ((zd == thr_val.view(wl.B, wl.K, 1)) &
-                                                     (ids <= thr_id.view(wl.B, wl.K, 1)))
-        gen = torch.Generator(device=dev)
-        gen.manual_seed(synth.BENCH_SEED[wl.name] + 7 + rank)
-        gum = -torch.log(-torch.log(torch.rand(zd.shape, generator=gen, device=dev).clamp_min(1e-30)))
-        tau = d["temperature"].view(wl.B, 1, 1)
-        score = zd / tau.clamp_min(1e-30) + mem.float() * float(np.log(wl.reshape_C)) + gum
-        d["tokens"] = torch.where(tau.view(wl.B, 1) > 0, torch.argmax(score, dim=-1),
-                                  torch.argmax(zd, dim=-1)).to(torch.int32).contiguous()
-        del zd, mem, gum, score
-
-    def step():
-        if wl.mode == "round":
-            return ssd.ssd_round(d["tgt"], d["drf"], d["tokens"], d["uniforms"], d["temperature"], F,
-                                 wl.budget, out=out, probs=False, workspace=ws, stream=stream)
-        if sig and args.two_pass_sigma:
-            ssd.ssd_reshape_draft(d["drf"], wl.reshape_F, wl.reshape_C, desc=desc, stream=stream)
-            return ssd.ssd_verify(d["tgt"], d["drf"], d["tokens"], d["uniforms"], d["temperature"],
-                                  reshape=desc, probs=False, workspace=ws, stream=stream)
-        if sig:
-            return ssd.ssd_verify_sigma(d["tgt"], d["drf"], d["tokens"], d["uniforms"],
-                                        d["temperature"], sig_F, wl.reshape_C, desc_out=desc,
-                                        probs=False, workspace=ws, stream=stream)
-        return ssd.ssd_verify(d["tgt"], d["drf"], d["tokens"], d["uniforms"], d["temperature"],
-                              probs=False, workspace=ws, stream=stream)
+    pr = prepare(wl, rank_seed(wl.name, rank), ssd, torch, dev, args.two_pass_sigma)
+    inp, F, off, d, ws, stream = pr["inp"], pr["F"], pr["off"], pr["d"], pr["ws"], pr["stream"]
+    sig, sig_F, desc, step = pr["sig"], pr["sig_F"], pr["desc"], pr["step"]
+    launches_per_step = pr["launches_per_step"]
 
     out = step()
     torch.cuda.synchronize(dev)
     acc = out["accept_len"].cpu().numpy()
     alg_bytes = synth.algorithmic_bytes(wl, inp["temperature"], acc)
+    if sig and not args.two_pass_sigma:
+        # descriptors found while the rows are read: the bytes are the rows verification needs
+        alg_bytes = synth.algorithmic_bytes(wl.replace(reshape_F=0), inp["temperature"], acc)
     dense_bytes = wl.B * (2 * wl.K + 1) * wl.V * wl.elem_bytes
 
     sampler = ClockSampler(local)
@@ -334,14 +434,8 @@ def run_ours(args):
     clocks = sampler.summary(t_wall0, t_wall1)
     # isolated launch durations (an event on each side of every launch), after the timed region
     n_iso = min(args.steps, 200)
-    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(n_iso)]
-    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(n_iso)]
-    for i in range(n_iso):
-        ev0[i].record(stream)
-        step()
-        ev1[i].record(stream)
-    torch.cuda.synchronize(dev)
-    kernel_ms = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
+    kernel_ms = isolated_ms(step, stream, torch, dev, n_iso)
+    kernel_name = ssd.ssd_last_kernel()
 
     # end to end: pinned host inputs -> device, round, outputs -> host, every step
     host = {k: v.cpu().pin_memory() for k, v in d.items()}
@@ -413,7 +507,7 @@ def run_ours(args):
                      "frac": achieved / peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
                      "traffic": traffic_record(_build.stream_kernel_digest()),
-                     "kernel": "ssd_stream_kernel<BF16Tag>"},
+                     "kernel": kernel_label(kernel_name, wl)},
         "e2e": {"value": job_rate(args.e2e_steps, world, e2e_ms), "unit": "rounds/s",
                 "h2d_bytes_per_step": h2d_box[0], "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps * launches_per_step,
@@ -429,6 +523,11 @@ def run_ours(args):
             "drafted_tokens": "drawn from sigma_{F,C} of the draft (Gumbel-max on the device)"}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(inp, wl, off)
+    others = [w for w in args.workloads.split(",") if w and w != "none" and w != wl.name]
+    if world == 1 and others and not args.batch:
+        line["workloads"] = {w: measure_workload(w, ssd, torch, dev, peak) for w in others}
+        line["gpu_launches_workloads"] = sum(
+            e["launches_timed"] + 220 for e in line["workloads"].values())
     if pg:
         pg.destroy_process_group()
     if rank == 0:
