@@ -131,7 +131,7 @@ def test_standalone_lookup_matches_oracle(ssd):
     empty segments, outcomes of every length, invalid sequences (a = -1) and bonus
     tokens inside and outside the cache."""
     rng = np.random.default_rng(77)
-    K, B, V = 5, 3000, 40
+    K, B, V = 5, 3000, 10
     F = np.array([4, 0, 3, 7, 1, 6], np.int32)
     off = np.concatenate([[0], np.cumsum(F)]).astype(np.int32)
     budget = int(off[-1]) + 3                       # slots past the last segment: never read
