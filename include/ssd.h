@@ -107,10 +107,16 @@ typedef struct ssd_reshape_desc {
  * always take the cluster kernel).  AUTO: the persistent streaming kernel when
  * the batch has at least as many units (sequences x (K+1)) as the GPU has SMs,
  * or when sigma_{F,C} is found in the pass, else the cluster kernel, which
- * splits each row across a thread-block cluster.  STREAM / CLUSTER force one. */
+ * splits each row across a thread-block cluster.  STREAM / CLUSTER / SLICE force
+ * one.  SLICE, the slice kernel, splits every row into slices of 16 KB blocks
+ * that the whole GPU works on at once and combines the slices' partial results
+ * in the workspace; it applies to rows of whole 16-byte vectors (V a multiple of
+ * the vector), without sigma found in the pass, B <= 2048 and a workspace of
+ * ssd_workspace_size_v bytes; other calls fall back as under AUTO. */
 #define SSD_DISPATCH_AUTO 0
 #define SSD_DISPATCH_STREAM 1
 #define SSD_DISPATCH_CLUSTER 2
+#define SSD_DISPATCH_SLICE 3
 
 /* Sets the kernel choice; returns the previous one, or -1 (and changes nothing)
  * for an unknown policy.  Calls already enqueued are not affected. */
@@ -118,9 +124,9 @@ int ssd_set_dispatch(int policy);
 
 /* Name of the kernel that the most recent verify / cache / round call made on
  * the calling host thread launched ("stream" -- the persistent streaming kernel,
- * "cluster" -- the cluster kernel, "reshape+cluster" -- the reshape kernel and
- * then the cluster kernel for sigma found before the pass), or "none" before any
- * such call.  Plumbing for reporting (no counterpart on the pages); the string is
+ * "slice" -- the slice kernel, "cluster" -- the cluster kernel, "reshape+cluster"
+ * -- the reshape kernel and then the cluster kernel for sigma found before the
+ * pass), or "none" before any such call.  Plumbing for reporting (no counterpart on the pages); the string is
  * static, owned by the library. */
 const char *ssd_last_kernel(void);
 
@@ -141,6 +147,16 @@ const char *ssd_version(void);
 /* Bytes of workspace needed by ssd_verify / ssd_build_cache / ssd_round for a
  * batch of B sequences with K drafted tokens (0 when B or K is out of range). */
 size_t ssd_workspace_size(int B, int K);
+
+/* Workspace bytes that let every kernel serve a call with B sequences, K drafted
+ * tokens, V-token rows of `dtype` and a cache budget (0 without a cache): the
+ * ssd_workspace_size(B, K) regions plus the slice kernel's per-unit state,
+ * per-slice partial results, per-group arrays of every unit (2 x ceil(V / 64)
+ * floats) and its work queue.  A smaller workspace of at least
+ * ssd_workspace_size(B, K) bytes is still valid: the slice kernel is then not
+ * used.  Zero-filled once by the caller like the smaller one; each call leaves
+ * it zeroed.  Returns 0 for invalid arguments. */
+size_t ssd_workspace_size_v(int B, int K, int V, int dtype, int budget);
 
 /*
  * ssd_verify -- [SD] "The Algorithm (Step-by-Step)" step 3 for a batch

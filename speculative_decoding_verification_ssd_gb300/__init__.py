@@ -44,7 +44,7 @@ ABI_SYMBOLS = ("ssd_strerror", "ssd_version", "ssd_workspace_size", "ssd_verify"
                "ssd_noalloc_max_scratch", "ssd_round_noalloc", "ssd_fanout_uniform",
                "ssd_backup_fill", "ssd_draft_cache", "ssd_verify_sigma", "ssd_round_sigma",
                "ssd_set_dispatch", "ssd_check_wait_timeout", "ssd_verify_ld", "ssd_round_ld",
-               "ssd_host_staging_size", "ssd_round_host", "ssd_last_kernel")
+               "ssd_host_staging_size", "ssd_round_host", "ssd_last_kernel", "ssd_workspace_size_v")
 
 
 class SSDError(RuntimeError):
@@ -74,6 +74,8 @@ def lib() -> ctypes.CDLL:
         L.ssd_last_kernel.restype = ctypes.c_char_p
         L.ssd_workspace_size.argtypes = [i, i]
         L.ssd_workspace_size.restype = z
+        L.ssd_workspace_size_v.argtypes = [i, i, i, i, i]
+        L.ssd_workspace_size_v.restype = z
         L.ssd_verify.argtypes = [P, P, i, i, i, i, i, P, P, P, P, P, P, P, P, P, z, P, P]
         L.ssd_verify.restype = i
         L.ssd_fanout.argtypes = [i, i, d, d, i, P, P]
@@ -121,7 +123,7 @@ def lib() -> ctypes.CDLL:
     return _lib
 
 
-SSD_DISPATCH_AUTO, SSD_DISPATCH_STREAM, SSD_DISPATCH_CLUSTER = 0, 1, 2
+SSD_DISPATCH_AUTO, SSD_DISPATCH_STREAM, SSD_DISPATCH_CLUSTER, SSD_DISPATCH_SLICE = 0, 1, 2, 3
 
 
 def ssd_set_dispatch(policy: int) -> int:
@@ -204,6 +206,10 @@ def ssd_workspace_size(B: int, K: int) -> int:
     return int(lib().ssd_workspace_size(int(B), int(K)))
 
 
+def ssd_workspace_size_v(B: int, K: int, V: int, dtype: int, budget: int = 0) -> int:
+    return int(lib().ssd_workspace_size_v(int(B), int(K), int(V), int(dtype), int(budget)))
+
+
 def ssd_fanout(K: int, budget: int, a_p: float, r: float, V: int):
     """Geometric fan-out: (F [K+1], off [K+2]) as numpy int32 arrays."""
     F = np.empty(K + 1, np.int32)
@@ -222,17 +228,22 @@ def ssd_fanout_uniform(K: int, budget: int, V: int):
     return F, off
 
 
-def workspace(B: int, K: int, device=None) -> torch.Tensor:
-    """A zero-filled workspace for B sequences of K drafted tokens."""
-    n = ssd_workspace_size(B, K)
+def workspace(B: int, K: int, device=None, V: int | None = None, dtype: int | None = None,
+              budget: int = 0) -> torch.Tensor:
+    """A zero-filled workspace for B sequences of K drafted tokens; with V and dtype
+    (and the cache budget) it also holds the slice kernel's regions."""
+    if V is not None and dtype is not None:
+        n = ssd_workspace_size_v(B, K, V, dtype, budget)
+    else:
+        n = ssd_workspace_size(B, K)
     if n == 0:
-        raise ValueError("invalid B or K")
+        raise ValueError("invalid workspace arguments")
     return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
 
 
-def _workspace(ws, B, K, device):
+def _workspace(ws, B, K, device, V=None, dtype=None, budget=0):
     if ws is None:
-        ws = workspace(B, K, device)
+        ws = workspace(B, K, device, V, dtype, budget)
     _dev(ws, "workspace", torch.uint8)
     return ws
 
@@ -305,7 +316,7 @@ def ssd_verify(tgt, drf, tokens, uniforms, temperature, reshape=None, *, accept_
     if probs:
         p_tok = p_tok if p_tok is not None else torch.empty((B, K), dtype=torch.float32, device=dev)
         q_tok = q_tok if q_tok is not None else torch.empty((B, K), dtype=torch.float32, device=dev)
-    ws = _workspace(workspace, B, K, dev)
+    ws = _workspace(workspace, B, K, dev, V, _logit_dtype(tgt))
     _opt(reshape, "reshape", torch.int32)
     _check(lib().ssd_verify_ld(
         _ptr(tgt), _ptr(drf), _logit_dtype(tgt), B, K, V, ld, drf_rows, _ptr(tokens), _ptr(uniforms),
@@ -326,7 +337,7 @@ def ssd_build_cache(tgt, drf, tokens, temperature, F, budget, reshape=None, *, c
     _dev(temperature, "temperature", torch.float32)
     Fh = _F_host(F)
     cache_tok = cache_tok if cache_tok is not None else torch.full((B, budget), -1, dtype=torch.int32, device=dev)
-    ws = _workspace(workspace, B, K, dev)
+    ws = _workspace(workspace, B, K, dev, V, _logit_dtype(tgt), int(budget))
     _check(lib().ssd_build_cache(
         _ptr(tgt), _ptr(drf), _logit_dtype(tgt), B, K, V, drf_rows, _ptr(tokens),
         _ptr(temperature), _ptr(_opt(reshape, "reshape", torch.int32)), _ptr(Fh), int(budget),
@@ -394,7 +405,7 @@ def ssd_round(tgt, drf, tokens, uniforms, temperature, F, budget, reshape=None, 
         o["hit"] = torch.empty(B, dtype=torch.uint8, device=dev)
     if "slot" not in o:
         o["slot"] = torch.empty(B, dtype=torch.int32, device=dev)
-    ws = _workspace(workspace, B, K, dev)
+    ws = _workspace(workspace, B, K, dev, V, _logit_dtype(tgt), int(budget))
     _check(lib().ssd_round_ld(
         _ptr(tgt), _ptr(drf), _logit_dtype(tgt), B, K, V, ld, drf_rows, _ptr(tokens), _ptr(uniforms),
         _ptr(temperature), _ptr(_opt(reshape, "reshape", torch.int32)), _ptr(Fh), int(budget),
@@ -456,7 +467,7 @@ def ssd_round_host(tgt, drf, tokens, uniforms, temperature, F, budget, *, out=No
     if staging is None:
         staging = torch.empty(need, dtype=torch.uint8, device=dev)
     _dev(staging, "staging", torch.uint8)
-    ws = _workspace(workspace, B, K, dev)
+    ws = _workspace(workspace, B, K, dev, V, dt, int(budget))
     moved = ctypes.c_size_t(0)
     _check(lib().ssd_round_host(
         _ptr(tgt), _ptr(drf), dt, B, K, V, _ptr(tokens), _ptr(uniforms), _ptr(temperature), _ptr(Fh),

@@ -15,6 +15,7 @@
 #include "ssd_device.cuh"
 #include "ssd_launch.cuh"
 #include "ssd_reshape.cuh"
+#include "ssd_slice.cuh"
 #include "ssd_stream.cuh"
 #include "ssd_unit.cuh"
 
@@ -28,7 +29,7 @@ struct DeviceInfo {
     int status = SSD_OK;
     int sm_count = 0;
     int max_cluster = 8;       // 16 when the non-portable size is available
-    size_t max_dyn[6] = {0};   // max dynamic smem: unit f32/bf16, reshape f32/bf16, stream f32/bf16
+    size_t max_dyn[8] = {0};   // max dynamic smem: unit, reshape, stream, slice (f32 / bf16 each)
 };
 
 DeviceInfo g_dev[kMaxDevices];
@@ -53,6 +54,8 @@ int device_info(DeviceInfo **out) {
         st = st ? st : ssd::reshape_setup(SSD_BF16, optin, &d.max_dyn[3], &allow16);
         st = st ? st : ssd::stream_setup(SSD_F32, optin, &d.max_dyn[4]);
         st = st ? st : ssd::stream_setup(SSD_BF16, optin, &d.max_dyn[5]);
+        st = st ? st : ssd::slice_setup(SSD_F32, optin, &d.max_dyn[6]);
+        st = st ? st : ssd::slice_setup(SSD_BF16, optin, &d.max_dyn[7]);
         if (st != SSD_OK) return st;
         d.max_cluster = allow16 ? 16 : 8;
         d.ready = true;
@@ -198,10 +201,18 @@ int run_units(int mode, const void *tgt, const void *drf, int dtype, int B, int 
     // streams at one group's share of an SM; the cluster kernel splits every row
     // across a cluster instead (c2: 8 sequences, K = 5: 38.5 us against 58.7).
     const int policy = g_dispatch.load(std::memory_order_relaxed);
-    const bool streaming = stream_ok && policy != SSD_DISPATCH_CLUSTER &&
+    // The slice kernel (rows split into slices scheduled over every SM) needs rows of
+    // whole vectors, its own workspace regions and a batch it can order by kind.
+    const int key_stride = ssd::slice_key_stride(K, cache ? F_host : nullptr);
+    const ssd::SliceWs SW = ssd::slice_ws_layout(B, K, V, elem, key_stride);
+    const bool slice_ok = stream_ok && sig_F == nullptr && V % (16 / elem) == 0 && B <= 2048 &&
+                          ssd::slice_pair_chunks(V, elem) <= 96 &&
+                          workspace_bytes >= SW.total && ssd::slice_dyn_bytes() <= dv->max_dyn[dtype == SSD_F32 ? 6 : 7];
+    const bool sliced = slice_ok && policy == SSD_DISPATCH_SLICE;
+    const bool streaming = !sliced && stream_ok && policy != SSD_DISPATCH_CLUSTER &&
                            (policy == SSD_DISPATCH_STREAM || sig_F != nullptr || units >= dv->sm_count);
     Geometry g;
-    if (!streaming) {
+    if (!streaming && !sliced) {
         st = choose_geometry(V, elem, 2, units, *dv, dv->max_dyn[dtype == SSD_F32 ? 0 : 1], &g);
         if (st != SSD_OK) return st;
     }
@@ -242,6 +253,27 @@ int run_units(int mode, const void *tgt, const void *drf, int dtype, int B, int 
     P.exit_counter = sched + 1;
     P.unit_ends = reinterpret_cast<unsigned long long *>(sched + 2);
     P.perm_mul = coprime_stride(B);
+    if (sliced) {
+        P.S = ssd::slice_count(units, V, elem);
+        P.nblk = ssd::slice_blocks(V, elem);
+        P.key_stride = key_stride;
+        int ko = 0;
+        for (int k = 0; k <= K; ++k) {
+            P.koff[k] = ko;
+            const int f = cache ? F_host[k] : 0;
+            ko += f > 1 ? f : 1;
+        }
+        P.slice_ctr = reinterpret_cast<uint32_t *>(ws + SW.counters);
+        P.ustate = reinterpret_cast<ssd::SliceUnitState *>(ws + SW.ustate);
+        P.sstat = reinterpret_cast<float4 *>(ws + SW.sstat);
+        P.skeys = reinterpret_cast<unsigned long long *>(ws + SW.skeys);
+        P.garr = reinterpret_cast<float *>(ws + SW.garr);
+        P.queue = reinterpret_cast<unsigned long long *>(ws + SW.queue);
+        P.pcand = reinterpret_cast<float *>(ws + SW.pcand);
+        P.cmax = reinterpret_cast<float *>(ws + SW.cmax);
+        t_last_kernel = "slice";
+        return ssd::slice_launch(dtype, P, dv->sm_count, ssd::slice_dyn_bytes(), stream);
+    }
     if (streaming) {
         if (sig_F) {
             P.sig_on = 1;
@@ -302,7 +334,8 @@ const char *ssd_version(void) { return "libssd 0.2 (sm_103a)"; }
 const char *ssd_last_kernel(void) { return t_last_kernel; }
 
 int ssd_set_dispatch(int policy) {
-    if (policy != SSD_DISPATCH_AUTO && policy != SSD_DISPATCH_STREAM && policy != SSD_DISPATCH_CLUSTER)
+    if (policy != SSD_DISPATCH_AUTO && policy != SSD_DISPATCH_STREAM && policy != SSD_DISPATCH_CLUSTER &&
+        policy != SSD_DISPATCH_SLICE)
         return -1;
     return g_dispatch.exchange(policy);
 }
@@ -310,6 +343,16 @@ int ssd_set_dispatch(int policy) {
 size_t ssd_workspace_size(int B, int K) {
     if (B < 1 || K < 1 || K > SSD_MAX_K) return 0;
     return ssd::ws_total_bytes(B, K);
+}
+
+size_t ssd_workspace_size_v(int B, int K, int V, int dtype, int budget) {
+    if (B < 1 || K < 1 || K > SSD_MAX_K || V < 2 || budget < 0) return 0;
+    if (dtype != SSD_F32 && dtype != SSD_BF16) return 0;
+    const int elem = dtype == SSD_F32 ? 4 : 2;
+    // every position keeps max(F_k, 1) keys per slice, and sum F_k <= budget
+    const size_t sl = ssd::slice_ws_layout(B, K, V, elem, budget + K + 1).total;
+    const size_t base = ssd::ws_total_bytes(B, K);
+    return sl > base ? sl : base;
 }
 
 int ssd_verify(const void *tgt, const void *drf, int dtype, int B, int K, int V, int drf_rows,

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cstdint>
+#include <vector_types.h>
 
 #include "../../include/ssd.h"
 
@@ -68,6 +69,18 @@ struct UnitParams {
     int sig_F[SSD_MAX_K];
     float sig_C;
     ssd_reshape_desc *desc_out;  // [B, K] descriptors found (sampled sequences), or nullptr
+    // slice kernel only: S slices of nblk 16 KB blocks per row; per-(sequence,
+    // slice) key areas of key_stride entries (position k at koff[k])
+    int S, nblk, key_stride;
+    int koff[SSD_MAX_K + 1];
+    struct SliceUnitState *ustate;  // [B, K+1]
+    float4 *sstat;                  // [B, K+1, S] slice statistics / residual totals
+    unsigned long long *skeys;      // [B, S, key_stride] slice top-F keys
+    float *garr;                    // [B, K+1, 2, G] per-group data in global memory
+    unsigned long long *queue;      // [B (K+1) S] second-pass items
+    float *pcand;                   // [B, K+1, S, kSliceCand, 2] residual-bound candidates
+    float *cmax;                    // [B, K+1, pair chunks] largest target maximum per chunk
+    uint32_t *slice_ctr;            // scheduler counters (reset by the last CTA to exit)
 };
 
 // Workspace layout (each region 256-byte aligned).

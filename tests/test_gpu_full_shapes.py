@@ -103,7 +103,7 @@ def round_case():
     return wl, inp, Fo, off, o
 
 
-@pytest.mark.parametrize("policy", [1, 2])  # streaming kernel, cluster kernel
+@pytest.mark.parametrize("policy", [1, 2, 3])  # streaming, cluster, slice kernel
 def test_round_full_shape_fp32(ssd, round_case, policy):
     wl, inp, Fo, off, o = round_case
     F, off_g = ssd.ssd_fanout(wl.K, wl.budget, wl.a_p, wl.r, wl.V)
@@ -113,6 +113,7 @@ def test_round_full_shape_fp32(ssd, round_case, policy):
     with use_dispatch(ssd, policy):
         out = ssd.ssd_round(d["tgt"], d["drf"], d["tokens"], d["uniforms"], d["temperature"],
                             F, wl.budget)
+        assert ssd.ssd_last_kernel() == {1: "stream", 2: "cluster", 3: "slice"}[policy]
         torch.cuda.synchronize()
     g = np_out(out)
     t = Tally()

@@ -27,15 +27,17 @@ pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
 
 
-@pytest.fixture(scope="module")
-def ssd():
+@pytest.fixture(scope="module", params=["stream", "slice"])
+def ssd(request):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     import speculative_decoding_verification_ssd_gb300 as m
     from speculative_decoding_verification_ssd_gb300 import _build
     _build.build()
-    # these batches are small: force the streaming kernel, whose paths they exercise
-    with use_dispatch(m, m.SSD_DISPATCH_STREAM):
+    # these batches are small: force the persistent kernel whose paths they exercise
+    # (the streaming kernel, or the slice kernel, which has the same paths per slice)
+    policy = m.SSD_DISPATCH_STREAM if request.param == "stream" else m.SSD_DISPATCH_SLICE
+    with use_dispatch(m, policy):
         yield m
 
 
@@ -184,7 +186,7 @@ def test_round_reads_inputs_written_just_before_it(ssd):
     rng = np.random.default_rng(5)
     tau_dev = torch.empty_like(d["temperature"])
     u_dev = torch.empty_like(d["uniforms"])
-    ws = ssd.workspace(wl.B, wl.K)
+    ws = ssd.workspace(wl.B, wl.K, V=wl.V, dtype=ssd.SSD_BF16, budget=wl.budget)
     outs, cases = [], []
     for tau_np in (tau_a, tau_b, tau_a):
         u_np = rng.random((wl.B, wl.K + 1), dtype=np.float32)
