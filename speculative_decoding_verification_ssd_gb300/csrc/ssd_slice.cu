@@ -143,12 +143,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) ssd_slice_kernel(const __gr
     constexpr int VPT1 = FULL_PAIR / (kGT / 2), VPTS = GV / TPGS, VPT2 = GV / TPG2;
     constexpr int TPG1 = GV / VPT1;        // pass 1 of a pair: threads per group of one row
     static_assert(VPT1 == 4 && VPTS == 4 && VPT2 == 2, "stage geometry");
-    constexpr int LPG = GV < 32 ? GV : 32;  // tail: lanes per group re-read (one vector each)
-    constexpr int GPI = 32 / LPG;           // tail: groups per warp iteration
-    constexpr int VPL = GV / LPG;           // tail: vectors per lane per group
     constexpr int TPL = kGTok / 32;         // tail: tokens per lane of one group
-    constexpr int kBatch = 2;               // tail: vectors in flight per lane when re-reading
-    static_assert(32 % LPG == 0 && TPL >= 1 && kBatch % VPL == 0, "tail geometry");
+    static_assert(TPL >= 1, "tail geometry");
 
     extern __shared__ __align__(128) unsigned char dyn_smem[];
     __shared__ SGroup gsh[kNG];
@@ -565,35 +561,40 @@ __global__ void __launch_bounds__(kStreamThreads, 1) ssd_slice_kernel(const __gr
             const bool all_groups = ncg > kCandGroupsCap;
             const int ngroups = all_groups ? gn : ncg;
             uint64_t theta = static_cast<uint64_t>(th) << 32;
-            const int sub = lane / LPG, li = lane % LPG;
+            // The candidate groups' vectors are fetched into the scratch with cp.async,
+            // as many groups at a time as it holds, so that a batch costs one round trip.
+            const int nrow = mode == 1 ? 2 : 1;
+            const int gcap = (kSliceScratch * 4) / (GV * 16 * nrow);  // groups per batch
+            unsigned char *const stage = reinterpret_cast<unsigned char *>(scr);
             int count = 0;
             for (int round = 0; round < 64; ++round) {
-                for (int q0 = 0; q0 < ngroups; q0 += kBatch / VPL * GPI) {
-                    uint4 wt[kBatch], wd[kBatch];
-                    int e0[kBatch];
-#pragma unroll
-                    for (int x = 0; x < kBatch; ++x) {
-                        const int q = q0 + (x / VPL) * GPI + sub;
-                        e0[x] = V;
-                        if (q < ngroups) {
-                            const int g = g0 + (all_groups ? q : gs.cgroups[q]);
-                            e0[x] = g * kGTok + ((x % VPL) * LPG + li) * VEC;
-                        }
-                        if (e0[x] < V) {
-                            wt[x] = __ldg(reinterpret_cast<const uint4 *>(trow + static_cast<int64_t>(e0[x]) * EB));
-                            if (mode == 1)
-                                wd[x] = __ldg(reinterpret_cast<const uint4 *>(drow + static_cast<int64_t>(e0[x]) * EB));
+                for (int q0 = 0; q0 < ngroups; q0 += gcap) {
+                    const int nb = min(gcap, ngroups - q0);
+                    for (int v = lane; v < nb * GV * nrow; v += 32) {
+                        const int q = v / (GV * nrow), r = (v / GV) % nrow, j = v % GV;
+                        const int g = g0 + (all_groups ? q0 + q : gs.cgroups[q0 + q]);
+                        const int e = g * kGTok + j * VEC;
+                        if (e < V) {
+                            const unsigned char *src = (r ? drow : trow) + static_cast<int64_t>(e) * EB;
+                            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(stage + 16 * v)),
+                                         "l"(src)
+                                         : "memory");
                         }
                     }
-#pragma unroll
-                    for (int x = 0; x < kBatch; ++x) {
-                        if (e0[x] >= V) continue;
+                    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+                    __syncwarp();
+                    for (int v = lane; v < nb * GV; v += 32) {
+                        const int q = v / GV, j = v % GV;
+                        const int g = g0 + (all_groups ? q0 + q : gs.cgroups[q0 + q]);
+                        const int e0 = g * kGTok + j * VEC;
+                        if (e0 >= V) continue;
                         float zt[VEC], zd[VEC];
-                        decode_vec<D>(wt[x], zt);
-                        if (mode == 1) decode_vec<D>(wd[x], zd);
+                        decode_vec<D>(*reinterpret_cast<const uint4 *>(stage + 16 * ((q * nrow) * GV + j)), zt);
+                        if (mode == 1)
+                            decode_vec<D>(*reinterpret_cast<const uint4 *>(stage + 16 * ((q * nrow + 1) * GV + j)), zd);
 #pragma unroll
                         for (int i = 0; i < VEC; ++i) {
-                            const int e = e0[x] + i;
+                            const int e = e0 + i;
                             uint64_t key;
                             if (mode == 1)
                                 key = make_key(resid_of(zt[i], zd[i], c, nLT, draft_bias(shape, zd[i], e) - LD), e);
@@ -605,6 +606,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) ssd_slice_kernel(const __gr
                             }
                         }
                     }
+                    __syncwarp();
                 }
                 __syncwarp();
                 count = gs.cnt[1];
@@ -654,12 +656,27 @@ __global__ void __launch_bounds__(kStreamThreads, 1) ssd_slice_kernel(const __gr
             int32_t *seg = P.cache_tok + static_cast<int64_t>(b) * P.budget + P.off[k];
             uint64_t best = 0;
             if (n <= kCandCap) {
-                int j = 0;
-                for (int s = 0; s < S; ++s) {
-                    if (!((smask >> s) & 1u)) continue;
-                    const unsigned long long *src = key_area(b, s, k);
-                    for (int i = lane; i < F_list; i += 32) gs.cand[j + i] = __ldcg(src + i);
-                    j += F_list;
+                // key x of the n: list x / F_list (the (x / F_list)-th slice in smask), entry
+                // x % F_list; loaded eight per lane at a time, all in flight together
+                for (int x0 = 0; x0 < n; x0 += 32 * 8) {
+                    unsigned long long kv[8];
+#pragma unroll
+                    for (int y = 0; y < 8; ++y) {
+                        const int x = x0 + 32 * y + lane;
+                        kv[y] = 0ull;
+                        if (x < n) {
+                            int li = x / F_list, s = 0;
+                            uint32_t m = smask;
+                            for (; li > 0; --li) m &= m - 1;  // drop the lists before it
+                            s = __ffs(m) - 1;
+                            kv[y] = __ldcg(key_area(b, s, k) + x % F_list);
+                        }
+                    }
+#pragma unroll
+                    for (int y = 0; y < 8; ++y) {
+                        const int x = x0 + 32 * y + lane;
+                        if (x < n) gs.cand[x] = kv[y];
+                    }
                 }
                 __syncwarp();
                 for (int i = lane; i < n; i += 32) {
@@ -888,12 +905,22 @@ __global__ void __launch_bounds__(kStreamThreads, 1) ssd_slice_kernel(const __gr
         auto finish_pair1 = [&](int b, int k) {
             const int u = unit_of(b, k);
             SliceUnitState *us = P.ustate + u;
+            // every input of the unit requested at once (the logits at x~ one step later)
             int flags = static_cast<int>(__ldcg(&us->flags));
             const float tau = P.temperature[b];
-            const float c = kLog2e / tau;
-            // slice statistics merged in slice order (the same in every CTA)
+            const int xt = P.tokens[static_cast<int64_t>(b) * K + k];
+            const float u_k = P.uniforms ? P.uniforms[static_cast<int64_t>(b) * (K + 1) + k] : 0.f;
+            ssd_reshape_desc rdesc{0.f, 0, 0, 1.f};
+            if (P.reshape) rdesc = P.reshape[static_cast<int64_t>(b) * K + k];
             float4 st4 = make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
             if (lane < S) st4 = __ldcg(P.sstat + static_cast<int64_t>(u) * S + lane);
+            const unsigned char *trow = row_ptr(P.tgt, P.tgt_seq_stride, b, k);
+            const unsigned char *drow = row_ptr(P.drf, P.drf_seq_stride, b, k);
+            const bool xt_ok = xt >= 0 && xt < V;
+            const float ztx = xt_ok ? load_logit<D>(trow, xt) : 0.f;
+            const float zdx = xt_ok ? load_logit<D>(drow, xt) : 0.f;
+            const float c = kLog2e / tau;
+            // slice statistics merged in slice order (the same in every CTA)
             Stat gT{-INFINITY, 0.f}, gD{-INFINITY, 0.f};
             for (int s = 0; s < S; ++s) {
                 const Stat a{__shfl_sync(kFull, st4.x, s), __shfl_sync(kFull, st4.y, s)};
@@ -914,18 +941,12 @@ __global__ void __launch_bounds__(kStreamThreads, 1) ssd_slice_kernel(const __gr
             float cthr = -INFINITY, LT = 0.f, LD = 0.f;
             bool need_bonus = false;
             if (!skipped && flags == 0) {
-                const int xt = P.tokens[static_cast<int64_t>(b) * K + k];
-                const unsigned char *trow = row_ptr(P.tgt, P.tgt_seq_stride, b, k);
-                const unsigned char *drow = row_ptr(P.drf, P.drf_seq_stride, b, k);
-                const float ztx = load_logit<D>(trow, xt), zdx = load_logit<D>(drow, xt);
-                const float u_k = P.uniforms ? P.uniforms[static_cast<int64_t>(b) * (K + 1) + k] : 0.f;
                 DraftShape shape{0, 0.f, 0, 0.f};
                 if (P.reshape) {
-                    const ssd_reshape_desc dd = P.reshape[static_cast<int64_t>(b) * K + k];
-                    shape.on = dd.F > 0;
-                    shape.thr = dd.thr_val;
-                    shape.thr_id = dd.thr_id;
-                    shape.l2C = dd.C > 0.f ? (dd.C == 1.f ? 0.f : lg2(dd.C)) : -INFINITY;
+                    shape.on = rdesc.F > 0;
+                    shape.thr = rdesc.thr_val;
+                    shape.thr_id = rdesc.thr_id;
+                    shape.l2C = rdesc.C > 0.f ? (rdesc.C == 1.f ? 0.f : lg2(rdesc.C)) : -INFINITY;
                 }
                 LT = gT.m + lg2(gT.S);
                 LD = gD.m + lg2(gD.S);
@@ -966,17 +987,32 @@ __global__ void __launch_bounds__(kStreamThreads, 1) ssd_slice_kernel(const __gr
                         }
                     }
                     __syncwarp();
-                    // largest th with at least F candidates at or above it (ordered bits)
-                    uint32_t lo = 0, hi = 0xFFFFFFFFu;
-                    while (lo < hi) {
-                        const uint32_t mid = lo + ((hi - lo) >> 1) + 1;
-                        int cnt = 0;
-                        for (int i = lane; i < nc; i += 32) cnt += ordered_bits(lbs[i]) >= mid;
-                        cnt = __reduce_add_sync(kFull, cnt);
-                        if (cnt >= F)
-                            lo = mid;
-                        else
-                            hi = mid - 1;
+                    // the F-th largest candidate: F rounds of a warp maximum over the lanes'
+                    // best remaining candidates (the winner takes its next one)
+                    uint32_t lo = 0;
+                    if (F <= nc) {
+                        uint32_t bv = 0;
+                        int bi = -1;
+                        auto lane_best = [&]() {
+                            bv = 0;
+                            bi = -1;
+                            for (int i = lane; i < nc; i += 32) {
+                                const uint32_t o = ordered_bits(lbs[i]);
+                                if (o > bv) {
+                                    bv = o;
+                                    bi = i;
+                                }
+                            }
+                        };
+                        lane_best();
+                        for (int it = 0; it < F; ++it) {
+                            lo = __reduce_max_sync(kFull, bv);
+                            const uint32_t who = __ballot_sync(kFull, bv == lo && bi >= 0);
+                            if (who && lane == __ffs(who) - 1) {
+                                lbs[bi] = -INFINITY;
+                                lane_best();
+                            }
+                        }
                     }
                     __syncwarp();
                     const float tv = value_of_ordered(lo);
@@ -1015,7 +1051,11 @@ __global__ void __launch_bounds__(kStreamThreads, 1) ssd_slice_kernel(const __gr
             }
             __threadfence();
             __syncwarp();
-            // queue the second pass, one item per slice with chunks to stream
+            // queue the second pass, one item per slice with chunks to stream (the slots
+            // taken with one atomic add)
+            uint32_t qbase = 0;
+            if (lane == 0 && nq > 0) qbase = atomicAdd(P.slice_ctr + kCtrQAlloc, static_cast<uint32_t>(nq));
+            qbase = __shfl_sync(kFull, qbase, 0);
             if (lane < S && ((smask >> lane) & 1u)) {
                 const int s = lane;
                 const int c0 = 2 * slice_block0(s, S, nblk);
@@ -1023,7 +1063,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) ssd_slice_kernel(const __gr
                 uint32_t m = 0;
                 for (int pc = c0; pc < c1; ++pc)
                     if ((row_chunks[pc >> 5] >> (pc & 31)) & 1u) m |= 1u << (pc - c0);
-                const uint32_t idx = atomicAdd(P.slice_ctr + kCtrQAlloc, 1u);
+                const uint32_t idx = qbase + static_cast<uint32_t>(__popc(smask & ((1u << s) - 1u)));
                 const unsigned long long e = (static_cast<unsigned long long>(m) << 32) |
                                              static_cast<unsigned long long>(static_cast<uint32_t>(u) * S + s + 1u);
                 atomicExch(P.queue + idx, e);
@@ -1038,6 +1078,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1) ssd_slice_kernel(const __gr
         auto finish_pair2 = [&](int b, int k) {
             const int u = unit_of(b, k);
             SliceUnitState *us = P.ustate + u;
+            // the slices' residual masses and the bonus uniform, requested with the state
+            const float zs = lane < S ? __ldcg(&P.sstat[static_cast<int64_t>(u) * S + lane].x) : 0.f;
+            const float uK = P.uniforms ? P.uniforms[static_cast<int64_t>(b) * (K + 1) + K] : 0.f;
             UnitRecord rec{};
             rec.accept = __ldcg(&us->accept);
             rec.p_tok = __ldcg(&us->p_tok);
@@ -1060,8 +1103,6 @@ __global__ void __launch_bounds__(kStreamThreads, 1) ssd_slice_kernel(const __gr
                     shape.thr_id = dd.thr_id;
                     shape.l2C = dd.C > 0.f ? (dd.C == 1.f ? 0.f : lg2(dd.C)) : -INFINITY;
                 }
-                const float uK = P.uniforms[static_cast<int64_t>(b) * (K + 1) + K];
-                const float zs = lane < S ? __ldcg(&P.sstat[static_cast<int64_t>(u) * S + lane].x) : 0.f;
                 float Z = zs;
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) Z += __shfl_xor_sync(kFull, Z, o);
