@@ -36,8 +36,9 @@
  *   - draft-only cache keys: raw draft logits of row k (of K+1 draft rows), the
  *     drafted token left out for k < K; the reshape at position k uses F = F_k.
  * Parity unpinned: the pages print no value that fixes which uniform draws the
- * bonus, the CDF order and boundary, or the Z == 0 fallback; for those three
- * readings the pins can only check internal consistency.
+ * bonus or the CDF order and boundary; for those two readings the pins can only
+ * check internal consistency.  The Z == 0 fallback is pinned against the p_a it
+ * reduces to (its draw and its hit probability), though no page value fixes it.
  */
 #include <math.h>
 #include <stdint.h>
