@@ -327,8 +327,11 @@ int ssd_round_ld(const void *tgt, const void *drf, int dtype, int B, int K, int 
  * and F_k >= V).  desc_out [B, K] (device, required) receives the
  * descriptor found for every position of every sampled sequence (the same
  * set ssd_reshape_draft gives with F = F_k); entries of greedy sequences,
- * and of sequences flagged invalid, may be left untouched.  Everything else
- * as ssd_verify / ssd_round with reshape = the descriptors found.
+ * and of sequences flagged invalid, may be left untouched, and so may, in
+ * ssd_verify_sigma, the positions after a sequence's accepted length (their
+ * rows are not needed once an earlier position rejected, and may be skipped).
+ * Everything else as ssd_verify / ssd_round with reshape = the descriptors
+ * found.
  * When the rows do not suit the streaming kernel (a row not on a 16-byte
  * boundary, or V too large for its shared memory) the descriptors are found
  * by a separate pass over the draft rows first.

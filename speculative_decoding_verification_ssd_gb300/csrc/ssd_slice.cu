@@ -957,6 +957,14 @@ __global__ void __launch_bounds__(kStreamThreads, 1) ssd_slice_kernel(const __gr
                 rec.q_tok = q_tok;
                 rec.accept = accept;
                 need_bonus = do_verify && !accept;
+                // verification alone: publish the rejection now (units of the sequence not yet
+                // started skip their rows); after an earlier rejection no residual is needed
+                if (need_bonus && (P.mode & kModeEarlyExit) && k < 32) {
+                    uint32_t old = 0;
+                    if (lane == 0) old = atomicOr(P.seq_reject + b, 1u << k);
+                    old = __shfl_sync(kFull, old, 0);
+                    if (old & ((1u << k) - 1u)) need_bonus = false;
+                }
                 const bool need_cache = do_cache && P.F[k] > 0;
                 if (need_bonus) {
                     row_chunks[0] = row_chunks[1] = row_chunks[2] = 0xFFFFFFFFu;
@@ -1047,7 +1055,6 @@ __global__ void __launch_bounds__(kStreamThreads, 1) ssd_slice_kernel(const __gr
                 us->accept = accept;
                 us->slice_mask = smask;
                 us->p2_expect = static_cast<uint32_t>(nq);
-                if (need_bonus && (P.mode & kModeEarlyExit)) atomicOr(P.seq_reject + b, 1u << k);
             }
             __threadfence();
             __syncwarp();

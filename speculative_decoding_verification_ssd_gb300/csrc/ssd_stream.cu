@@ -93,7 +93,8 @@ struct __align__(16) Hdr {
 // A finished unit's hand-off from a consumer group to its tail warp.
 struct TailDesc {
     int kind, b, k, flags;
-    int state, accept, xt, pad0;
+    int state, accept, xt;
+    int notfirst;  // pair: rejected after an earlier rejection of the sequence (bonus unused)
     float c;       // log2 e / tau
     float M, S;    // sampled single row: target statistics (base 2)
     float LT, LD;  // pair: normalisers (base 2)
@@ -894,8 +895,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             if (d.kind == kKindPair) {
                 if (Fk > 0) top_f(true);
                 // the bonus at k is drawn only where k rejected (the second pass left
-                // every residual mass only there)
-                if (do_verify && !d.accept) {
+                // every residual mass only there), and not after an earlier rejection
+                if (do_verify && !d.accept && !d.notfirst) {
                     float zs = 0.f;
                     for (int g = g0; g < g1; ++g) zs += gsum[g];
                     const float Z = warp_sum(zs);
@@ -1078,6 +1079,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     int b = 0, k = 0, flags = 0, xt = -1, xmask = -1;
     bool sampled = false, pair = false, active = false, want_p2 = false, sig = false;
     bool bnd = false;      // a pair that builds a cache: pass 1 keeps both rows' group maxima
+    bool notfirst = false;  // thread 0: a rejection after an earlier one of the sequence (verification alone)
     float cthr = -INFINITY;  // pass 2: residuals of the groups whose upper bound reaches this only
     const int nch_pair = static_cast<int>((row_bytes + HALF - 1) / HALF);  // chunks of a pair pass
     float c = 0.f, LT = 0.f, LD = 0.f;
@@ -1106,6 +1108,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             D0.state = state;
             D0.accept = accept;
             D0.xt = xt;
+            D0.notfirst = notfirst ? 1 : 0;
             D0.c = c;
             D0.M = M;
             D0.S = Ssum;
@@ -1159,6 +1162,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             want_p2 = pair && (do_verify || (do_cache && P.F[k] > 0));
             bnd = pair && do_cache && P.F[k] > 0;
             cthr = -INFINITY;
+            notfirst = false;
             c = sampled ? kLog2e / tau : 0.f;
             shape = DraftShape{0, 0.f, 0, 0.f};
             sig = kSig && pair && P.sig_F[k] > 0;
@@ -1402,9 +1406,19 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                     cthr = tv > 0.f ? tv : -INFINITY;  // no positive bound: every group
                 }
             }
+            // Verification alone: a rejection publishes its bit now (units of the sequence
+            // not yet started skip their rows), and one after an earlier rejection of the
+            // sequence needs no residual (only the first rejection's bonus is used).
+            if (t == 0 && do_verify && !accept && (P.mode & kModeEarlyExit) && k < 32) {
+                const uint32_t old = atomicOr(P.seq_reject + b, 1u << k);
+                notfirst = (old & ((1u << k) - 1u)) != 0u;
+            }
             if (gated) {
                 if (cthr == -INFINITY) {
-                    list_chunks(0xFFFFFFFFu);  // every chunk
+                    if (t == 0 && notfirst)
+#pragma unroll
+                        for (int w = 0; w < kDecWords; ++w) gs.dec_mask[w] = 0u;
+                    list_chunks(notfirst ? 0u : 0xFFFFFFFFu);  // every chunk, or none
                 } else {
                     // the chunks holding a group whose bound reaches cthr; every other
                     // group's largest residual reads as 0 (its chunk may not be streamed)

@@ -66,13 +66,17 @@ def test_sigma_verify_full_shape(ssd, sigma_case, policy):
                                  d["temperature"], [wl.reshape_F] * wl.K, wl.reshape_C)
         torch.cuda.synchronize()
     desc = g.pop("desc")
+    gn = np_out(g)
     t = Tally()
-    compare_verify(np_out(g), o, wl.K, t)
+    compare_verify(gn, o, wl.K, t)
     t.check()
-    # descriptors: the F-th largest raw logit (value, id) of every draft row
+    # descriptors: the F-th largest raw logit (value, id) of every verified draft row
+    # (positions after the accepted length may be skipped, their entries untouched)
     thr_val, thr_id, Fd, _ = [x.cpu().numpy().reshape(-1) for x in ssd.desc_fields(desc)]
     drf32 = synth.stored_to_f32(inp["drf"], wl.dtype).reshape(-1, wl.V)
-    rows = np.random.default_rng(3).choice(drf32.shape[0], 48, replace=False)
+    a = gn["accept_len"]
+    verified = np.array([r for r in range(drf32.shape[0]) if r % wl.K <= a[r // wl.K]])
+    rows = np.random.default_rng(3).choice(verified, min(48, len(verified)), replace=False)
     for r in rows:
         ids = oracle.topf(drf32[r].astype(np.float64), wl.reshape_F)
         assert thr_id[r] == ids[-1] and thr_val[r] == drf32[r, ids[-1]]

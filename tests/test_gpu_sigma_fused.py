@@ -80,17 +80,19 @@ def test_verify_sigma_matches_oracle(ssd, dtype, V, C, peaked):
     g = ssd.ssd_verify_sigma(_dev_logits(tgt, dtype), dd, torch.from_numpy(tok).cuda(),
                              torch.from_numpy(u).cuda(), torch.from_numpy(tau).cuda(), F, C)
     desc = g.pop("desc")
+    gn = np_out(g)
     o = oracle.verify(tgt, drf, tok, u, tau, dtype, reshape_F=F, reshape_C=C)
     t = Tally()
-    compare_verify(np_out(g), o, K, t)
+    compare_verify(gn, o, K, t)
     t.check()
-    # the descriptors of the sampled sequences equal the draft side's
+    # the descriptors of the sampled sequences' verified positions (up to the accepted
+    # length; later ones may be skipped) equal the draft side's
     pad = np.concatenate([drf, drf[:, :1]], axis=1)  # a row K for ssd_draft_cache's layout
     _, ref = ssd.ssd_draft_cache(_dev_logits(pad, dtype), None, F + [0], sum(F), C, cache=False,
                                  reshape=True)
     got, want = desc.cpu().numpy().reshape(B, K, 4), ref.cpu().numpy().reshape(B, K, 4)
-    sampled = tau > 0
-    np.testing.assert_array_equal(got[sampled], want[sampled])
+    verified = (tau > 0)[:, None] & (np.arange(K)[None, :] <= gn["accept_len"][:, None])
+    np.testing.assert_array_equal(got[verified], want[verified])
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
