@@ -104,19 +104,26 @@ typedef struct ssd_reshape_desc {
 } ssd_reshape_desc;
 
 /* Kernel choice for rows on the 16-byte grid (process-wide; rows off the grid
- * always take the cluster kernel).  AUTO: the persistent streaming kernel when
- * the batch has at least as many units (sequences x (K+1)) as the GPU has SMs,
- * or when sigma_{F,C} is found in the pass, else the cluster kernel, which
- * splits each row across a thread-block cluster.  STREAM / CLUSTER / SLICE force
+ * always take the cluster kernel).  AUTO: for verification alone, the persistent
+ * streaming kernel in its wide form (below); otherwise the streaming kernel when
+ * the batch has at least as many units (sequences x (K+1)) as the GPU has SMs --
+ * in its wide form below twice as many -- or when sigma_{F,C} is found in the
+ * pass, else the cluster kernel, which splits each row across a thread-block
+ * cluster.  STREAM / CLUSTER / SLICE force
  * one.  SLICE, the slice kernel, splits every row into slices of 16 KB blocks
  * that the whole GPU works on at once and combines the slices' partial results
  * in the workspace; it applies to rows of whole 16-byte vectors (V a multiple of
  * the vector), without sigma found in the pass, B <= 2048 and a workspace of
- * ssd_workspace_size_v bytes; other calls fall back as under AUTO. */
+ * ssd_workspace_size_v bytes; other calls fall back as under AUTO.  WIDE forces
+ * the streaming kernel in its wide form, where both consumer groups of a CTA
+ * work on each unit (half the units in flight, each at about twice the rate),
+ * for rows of whole 16-byte vectors (V a multiple of the vector); other calls
+ * fall back as under AUTO. */
 #define SSD_DISPATCH_AUTO 0
 #define SSD_DISPATCH_STREAM 1
 #define SSD_DISPATCH_CLUSTER 2
 #define SSD_DISPATCH_SLICE 3
+#define SSD_DISPATCH_WIDE 4
 
 /* Sets the kernel choice; returns the previous one, or -1 (and changes nothing)
  * for an unknown policy.  Calls already enqueued are not affected. */
@@ -124,6 +131,7 @@ int ssd_set_dispatch(int policy);
 
 /* Name of the kernel that the most recent verify / cache / round call made on
  * the calling host thread launched ("stream" -- the persistent streaming kernel,
+ * "stream-wide" -- the same kernel in its wide form,
  * "slice" -- the slice kernel, "cluster" -- the cluster kernel, "reshape+cluster"
  * -- the reshape kernel and then the cluster kernel for sigma found before the
  * pass), or "none" before any such call.  Plumbing for reporting (no counterpart on the pages); the string is

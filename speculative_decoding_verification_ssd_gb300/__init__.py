@@ -123,7 +123,7 @@ def lib() -> ctypes.CDLL:
     return _lib
 
 
-SSD_DISPATCH_AUTO, SSD_DISPATCH_STREAM, SSD_DISPATCH_CLUSTER, SSD_DISPATCH_SLICE = 0, 1, 2, 3
+SSD_DISPATCH_AUTO, SSD_DISPATCH_STREAM, SSD_DISPATCH_CLUSTER, SSD_DISPATCH_SLICE, SSD_DISPATCH_WIDE = 0, 1, 2, 3, 4
 
 
 def ssd_set_dispatch(policy: int) -> int:

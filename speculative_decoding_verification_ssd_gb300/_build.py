@@ -21,7 +21,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libssd.so")
 
-SOURCES = ["ssd_unit.cu", "ssd_stream.cu", "ssd_slice.cu", "ssd_reshape.cu", "ssd_api.cu", "ssd_fanout.cpp", "ssd_backup.cu",
+SOURCES = ["ssd_unit.cu", "ssd_stream.cu", "ssd_stream_wide.cu", "ssd_slice.cu", "ssd_reshape.cu", "ssd_api.cu", "ssd_fanout.cpp", "ssd_backup.cu",
            "ssd_diag.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -199,7 +199,14 @@ int run_units(int mode, const void *tgt, const void *drf, int dtype, int B, int 
                            sdyn <= dv->max_dyn[dtype == SSD_F32 ? 4 : 5];
     // With fewer units than SMs the persistent kernel leaves SMs idle and each unit
     // streams at one group's share of an SM; the cluster kernel splits every row
-    // across a cluster instead (c2: 8 sequences, K = 5: 38.5 us against 58.7).
+    // across a cluster instead (c2: 8 sequences, K = 5: 38.5 us against 58.7), and
+    // so does the streaming kernel's wide form, which puts both consumer groups of
+    // a CTA on each unit.  The wide form pays wherever few units reach a second
+    // pass -- verification alone, where only a sequence's first rejection streams
+    // its rows again (c3: 84.0 against 103.2 us, c2: 38.5 against 39.2 on the
+    // cluster kernel) -- and where a cache build has fewer than two units per SM
+    // (c4: 115.0 against 119.4); a cache build with more keeps two units per SM, so
+    // that one unit's second pass (L2 reads) overlaps the other's first (HBM).
     const int policy = g_dispatch.load(std::memory_order_relaxed);
     // The slice kernel (rows split into slices scheduled over every SM) needs rows of
     // whole vectors, its own workspace regions and a batch it can order by kind.
@@ -209,8 +216,12 @@ int run_units(int mode, const void *tgt, const void *drf, int dtype, int B, int 
                           ssd::slice_pair_chunks(V, elem) <= 96 &&
                           workspace_bytes >= SW.total && ssd::slice_dyn_bytes() <= dv->max_dyn[dtype == SSD_F32 ? 6 : 7];
     const bool sliced = slice_ok && policy == SSD_DISPATCH_SLICE;
+    const bool wide = !sliced && stream_ok && V % (16 / elem) == 0 &&
+                      (policy == SSD_DISPATCH_WIDE ||
+                       (policy == SSD_DISPATCH_AUTO &&
+                        ((verify && !cache) || (units >= dv->sm_count && units < 2 * dv->sm_count))));
     const bool streaming = !sliced && stream_ok && policy != SSD_DISPATCH_CLUSTER &&
-                           (policy == SSD_DISPATCH_STREAM || sig_F != nullptr || units >= dv->sm_count);
+                           (wide || policy == SSD_DISPATCH_STREAM || sig_F != nullptr || units >= dv->sm_count);
     Geometry g;
     if (!streaming && !sliced) {
         st = choose_geometry(V, elem, 2, units, *dv, dv->max_dyn[dtype == SSD_F32 ? 0 : 1], &g);
@@ -282,7 +293,8 @@ int run_units(int mode, const void *tgt, const void *drf, int dtype, int B, int 
             P.desc_out = desc_out;
         }
         const int grid = std::min(dv->sm_count, units);
-        t_last_kernel = "stream";
+        P.wide = wide ? 1 : 0;
+        t_last_kernel = wide ? "stream-wide" : "stream";
         return ssd::stream_launch(dtype, P, grid, sdyn, stream);
     }
     if (sig_F) {
@@ -335,7 +347,7 @@ const char *ssd_last_kernel(void) { return t_last_kernel; }
 
 int ssd_set_dispatch(int policy) {
     if (policy != SSD_DISPATCH_AUTO && policy != SSD_DISPATCH_STREAM && policy != SSD_DISPATCH_CLUSTER &&
-        policy != SSD_DISPATCH_SLICE)
+        policy != SSD_DISPATCH_SLICE && policy != SSD_DISPATCH_WIDE)
         return -1;
     return g_dispatch.exchange(policy);
 }

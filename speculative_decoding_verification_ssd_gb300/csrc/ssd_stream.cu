@@ -275,8 +275,10 @@ __device__ __noinline__ SigResult sigma_fuse(const unsigned char *drow, const fl
 
 // kSig: sigma_{F,C} found in the pass.  kTail: rows are not whole 16-byte
 // vectors (a row stride longer than V), so each row's last vector is masked; the
-// common form carries none of that code.
-template <class D, bool kSig, bool kTail>
+// common form carries none of that code.  kWide: both consumer groups work on
+// each unit (instantiated in its own translation unit, ssd_stream_wide.cu, for
+// rows of whole vectors; the one-group forms carry none of its code).
+template <class D, bool kSig, bool kTail, bool kWide>
 __global__ void __launch_bounds__(kStreamThreads, 1)
     ssd_stream_kernel(const __grid_constant__ UnitParams P) {
     constexpr int VEC = D::kVec, S = D::kBytes;
@@ -304,6 +306,13 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     __shared__ GroupShared gsh[kNG];
     __shared__ int s_abort;
     __shared__ int s_nS;
+    __shared__ uint64_t s_ubar;  // wide: one arrival per consumer group at each shared step of a unit
+    // wide: what group 0 finds between a pair's passes, for group 1
+    __shared__ struct {
+        float cthr, LD;
+        DraftShape shape;
+    } s_pub;
+    __shared__ float s_wscr[kGW];  // wide: group 0's scratch for the fused sigma selection
     __shared__ int s_cnt[kSchedCap / 32];
     __shared__ uint16_t sched[kSchedCap];  // sampled sequences, then the others
 
@@ -334,6 +343,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             }
             mbar_init(&gsh[g].dec_bar, 1);
         }
+        mbar_init(&s_ubar, kNG);
         s_abort = 0;
         s_nS = 0;
         fence_mbar_init();
@@ -399,6 +409,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     if (warp >= kProducerWarp0 && warp < kTailWarp0) {
         if (lane != 0) return;
         const int rg = warp - kProducerWarp0;  // ring served by this producer
+        if (kWide && rg == 1) return;          // wide: producer 0 serves both rings
         GroupShared &gq = gsh[rg];
         unsigned char *ring = dyn_smem + rg * kRS * kSB;
         const uint64_t pol = policy_evict_first();
@@ -463,6 +474,115 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         uint32_t n = 0;     // stages pushed
         uint32_t ndec = 0;  // second-pass chunk lists received
         bool ok = true;
+        if (kWide) {
+            // Both consumer groups share each unit: its chunk stages alternate between
+            // ring 0 and ring 1 (every pass puts its last chunk on each ring with the
+            // end bit, or a header-only end stage on a ring that got no chunk), and a
+            // second pass longer than both rings follows group 0's chunk list.
+            uint32_t nr1 = 0;  // stages pushed to ring 1 (n counts ring 0's)
+            auto push = [&](int r, Hdr hd, const unsigned char *src_t, const unsigned char *src_d,
+                            uint32_t bytes) -> bool {
+                const uint32_t nn = r ? nr1 : n;
+                const int s = static_cast<int>(nn % kRS);
+                if (!mbar_wait_suspend(&gsh[r].empty_bar[s], ((nn / kRS) & 1) ^ 1)) return false;
+                gsh[r].hdr[s] = hd;
+                unsigned char *dst = dyn_smem + (r * kRS + s) * kSB;
+                mbar_arrive_expect_tx(&gsh[r].full_bar[s], src_t ? bytes * (src_d ? 2u : 1u) : 0u);
+                if (src_t) {
+                    bulk_copy_hint(dst, src_t, bytes, &gsh[r].full_bar[s], pol);
+                    if (src_d) bulk_copy_hint(dst + HALF, src_d, bytes, &gsh[r].full_bar[s], pol);
+                }
+                if (r) ++nr1; else ++n;
+                return true;
+            };
+            for (;;) {
+                while (pf_state < 2) pf_step();
+                pf_state = 0;
+                const int u = pf_u;
+                if (u >= nunits) {
+                    const Hdr stop{-1, kPassStop | (1 << 4), 0, 0, 0, 0, 0, 0};
+                    ok = push(0, stop, nullptr, nullptr, 0) && push(1, stop, nullptr, nullptr, 0);
+                    break;
+                }
+                const int b = pf_b, k = pf_k;
+                const float tau = pf_tau;
+                const bool sampled = (tau > 0.f) && (tau < INFINITY);
+                const bool pair = sampled && k < K;
+                const bool p2 = pair && (do_verify || (do_cache && P.F[k] > 0));
+                const uint32_t mask = (k >= 32) ? 0xFFFFFFFFu : ((1u << k) - 1u);
+                if ((P.mode & kModeEarlyExit) && k > 0 && (pf_rej & mask) != 0) {
+                    const Hdr sk{u, kPassSkip | (1 << 4), 0, 0, b, k, 0, 0};
+                    ok = push(0, sk, nullptr, nullptr, 0) && push(1, sk, nullptr, nullptr, 0);
+                    if (!ok) break;
+                    continue;
+                }
+                const unsigned char *trow = static_cast<const unsigned char *>(P.tgt) +
+                                            (static_cast<int64_t>(b) * P.tgt_seq_stride + static_cast<int64_t>(k) * P.ld) * S;
+                const unsigned char *drow =
+                    pair ? static_cast<const unsigned char *>(P.drf) +
+                               (static_cast<int64_t>(b) * P.drf_seq_stride + static_cast<int64_t>(k) * P.ld) * S
+                         : nullptr;
+                const int cb = pair ? HALF : kSB;
+                const int nch = static_cast<int>((row_bytes + cb - 1) / cb);
+                const int pbit = (pair ? 1 : 0) << 5;
+                auto chunk_stage = [&](int r, int pass, int chunk, bool last) -> bool {
+                    const int64_t off = static_cast<int64_t>(chunk) * cb;
+                    const uint32_t bytes = static_cast<uint32_t>(row_bytes - off < cb ? row_bytes - off : cb);
+                    const Hdr hd{u, pass | ((last ? 1 : 0) << 4) | pbit, chunk, static_cast<int>(bytes / 16), b, k, 0, 0};
+                    return push(r, hd, trow + off, drow ? drow + off : nullptr, bytes);
+                };
+                auto end_stage = [&](int r, int pass) -> bool {
+                    const Hdr hd{u, pass | (1 << 4) | pbit, -1, 0, b, k, 0, 0};
+                    return push(r, hd, nullptr, nullptr, 0);
+                };
+                for (int c = 0; c < nch && ok; ++c) {
+                    ok = chunk_stage(c & 1, kPassStats, c, c >= nch - 2);
+                    if (!p2 && nch - c <= 3) pf_step();
+                }
+                if (ok && nch == 1) ok = end_stage(1, kPassStats);
+                if (ok && p2) {
+                    // from the row's end back to its start, as in the one-ring form
+                    if (nch <= 2 * kRS) {
+                        for (int i = 0; i < nch && ok; ++i) {
+                            ok = chunk_stage(i & 1, kPassResid, nch - 1 - i, i >= nch - 2);
+                            if (nch - i <= 3) pf_step();
+                        }
+                        if (ok && nch == 1) ok = end_stage(1, kPassResid);
+                    } else {
+                        for (int i = 0; i < 2 * kRS && ok; ++i) ok = chunk_stage(i & 1, kPassResid, nch - 1 - i, false);
+                        if (ok) ok = mbar_wait_suspend(&gsh[0].dec_bar, ndec & 1);
+                        if (ok) {
+                            ++ndec;
+                            const int lim = nch - 2 * kRS;  // chunks [0, lim) stream only when listed
+                            const volatile uint32_t *dm = gsh[0].dec_mask;
+                            int L = 0;
+                            for (int w = 0; w * 32 < lim; ++w) {
+                                uint32_t m = dm[w];
+                                if (lim - w * 32 < 32) m &= (1u << (lim - w * 32)) - 1u;
+                                L += __popc(m);
+                            }
+                            // the next unit is claimed near this one's end (not before the
+                            // accept test: a rejected pair's long pass would hold it back)
+                            int idx = 0;
+                            for (int c = lim - 1; c >= 0 && ok; --c) {
+                                if (!((dm[c >> 5] >> (c & 31)) & 1u)) continue;
+                                ok = chunk_stage(idx & 1, kPassResid, c, idx >= L - 2);
+                                ++idx;
+                                if (L - idx <= 3) pf_step();
+                            }
+                            for (int r = L; r < 2 && ok; ++r) ok = end_stage(r, kPassResid);
+                            pf_step();
+                        }
+                    }
+                }
+                if (!ok) break;
+            }
+            if (!ok) {
+                atomicOr(&s_abort, 1);
+                if (P.dev_status) atomicOr(P.dev_status, SSD_DEV_TIMEOUT);
+            }
+            return;
+        }
         for (;;) {
             while (pf_state < 2) pf_step();
             pf_state = 0;
@@ -1059,7 +1179,17 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     const int bar_id = 1 + grp;
     auto gbar = [&]() { asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "r"(kGT) : "memory"); };
     unsigned char *const ring = dyn_smem + grp * kRS * kSB;
-    float *const arrays = reinterpret_cast<float *>(dyn_smem + kNG * kRS * kSB) + grp * kNBuf * 2 * Gp;
+    float *const abase = reinterpret_cast<float *>(dyn_smem + kNG * kRS * kSB);
+    float *const arrays = abase + grp * kNBuf * 2 * Gp;
+    // Wide form: both groups take every unit (alternate chunks from their rings) and
+    // write one set of group arrays; unit j goes to tail warp j % 2, buffer (j / 2) % 2.
+    // The steps they share meet at s_ubar (a bounded wait), group 0 alone finds the
+    // top-F bound and the chunk list, and group 0's thread 0 hands the unit off.
+    constexpr bool wide = kWide;
+    static_assert(kNG == 2 && kNBuf == 2, "wide unit hand-off");
+    const bool lead = t == 0 && (!wide || grp == 0);
+    uint32_t nub = 0;  // wide: s_ubar phases passed
+    int u_team = grp, u_buf = 0;  // tail warp and buffer of the current unit
     // fused sigma: candidate keys after the group arrays (present only when P.sig_on)
     uint64_t *const sig_keys =
         reinterpret_cast<uint64_t *>(dyn_smem + kNG * kRS * kSB + static_cast<size_t>(kNG) * kNBuf * 2 * Gp * 4) +
@@ -1096,11 +1226,26 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     float ztx = 0.f, zdx = 0.f, u_k = 0.f, p_tok = NAN, q_tok = NAN;
     int accept = 0;
 
+    // the unit's shared steps: the group's barrier, and in the wide form both groups'
+    // (bounded: a group that gave up on its ring cannot hold the other one forever)
+    auto usync = [&]() {
+        gbar();
+        if (!wide) return;
+        if (t == 0) {
+            __threadfence_block();
+            mbar_arrive(&s_ubar);
+        }
+        if (!mbar_wait_suspend(&s_ubar, nub & 1)) {
+            atomicOr(&s_abort, 1);
+            if (t == 0 && P.dev_status) atomicOr(P.dev_status, SSD_DEV_TIMEOUT);
+        }
+        ++nub;
+    };
     // hands the unit to the tail warp (the barrier orders every thread's array writes first)
     auto handoff = [&](int hk, int state, float M, float Ssum) {
-        gbar();
-        if (t == 0) {
-            TailDesc &D0 = gs.desc[nho % kNBuf];
+        usync();
+        if (lead) {
+            TailDesc &D0 = gsh[u_team].desc[u_buf];
             D0.kind = hk;
             D0.b = b;
             D0.k = k;
@@ -1119,7 +1264,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             D0.ztx = ztx;
             D0.shape = shape;
             D0.tlo = (hk == kKindPair && cthr > 0.f && cthr < INFINITY) ? cthr : -INFINITY;
-            mbar_arrive(&gs.tail_full[nho % kNBuf]);
+            mbar_arrive(&gsh[u_team].tail_full[u_buf]);
         }
         ++nho;
     };
@@ -1136,7 +1281,10 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         if (pass == kPassStop) break;
         if (h.unit != cur) {
             // a new unit: wait for its group-array buffer, then per-unit constants
-            if (!mbar_wait_suspend(&gs.tail_empty[nho % kNBuf], ((nho / kNBuf) & 1) ^ 1)) {
+            u_team = wide ? static_cast<int>(nho & 1) : grp;
+            u_buf = static_cast<int>(wide ? (nho >> 1) & 1 : nho % kNBuf);
+            const uint32_t upar = wide ? (nho >> 2) & 1 : (nho / kNBuf) & 1;
+            if (!mbar_wait_suspend(&gsh[u_team].tail_empty[u_buf], upar ^ 1)) {
                 atomicOr(&s_abort, 1);
                 if (t == 0 && P.dev_status) atomicOr(P.dev_status, SSD_DEV_TIMEOUT);
                 break;
@@ -1144,7 +1292,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             cur = h.unit;
             k = h.k;
             b = h.b;
-            gmax = arrays + (nho % kNBuf) * 2 * Gp;
+            gmax = abase + (u_team * kNBuf + u_buf) * 2 * Gp;
             gsum = gmax + Gp;
             const float tau = P.temperature[b];
             const bool tau_ok = (tau >= 0.f) && (tau < INFINITY);
@@ -1204,8 +1352,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         // the stage holding a row's partial last vector (row stride longer than V)
         const bool part = vtail != 0 && h.chunk * (stage_pair ? FULL_PAIR : FULL_ONE) + h.nvec == nvec_row;
         const int pv = part ? h.nvec - 1 : -1;
-        // ---- stage processing -----------------------------------------------
-        if (active) {
+        // ---- stage processing (a header-only stage just ends a pass) -----------
+        if (active && h.nvec > 0) {
             if (pass == kPassStats && stage_pair) {
                 // online statistics: threads [0, 128) target, the rest draft
                 uint4 w[VPT1];
@@ -1258,7 +1406,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                 } else if (s_part == 0 && g < G) {
                     gmax[g] = canon_zero(gm);
                 }
-            } else if (h.nvec > 0) {  // (a header-only stage just ends a shortened pass)
+            } else {
                 // pass 2 (pair): residual masses and maxima per group
                 const bool full = h.nvec == FULL_PAIR && !part;
                 float2 acc = make_float2(0.f, 0.f);
@@ -1320,9 +1468,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         // ---- end of a pass ------------------------------------------------------
         // A second pass longer than the ring continues after its first kRS stages
         // only with the chunks thread 0 lists here (dec_mask, then dec_bar).
-        const bool gated = pass == kPassStats && want_p2 && nch_pair > kRS;
+        const bool gated = pass == kPassStats && want_p2 && nch_pair > (wide ? 2 : 1) * kRS;
         auto list_chunks = [&](uint32_t all) {
-            if (gated && t == 0) {
+            if (gated && lead) {
                 if (all != 0u)
 #pragma unroll
                     for (int w = 0; w < kDecWords; ++w) gs.dec_mask[w] = all;
@@ -1333,7 +1481,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             // an inactive pair still receives (the unasked part of) its second pass;
             // hand off after it
             if (pass == kPassStats && pair) {
-                if (gated && t == 0)
+                if (gated && lead)
 #pragma unroll
                     for (int w = 0; w < kDecWords; ++w) gs.dec_mask[w] = 0u;
                 list_chunks(0u);
@@ -1342,21 +1490,28 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             continue;
         }
         if (pass == kPassStats && pair) {
-            // normalisers: warps 0-3 hold the target statistics, 4-7 the draft's
+            // normalisers: warps 0-3 of a group hold the target statistics, 4-7 the
+            // draft's (wide: group 0's, then group 1's, in every thread)
             const Stat ws = warp_stat(st);
-            gbar();
+            usync();
             if (lane == 0) gs.red[gw] = ws;
-            gbar();
-            Stat gT = gs.red[0], gD = gs.red[kGW / 2];
+            usync();
+            Stat gT = gsh[wide ? 0 : grp].red[0], gD = gsh[wide ? 0 : grp].red[kGW / 2];
 #pragma unroll
             for (int w = 1; w < kGW / 2; ++w) {
-                gT = stat_merge_nan(gT, gs.red[w]);
-                gD = stat_merge_nan(gD, gs.red[kGW / 2 + w]);
+                gT = stat_merge_nan(gT, gsh[wide ? 0 : grp].red[w]);
+                gD = stat_merge_nan(gD, gsh[wide ? 0 : grp].red[kGW / 2 + w]);
             }
+            if (wide)
+#pragma unroll
+                for (int w = 0; w < kGW / 2; ++w) {
+                    gT = stat_merge_nan(gT, gsh[1].red[w]);
+                    gD = stat_merge_nan(gD, gsh[1].red[kGW / 2 + w]);
+                }
             if (!stat_ok(gT) || !stat_ok(gD)) {
                 flags |= SSD_DEV_NONFINITE;
                 active = false;
-                if (gated && t == 0)
+                if (gated && lead)
 #pragma unroll
                     for (int w = 0; w < kDecWords; ++w) gs.dec_mask[w] = 0u;
                 list_chunks(0u);
@@ -1364,12 +1519,15 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                 continue;
             }
             LT = gT.m + lg2(gT.S);
+            // (wide: group 0 alone from here to the chunk list, with its own barriers;
+            // group 1 takes L_D, the draft shape and the top-F bound from it below)
+            if (!wide || grp == 0) {
             float qm = gD.m, qS = gD.S;
             if (sig) {
                 const unsigned char *drow = static_cast<const unsigned char *>(P.drf) +
                                             (static_cast<int64_t>(b) * P.drf_seq_stride + static_cast<int64_t>(k) * P.ld) * S;
                 const SigResult sr = sigma_fuse<D>(drow, gmax, G, V, P.sig_F[k], P.sig_C, c, gD, sig_keys, &gs.scnt,
-                                                   reinterpret_cast<float *>(gs.red), t, bar_id);
+                                                   wide ? s_wscr : reinterpret_cast<float *>(gs.red), t, bar_id);
                 shape = sr.shape;
                 qm = sr.qm;
                 qS = sr.qS;
@@ -1438,7 +1596,19 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                     list_chunks(0u);
                 }
             }
-            if (t == 0) {
+            }
+            if (wide) {
+                if (lead) {
+                    s_pub.cthr = cthr;
+                    s_pub.LD = LD;
+                    s_pub.shape = shape;
+                }
+                usync();
+                cthr = s_pub.cthr;
+                LD = s_pub.LD;
+                shape = s_pub.shape;
+            }
+            if (lead) {
                 if (kSig && P.desc_out) {
                     ssd_reshape_desc dd;
                     dd.F = sig ? P.sig_F[k] : 0;
@@ -1454,12 +1624,15 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         if (pass == kPassStats && sampled) {
             // sampled single row: target statistics for the tail's p-masses
             const Stat ws = warp_stat(st);
-            gbar();
+            usync();
             if (lane == 0) gs.red[gw] = ws;
-            gbar();
-            Stat gT = gs.red[0];
+            usync();
+            Stat gT = gsh[wide ? 0 : grp].red[0];
 #pragma unroll
-            for (int w = 1; w < kGW; ++w) gT = stat_merge_nan(gT, gs.red[w]);
+            for (int w = 1; w < kGW; ++w) gT = stat_merge_nan(gT, gsh[wide ? 0 : grp].red[w]);
+            if (wide)
+#pragma unroll
+                for (int w = 0; w < kGW; ++w) gT = stat_merge_nan(gT, gsh[1].red[w]);
             if (!stat_ok(gT)) {
                 flags |= SSD_DEV_NONFINITE;
                 handoff(kKindPass, 1, 0.f, 0.f);
@@ -1475,22 +1648,34 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         handoff(kKindPair, 1, 0.f, 0.f);
     }
 
-    // this group is done: tell its tail warp
-    if (!mbar_wait_suspend(&gs.tail_empty[nho % kNBuf], ((nho / kNBuf) & 1) ^ 1)) {
-        if (t == 0 && P.dev_status) atomicOr(P.dev_status, SSD_DEV_TIMEOUT);
+    // this group is done: tell its tail warp (wide: at the next unit index of that warp)
+    {
+        const uint32_t j = wide ? nho + ((nho ^ static_cast<uint32_t>(grp)) & 1u) : nho;
+        const int sb = static_cast<int>(wide ? (j >> 1) & 1 : j % kNBuf);
+        const uint32_t spar = wide ? (j >> 2) & 1 : (j / kNBuf) & 1;
+        if (!mbar_wait_suspend(&gs.tail_empty[sb], spar ^ 1)) {
+            if (t == 0 && P.dev_status) atomicOr(P.dev_status, SSD_DEV_TIMEOUT);
+        }
+        gbar();
+        if (t == 0) {
+            gs.desc[sb].kind = kKindStop;
+            mbar_arrive(&gs.tail_full[sb]);
+        }
     }
-    handoff(kKindStop, 0, 0.f, 0.f);
 }
 
+#ifndef SSD_STREAM_WIDE_TU
+// the one-group forms (this translation unit)
 template <class D>
 int stream_setup_d(size_t optin, size_t *max_dyn) {
     bool dummy = true;
     size_t lim[4];
-    int st = setup_kernel(ssd_stream_kernel<D, true, false>, optin, &lim[0], &dummy);
-    if (st == SSD_OK) st = setup_kernel(ssd_stream_kernel<D, false, true>, optin, &lim[1], &dummy);
-    if (st == SSD_OK) st = setup_kernel(ssd_stream_kernel<D, false, false>, optin, &lim[2], &dummy);
+    int st = setup_kernel(ssd_stream_kernel<D, true, false, false>, optin, &lim[0], &dummy);
+    if (st == SSD_OK) st = setup_kernel(ssd_stream_kernel<D, false, true, false>, optin, &lim[1], &dummy);
+    if (st == SSD_OK) st = setup_kernel(ssd_stream_kernel<D, false, false, false>, optin, &lim[2], &dummy);
+    if (st == SSD_OK) st = stream_wide_setup(D::kBytes == 4 ? SSD_F32 : SSD_BF16, optin, &lim[3]);
     if (st != SSD_OK) return st;
-    *max_dyn = std::min(lim[0], std::min(lim[1], lim[2]));  // one limit for every form
+    *max_dyn = std::min(std::min(lim[0], lim[1]), std::min(lim[2], lim[3]));  // one limit for every form
     return SSD_OK;
 }
 
@@ -1500,9 +1685,10 @@ int stream_setup(int dtype, size_t optin, size_t *max_dyn) {
 
 template <class D>
 cudaError_t stream_launch_d(const cudaLaunchConfig_t &cfg, const UnitParams &P) {
-    if (P.sig_on) return cudaLaunchKernelEx(&cfg, ssd_stream_kernel<D, true, false>, P);
-    if (P.V % D::kVec != 0) return cudaLaunchKernelEx(&cfg, ssd_stream_kernel<D, false, true>, P);
-    return cudaLaunchKernelEx(&cfg, ssd_stream_kernel<D, false, false>, P);
+    if (P.wide) return stream_wide_launch(D::kBytes == 4 ? SSD_F32 : SSD_BF16, cfg, P);
+    if (P.sig_on) return cudaLaunchKernelEx(&cfg, ssd_stream_kernel<D, true, false, false>, P);
+    if (P.V % D::kVec != 0) return cudaLaunchKernelEx(&cfg, ssd_stream_kernel<D, false, true, false>, P);
+    return cudaLaunchKernelEx(&cfg, ssd_stream_kernel<D, false, false, false>, P);
 }
 
 int stream_launch(int dtype, const UnitParams &P, int grid, size_t dyn, void *stream) {
@@ -1524,5 +1710,30 @@ int stream_launch(int dtype, const UnitParams &P, int grid, size_t dyn, void *st
     }
     return SSD_OK;
 }
+#else
+// the wide forms (rows of whole 16-byte vectors; sigma found in the pass or not)
+template <class D>
+int stream_wide_setup_d(size_t optin, size_t *max_dyn) {
+    bool dummy = true;
+    size_t lim[2];
+    int st = setup_kernel(ssd_stream_kernel<D, true, false, true>, optin, &lim[0], &dummy);
+    if (st == SSD_OK) st = setup_kernel(ssd_stream_kernel<D, false, false, true>, optin, &lim[1], &dummy);
+    if (st != SSD_OK) return st;
+    *max_dyn = std::min(lim[0], lim[1]);
+    return SSD_OK;
+}
+
+int stream_wide_setup(int dtype, size_t optin, size_t *max_dyn) {
+    return dtype == SSD_F32 ? stream_wide_setup_d<F32Tag>(optin, max_dyn) : stream_wide_setup_d<BF16Tag>(optin, max_dyn);
+}
+
+cudaError_t stream_wide_launch(int dtype, const cudaLaunchConfig_t &cfg, const UnitParams &P) {
+    if (dtype == SSD_F32)
+        return P.sig_on ? cudaLaunchKernelEx(&cfg, ssd_stream_kernel<F32Tag, true, false, true>, P)
+                        : cudaLaunchKernelEx(&cfg, ssd_stream_kernel<F32Tag, false, false, true>, P);
+    return P.sig_on ? cudaLaunchKernelEx(&cfg, ssd_stream_kernel<BF16Tag, true, false, true>, P)
+                    : cudaLaunchKernelEx(&cfg, ssd_stream_kernel<BF16Tag, false, false, true>, P);
+}
+#endif
 
 }  // namespace ssd

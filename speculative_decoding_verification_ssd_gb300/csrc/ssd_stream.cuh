@@ -4,6 +4,8 @@
 
 #include <cstddef>
 
+#include <cuda_runtime.h>
+
 namespace ssd {
 
 constexpr int kStreamGroups = 2;       // consumer groups, each with its own ring
@@ -34,5 +36,8 @@ inline size_t stream_dyn_bytes(int V, bool sig = false) {
 struct UnitParams;
 int stream_setup(int dtype, size_t optin, size_t *max_dyn);
 int stream_launch(int dtype, const UnitParams &P, int grid, size_t dyn, void *stream);
+// the wide forms (ssd_stream_wide.cu), reached through the two calls above
+int stream_wide_setup(int dtype, size_t optin, size_t *max_dyn);
+cudaError_t stream_wide_launch(int dtype, const cudaLaunchConfig_t &cfg, const UnitParams &P);
 
 }  // namespace ssd

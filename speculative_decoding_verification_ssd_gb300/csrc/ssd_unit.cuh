@@ -63,6 +63,7 @@ struct UnitParams {
                                     // 32 bits) and from the back (high 32 bits) of the order
     uint32_t *exit_counter;  // CTAs that have exited
     int perm_mul;            // unit u -> sequence ((u % B) * perm_mul) % B (coprime to B)
+    int wide;                // streaming kernel: both consumer groups of a CTA share each unit
     // sigma_{F,C} found in the pass over the draft rows (streaming kernel only):
     // position k of a sampled sequence reshapes with F = sig_F[k] (0: none)
     int sig_on;

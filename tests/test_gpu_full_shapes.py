@@ -57,7 +57,7 @@ def sigma_case():
     return wl, inp, o
 
 
-@pytest.mark.parametrize("policy", [1, 2])  # streaming kernel, cluster kernel
+@pytest.mark.parametrize("policy", [1, 2, 4])  # streaming kernel, cluster kernel, wide streaming
 def test_sigma_verify_full_shape(ssd, sigma_case, policy):
     wl, inp, o = sigma_case
     d = to_device(inp)
@@ -83,14 +83,16 @@ def test_sigma_verify_full_shape(ssd, sigma_case, policy):
         assert Fd[r] == wl.reshape_F
 
 
-def test_sigma_two_pass_full_shape(ssd, sigma_case):
+@pytest.mark.parametrize("policy", [0, 4])  # default choice, wide streaming
+def test_sigma_two_pass_full_shape(ssd, sigma_case, policy):
     wl, inp, o = sigma_case
     d = to_device(inp)
     tau_rows = d["temperature"].repeat_interleave(wl.K)
     desc, _ = ssd.ssd_reshape_draft(d["drf"], wl.reshape_F, wl.reshape_C, tau_rows)
-    g = ssd.ssd_verify(d["tgt"], d["drf"], d["tokens"], d["uniforms"], d["temperature"],
-                       reshape=desc)
-    torch.cuda.synchronize()
+    with use_dispatch(ssd, policy):
+        g = ssd.ssd_verify(d["tgt"], d["drf"], d["tokens"], d["uniforms"], d["temperature"],
+                           reshape=desc)
+        torch.cuda.synchronize()
     t = Tally()
     compare_verify(np_out(g), o, wl.K, t)
     t.check()
@@ -107,7 +109,7 @@ def round_case():
     return wl, inp, Fo, off, o
 
 
-@pytest.mark.parametrize("policy", [1, 2, 3])  # streaming, cluster, slice kernel
+@pytest.mark.parametrize("policy", [1, 2, 3, 4])  # streaming, cluster, slice kernel, wide streaming
 def test_round_full_shape_fp32(ssd, round_case, policy):
     wl, inp, Fo, off, o = round_case
     F, off_g = ssd.ssd_fanout(wl.K, wl.budget, wl.a_p, wl.r, wl.V)
@@ -117,7 +119,7 @@ def test_round_full_shape_fp32(ssd, round_case, policy):
     with use_dispatch(ssd, policy):
         out = ssd.ssd_round(d["tgt"], d["drf"], d["tokens"], d["uniforms"], d["temperature"],
                             F, wl.budget)
-        assert ssd.ssd_last_kernel() == {1: "stream", 2: "cluster", 3: "slice"}[policy]
+        assert ssd.ssd_last_kernel() == {1: "stream", 2: "cluster", 3: "slice", 4: "stream-wide"}[policy]
         torch.cuda.synchronize()
     g = np_out(out)
     t = Tally()

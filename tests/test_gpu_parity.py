@@ -48,7 +48,7 @@ def _run_verify(ssd, inp, reshape=None):
     return np_out(out)
 
 
-@pytest.mark.parametrize("policy", [1, 2, 3])  # streaming, cluster, slice kernel
+@pytest.mark.parametrize("policy", [1, 2, 3, 4])  # streaming, cluster, slice kernel, wide streaming
 @pytest.mark.parametrize("name,B,seed_off", [("c1", 1, 0), ("c1", 64, 1), ("c2", 8, 0),
                                              ("c2", 24, 1)])
 def test_verify_parity(ssd, name, B, seed_off, policy):
@@ -56,7 +56,7 @@ def test_verify_parity(ssd, name, B, seed_off, policy):
     inp = synth.make_inputs(wl, synth.PARITY_SEED[name] + 100 * seed_off)
     with use_dispatch(ssd, policy):
         g = _run_verify(ssd, inp)
-        assert ssd.ssd_last_kernel() == {1: "stream", 2: "cluster", 3: "slice"}[policy]
+        assert ssd.ssd_last_kernel() == {1: "stream", 2: "cluster", 3: "slice", 4: "stream-wide"}[policy]
     o = _oracle_verify(inp, wl)
     t = Tally()
     compare_verify(g, o, wl.K, t)
@@ -103,7 +103,7 @@ def test_verify_reshaped_parity(ssd):
     assert err <= 1e-5, err
 
 
-@pytest.mark.parametrize("policy", [1, 2, 3])  # streaming, cluster, slice kernel
+@pytest.mark.parametrize("policy", [1, 2, 3, 4])  # streaming, cluster, slice kernel, wide streaming
 @pytest.mark.parametrize("name,B", [("c4", 6), ("c5", 32)])
 def test_round_parity(ssd, name, B, policy):
     wl = _reduced(name, B)
@@ -115,7 +115,7 @@ def test_round_parity(ssd, name, B, policy):
     with use_dispatch(ssd, policy):
         out = ssd.ssd_round(d["tgt"], d["drf"], d["tokens"], d["uniforms"], d["temperature"], F,
                             wl.budget)
-        assert ssd.ssd_last_kernel() == {1: "stream", 2: "cluster", 3: "slice"}[policy]
+        assert ssd.ssd_last_kernel() == {1: "stream", 2: "cluster", 3: "slice", 4: "stream-wide"}[policy]
     torch.cuda.synchronize()
     g = np_out(out)
     o = oracle.round_(inp["tgt"], inp["drf"], inp["tokens"], inp["uniforms"],

@@ -13,21 +13,25 @@ import pytest
 
 import oracle
 import synth
-from tests._parity import Tally, compare_cache, compare_verify, lookup_from, np_out
+from tests._parity import Tally, compare_cache, compare_verify, lookup_from, np_out, use_dispatch
 
 pytestmark = pytest.mark.gpu
 
 torch = pytest.importorskip("torch")
 
 
-@pytest.fixture(scope="module")
-def ssd():
+@pytest.fixture(scope="module", params=["default", "wide"])
+def ssd(request):
+    """The library under its default kernel choice, and with the streaming kernel's
+    wide form forced (both consumer groups of a CTA on each unit)."""
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     import speculative_decoding_verification_ssd_gb300 as m
     from speculative_decoding_verification_ssd_gb300 import _build
     _build.build()
-    return m
+    policy = m.SSD_DISPATCH_AUTO if request.param == "default" else m.SSD_DISPATCH_WIDE
+    with use_dispatch(m, policy):
+        yield m
 
 
 def _dev_logits(a, dtype):

@@ -27,7 +27,7 @@ pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
 
 
-@pytest.fixture(scope="module", params=["stream", "slice"])
+@pytest.fixture(scope="module", params=["stream", "slice", "wide"])
 def ssd(request):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
@@ -35,8 +35,10 @@ def ssd(request):
     from speculative_decoding_verification_ssd_gb300 import _build
     _build.build()
     # these batches are small: force the persistent kernel whose paths they exercise
-    # (the streaming kernel, or the slice kernel, which has the same paths per slice)
-    policy = m.SSD_DISPATCH_STREAM if request.param == "stream" else m.SSD_DISPATCH_SLICE
+    # (the streaming kernel in either form, or the slice kernel, which has the same
+    # paths per slice)
+    policy = {"stream": m.SSD_DISPATCH_STREAM, "slice": m.SSD_DISPATCH_SLICE,
+              "wide": m.SSD_DISPATCH_WIDE}[request.param]
     with use_dispatch(m, policy):
         yield m
 

@@ -67,16 +67,18 @@ def _noalloc_round(ssd, tgt, drf, tok, u, tau, F, budget):
     return {k: v.cpu().numpy() for k, v in out.items()}
 
 
-@pytest.mark.parametrize("B,policy", [(48, "auto"), (48, "cluster"), (8, "auto")])
+@pytest.mark.parametrize("B,policy", [(48, "auto"), (48, "stream"), (48, "cluster"), (8, "auto")])
 def test_noalloc_round_matches_round_on_two_calls(ssd, B, policy):
-    """B = 48 (240 units) runs the persistent streaming kernel unless the cluster
-    kernel is forced; B = 8 (40 units, fewer than the SMs) takes the cluster kernel
-    by itself.  Both kernels use the same counters and records in the array."""
+    """B = 48 (240 units, between one and two per SM) runs the persistent streaming
+    kernel in its wide form by default, in its one-group-per-unit form or the cluster
+    kernel when forced; B = 8 (40 units, fewer than the SMs) takes the cluster kernel
+    by itself.  Every kernel uses the same counters and records in the array."""
     wl = synth.WORKLOADS["c5"].replace(B=B, greedy_first=B // 2)
     inp = synth.make_inputs(wl, 777 + B)
     tgt, drf, tok, u, tau = _device_inputs(inp)
     F, off = ssd.ssd_fanout(wl.K, wl.budget, wl.a_p, wl.r, wl.V)
-    pol = {"auto": ssd.SSD_DISPATCH_AUTO, "cluster": ssd.SSD_DISPATCH_CLUSTER}[policy]
+    pol = {"auto": ssd.SSD_DISPATCH_AUTO, "stream": ssd.SSD_DISPATCH_STREAM,
+           "cluster": ssd.SSD_DISPATCH_CLUSTER}[policy]
     prev = ssd.ssd_set_dispatch(pol)
     try:
         ref = ssd.ssd_round(tgt, drf, tok, u, tau, F, wl.budget)
