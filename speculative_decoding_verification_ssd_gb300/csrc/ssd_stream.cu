@@ -474,7 +474,12 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         uint32_t n = 0;     // stages pushed
         uint32_t ndec = 0;  // second-pass chunk lists received
         bool ok = true;
-        if (kWide) {
+        // Stages of a second pass streamed before the consumers' chunk list arrives: a
+        // ring's worth (per ring), also in verification alone, where only a rejected pair
+        // uses them -- they hide the decision's latency on the first rejection of a
+        // sequence, which bounds the launch (c3 with none: 85.5 against 82.5 us).
+        const int unasked = kRS;
+        if constexpr (kWide) {
             // Both consumer groups share each unit: its chunk stages alternate between
             // ring 0 and ring 1 (every pass puts its last chunk on each ring with the
             // end bit, or a header-only end stage on a ring that got no chunk), and a
@@ -542,18 +547,19 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                 if (ok && nch == 1) ok = end_stage(1, kPassStats);
                 if (ok && p2) {
                     // from the row's end back to its start, as in the one-ring form
-                    if (nch <= 2 * kRS) {
+                    if (nch <= 2 * unasked) {
                         for (int i = 0; i < nch && ok; ++i) {
                             ok = chunk_stage(i & 1, kPassResid, nch - 1 - i, i >= nch - 2);
                             if (nch - i <= 3) pf_step();
                         }
                         if (ok && nch == 1) ok = end_stage(1, kPassResid);
                     } else {
-                        for (int i = 0; i < 2 * kRS && ok; ++i) ok = chunk_stage(i & 1, kPassResid, nch - 1 - i, false);
+                        for (int i = 0; i < 2 * unasked && ok; ++i)
+                            ok = chunk_stage(i & 1, kPassResid, nch - 1 - i, false);
                         if (ok) ok = mbar_wait_suspend(&gsh[0].dec_bar, ndec & 1);
                         if (ok) {
                             ++ndec;
-                            const int lim = nch - 2 * kRS;  // chunks [0, lim) stream only when listed
+                            const int lim = nch - 2 * unasked;  // chunks [0, lim) stream only when listed
                             const volatile uint32_t *dm = gsh[0].dec_mask;
                             int L = 0;
                             for (int w = 0; w * 32 < lim; ++w) {
@@ -577,106 +583,102 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                 }
                 if (!ok) break;
             }
-            if (!ok) {
-                atomicOr(&s_abort, 1);
-                if (P.dev_status) atomicOr(P.dev_status, SSD_DEV_TIMEOUT);
-            }
-            return;
-        }
-        for (;;) {
-            while (pf_state < 2) pf_step();
-            pf_state = 0;
-            const int u = pf_u;
-            if (u >= nunits) {
-                const int s = static_cast<int>(n % kRS);
-                if (!mbar_wait_suspend(&gq.empty_bar[s], ((n / kRS) & 1) ^ 1)) {
-                    ok = false;
+        } else {
+            for (;;) {
+                while (pf_state < 2) pf_step();
+                pf_state = 0;
+                const int u = pf_u;
+                if (u >= nunits) {
+                    const int s = static_cast<int>(n % kRS);
+                    if (!mbar_wait_suspend(&gq.empty_bar[s], ((n / kRS) & 1) ^ 1)) {
+                        ok = false;
+                        break;
+                    }
+                    gq.hdr[s] = Hdr{-1, kPassStop | (1 << 4), 0, 0, 0, 0, 0, 0};
+                    mbar_arrive_expect_tx(&gq.full_bar[s], 0);
                     break;
                 }
-                gq.hdr[s] = Hdr{-1, kPassStop | (1 << 4), 0, 0, 0, 0, 0, 0};
-                mbar_arrive_expect_tx(&gq.full_bar[s], 0);
-                break;
-            }
-            const int b = pf_b, k = pf_k;
-            const float tau = pf_tau;
-            const bool sampled = (tau > 0.f) && (tau < INFINITY);
-            const bool pair = sampled && k < K;
-            const bool p2 = pair && (do_verify || (do_cache && P.F[k] > 0));
-            const uint32_t mask = (k >= 32) ? 0xFFFFFFFFu : ((1u << k) - 1u);
-            const bool skip = (P.mode & kModeEarlyExit) && k > 0 && (pf_rej & mask) != 0;
-            const unsigned char *trow = static_cast<const unsigned char *>(P.tgt) +
-                                        (static_cast<int64_t>(b) * P.tgt_seq_stride + static_cast<int64_t>(k) * P.ld) * S;
-            const unsigned char *drow =
-                pair ? static_cast<const unsigned char *>(P.drf) +
-                           (static_cast<int64_t>(b) * P.drf_seq_stride + static_cast<int64_t>(k) * P.ld) * S
-                     : nullptr;
-            const int cb = pair ? HALF : kSB;
-            const int nch = static_cast<int>((row_bytes + cb - 1) / cb);
-            const int total = skip ? 1 : nch * (p2 ? 2 : 1);
-            // A second pass longer than the ring streams its first kRS stages unasked;
-            // the rest follows the consumers' chunk list, which they publish once the
-            // accept test and the top-F bound are known (before those stages are used).
-            const bool gated = p2 && !skip && nch > kRS;
-            int lowest = 0;  // gated: the smallest listed chunk (streamed last), -1 for none
-            for (int i = 0; i < total; ++i) {
-                bool empty_end = false, listed_last = false;
-                if (gated && i >= nch + kRS) {
-                    if (i == nch + kRS) {
-                        if (!mbar_wait_suspend(&gq.dec_bar, ndec & 1)) {
-                            ok = false;
-                            break;
+                const int b = pf_b, k = pf_k;
+                const float tau = pf_tau;
+                const bool sampled = (tau > 0.f) && (tau < INFINITY);
+                const bool pair = sampled && k < K;
+                const bool p2 = pair && (do_verify || (do_cache && P.F[k] > 0));
+                const uint32_t mask = (k >= 32) ? 0xFFFFFFFFu : ((1u << k) - 1u);
+                const bool skip = (P.mode & kModeEarlyExit) && k > 0 && (pf_rej & mask) != 0;
+                const unsigned char *trow = static_cast<const unsigned char *>(P.tgt) +
+                                            (static_cast<int64_t>(b) * P.tgt_seq_stride + static_cast<int64_t>(k) * P.ld) * S;
+                const unsigned char *drow =
+                    pair ? static_cast<const unsigned char *>(P.drf) +
+                               (static_cast<int64_t>(b) * P.drf_seq_stride + static_cast<int64_t>(k) * P.ld) * S
+                         : nullptr;
+                const int cb = pair ? HALF : kSB;
+                const int nch = static_cast<int>((row_bytes + cb - 1) / cb);
+                const int total = skip ? 1 : nch * (p2 ? 2 : 1);
+                // A second pass longer than its unasked stages streams those first; the
+                // rest follows the consumers' chunk list, which they publish once the
+                // accept test and the top-F bound are known (before those stages are used).
+                const bool gated = p2 && !skip && nch > unasked;
+                int lowest = 0;  // gated: the smallest listed chunk (streamed last), -1 for none
+                for (int i = 0; i < total; ++i) {
+                    bool empty_end = false, listed_last = false;
+                    if (gated && i >= nch + unasked) {
+                        if (i == nch + unasked) {
+                            if (!mbar_wait_suspend(&gq.dec_bar, ndec & 1)) {
+                                ok = false;
+                                break;
+                            }
+                            ++ndec;
+                            lowest = -1;
+                            for (int c = 0; c < nch - unasked && lowest < 0; ++c)
+                                if ((reinterpret_cast<volatile uint32_t *>(gq.dec_mask)[c >> 5] >> (c & 31)) & 1u)
+                                    lowest = c;
                         }
-                        ++ndec;
-                        lowest = -1;
-                        for (int c = 0; c < nch - kRS && lowest < 0; ++c)
-                            if ((reinterpret_cast<volatile uint32_t *>(gq.dec_mask)[c >> 5] >> (c & 31)) & 1u)
-                                lowest = c;
+                        const int chunk = nch - 1 - (i - nch);
+                        if (lowest < 0) {
+                            empty_end = true;  // nothing listed: a header-only stage ends the pass
+                            i = total - 1;
+                        } else if (!((reinterpret_cast<volatile uint32_t *>(gq.dec_mask)[chunk >> 5] >> (chunk & 31)) & 1u)) {
+                            if (total - i <= 3) pf_step();
+                            continue;
+                        } else {
+                            listed_last = chunk == lowest;
+                        }
                     }
-                    const int chunk = nch - 1 - (i - nch);
-                    if (lowest < 0) {
-                        empty_end = true;  // nothing listed: a header-only stage ends the pass
-                        i = total - 1;
-                    } else if (!((reinterpret_cast<volatile uint32_t *>(gq.dec_mask)[chunk >> 5] >> (chunk & 31)) & 1u)) {
-                        if (total - i <= 3) pf_step();
-                        continue;
+                    const int s = static_cast<int>(n % kRS);
+                    if (!mbar_wait_suspend(&gq.empty_bar[s], ((n / kRS) & 1) ^ 1)) {
+                        ok = false;
+                        break;
+                    }
+                    if (skip) {
+                        gq.hdr[s] = Hdr{u, kPassSkip | (1 << 4), 0, 0, b, k, 0, 0};
+                        mbar_arrive_expect_tx(&gq.full_bar[s], 0);
+                    } else if (empty_end) {
+                        gq.hdr[s] = Hdr{u, kPassResid | (1 << 4) | (1 << 5), -1, 0, b, k, 0, 0};
+                        mbar_arrive_expect_tx(&gq.full_bar[s], 0);
                     } else {
-                        listed_last = chunk == lowest;
+                        const bool second = i >= nch;
+                        // the second pass runs from the row's end back to its start: the
+                        // chunks read last in the first pass are the likeliest still in L2
+                        const int chunk = second ? nch - 1 - (i - nch) : i;
+                        const int64_t off = static_cast<int64_t>(chunk) * cb;
+                        const uint32_t bytes = static_cast<uint32_t>(row_bytes - off < cb ? row_bytes - off : cb);
+                        const bool last = second ? (gated && i >= nch + unasked ? listed_last : chunk == 0)
+                                                 : chunk == nch - 1;
+                        const int code = (second ? kPassResid : kPassStats) | ((last ? 1 : 0) << 4) |
+                                         ((pair ? 1 : 0) << 5);
+                        gq.hdr[s] = Hdr{u, code, chunk, static_cast<int>(bytes / 16), b, k, 0, 0};
+                        unsigned char *dst = ring + s * kSB;
+                        mbar_arrive_expect_tx(&gq.full_bar[s], bytes * (pair ? 2u : 1u));
+                        // evict_first throughout: most second passes are cut to a few chunks,
+                        // so holding first-pass rows in L2 for them costs more than it saves
+                        bulk_copy_hint(dst, trow + off, bytes, &gq.full_bar[s], pol);
+                        if (pair) bulk_copy_hint(dst + HALF, drow + off, bytes, &gq.full_bar[s], pol);
                     }
+                    ++n;
+                    if (total - i <= 3) pf_step();
                 }
-                const int s = static_cast<int>(n % kRS);
-                if (!mbar_wait_suspend(&gq.empty_bar[s], ((n / kRS) & 1) ^ 1)) {
-                    ok = false;
-                    break;
-                }
-                if (skip) {
-                    gq.hdr[s] = Hdr{u, kPassSkip | (1 << 4), 0, 0, b, k, 0, 0};
-                    mbar_arrive_expect_tx(&gq.full_bar[s], 0);
-                } else if (empty_end) {
-                    gq.hdr[s] = Hdr{u, kPassResid | (1 << 4) | (1 << 5), -1, 0, b, k, 0, 0};
-                    mbar_arrive_expect_tx(&gq.full_bar[s], 0);
-                } else {
-                    const bool second = i >= nch;
-                    // the second pass runs from the row's end back to its start: the
-                    // chunks read last in the first pass are the likeliest still in L2
-                    const int chunk = second ? nch - 1 - (i - nch) : i;
-                    const int64_t off = static_cast<int64_t>(chunk) * cb;
-                    const uint32_t bytes = static_cast<uint32_t>(row_bytes - off < cb ? row_bytes - off : cb);
-                    const bool last = second ? (gated && i >= nch + kRS ? listed_last : chunk == 0)
-                                             : chunk == nch - 1;
-                    const int code = (second ? kPassResid : kPassStats) | ((last ? 1 : 0) << 4) |
-                                     ((pair ? 1 : 0) << 5);
-                    gq.hdr[s] = Hdr{u, code, chunk, static_cast<int>(bytes / 16), b, k, 0, 0};
-                    unsigned char *dst = ring + s * kSB;
-                    mbar_arrive_expect_tx(&gq.full_bar[s], bytes * (pair ? 2u : 1u));
-                    // evict_first throughout: most second passes are cut to a few chunks,
-                    // so holding first-pass rows in L2 for them costs more than it saves
-                    bulk_copy_hint(dst, trow + off, bytes, &gq.full_bar[s], pol);
-                    if (pair) bulk_copy_hint(dst + HALF, drow + off, bytes, &gq.full_bar[s], pol);
-                }
-                ++n;
-                if (total - i <= 3) pf_step();
+                if (!ok) break;
             }
-            if (!ok) break;
         }
         if (!ok) {
             atomicOr(&s_abort, 1);
@@ -1466,8 +1468,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         if (!((h.code >> 4) & 1)) continue;
 
         // ---- end of a pass ------------------------------------------------------
-        // A second pass longer than the ring continues after its first kRS stages
-        // only with the chunks thread 0 lists here (dec_mask, then dec_bar).
+        // A second pass longer than its unasked stages (a ring's worth per ring)
+        // continues only with the chunks thread 0 lists here (dec_mask, then dec_bar).
         const bool gated = pass == kPassStats && want_p2 && nch_pair > (wide ? 2 : 1) * kRS;
         auto list_chunks = [&](uint32_t all) {
             if (gated && lead) {
@@ -1572,7 +1574,14 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                 notfirst = (old & ((1u << k) - 1u)) != 0u;
             }
             if (gated) {
-                if (cthr == -INFINITY) {
+                if (cthr == INFINITY) {
+                    // no residual is used (no cache top-F here, no bonus): no chunk, and
+                    // no group array is read after this pass
+                    if (t == 0)
+#pragma unroll
+                        for (int w = 0; w < kDecWords; ++w) gs.dec_mask[w] = 0u;
+                    list_chunks(0u);
+                } else if (cthr == -INFINITY) {
                     if (t == 0 && notfirst)
 #pragma unroll
                         for (int w = 0; w < kDecWords; ++w) gs.dec_mask[w] = 0u;

@@ -9,6 +9,8 @@ compared with the float64 oracle:
   residual at all (draft equal to target: every group is computed);
 * a fan-out with F_k above 64, where the top-F threshold is found by bisection
   over the group maxima instead of from the lanes' two largest maxima;
+* pair rows of one chunk, of exactly the chunks a second pass streams unasked,
+  and of one chunk more;
 * rows whose logits are all equal, where every group reaches the threshold
   (the candidate-group list overflows and all groups are re-read) and every
   element ties (the candidate-key buffer overflows and the threshold is raised
@@ -113,6 +115,31 @@ def test_fanout_above_64_uses_bisection(ssd, dtype):
     u = rng.random((B, K + 1))
     _, _, F = _round_and_compare(ssd, _pack(zt, zd, tok, u, [1.0, 0.0, 0.7] * 2, dtype), 450, 0.8, 0.5)
     assert max(F) > 64
+
+
+# pair rows of one 8 KB chunk (the wide form ends each pass on its second ring with a
+# header-only stage), of exactly the eight chunks both rings take unasked in a second
+# pass, and of one chunk more (a chunk list of one entry); single rows of one 16 KB chunk
+@pytest.mark.parametrize("dtype,V", [("bf16", 1000), ("bf16", 4096), ("f32", 2000),
+                                     ("bf16", 32768), ("bf16", 36864), ("f32", 16384),
+                                     ("f32", 18432)])
+def test_row_lengths_around_the_rings(ssd, dtype, V):
+    rng = np.random.default_rng(V + (7 if dtype == "f32" else 0))
+    B, K = 6, 3
+    zt = (rng.standard_normal((B, K + 1, V)) * 2.5).astype(np.float32)
+    zd = (zt[:, :K] + rng.standard_normal((B, K, V)) * 0.9).astype(np.float32)
+    tok = np.argmax(zd + rng.gumbel(size=zd.shape), axis=-1)
+    u = rng.random((B, K + 1))
+    inp = _pack(zt, zd, tok, u, [1.0, 0.0, 0.7, 1.0, 1.0, 0.0], dtype)
+    _round_and_compare(ssd, inp, 24, 0.75, 0.5)
+    # verification alone (the early-exit form)
+    d = to_device(inp)
+    g = np_out(ssd.ssd_verify(d["tgt"], d["drf"], d["tokens"], d["uniforms"], d["temperature"]))
+    o = oracle.verify(inp["tgt"], inp["drf"], inp["tokens"], inp["uniforms"], inp["temperature"],
+                      inp["workload"].dtype)
+    t = Tally()
+    compare_verify(g, o, K, t)
+    t.check()
 
 
 def test_all_equal_rows_overflow_both_candidate_buffers(ssd):
