@@ -71,6 +71,7 @@ constexpr int kNBuf = kStreamBuffers;   // group-array buffers per consumer grou
 constexpr int kProducerWarp0 = kNG * kGW;
 constexpr int kTailWarp0 = kProducerWarp0 + kNG;
 constexpr int kCandGroupsCap = 512;
+constexpr int kConsCandCap = 256;  // candidate groups an accepted pair resolves by direct loads
 constexpr int kDecWords = 4;  // chunk bitmap of a second pass (128 chunks)
 constexpr int kSchedCap = 2048;  // largest batch ordered by unit kind
 static_assert(kStreamSigKeys == kCandCap && kGT == kThreads, "fused sigma selection geometry");
@@ -119,6 +120,10 @@ struct GroupShared {
     int cgroups[kCandGroupsCap];
     int cnt[2];
     int scnt;  // consumer group: candidate count of the fused sigma selection
+    // consumer group: an accepted pair's candidate groups (their largest residual is
+    // computed from direct loads instead of a second pass over their chunks)
+    uint16_t ccg[kConsCandCap];
+    int ccnt;
 };
 
 // sigma_{F,C} of one draft row found in the streaming pass ([SSD] item 2): the
@@ -1587,22 +1592,74 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                         for (int w = 0; w < kDecWords; ++w) gs.dec_mask[w] = 0u;
                     list_chunks(notfirst ? 0u : 0xFFFFFFFFu);  // every chunk, or none
                 } else {
-                    // the chunks holding a group whose bound reaches cthr; every other
-                    // group's largest residual reads as 0 (its chunk may not be streamed)
-                    if (t == 0)
+                    // The groups whose bound reaches cthr are the candidates; every other
+                    // group's largest residual reads as 0.  Only the candidates' largest
+                    // residuals matter here (the tail ranks the cache top-F from them; no
+                    // residual is sampled at this position), so the group loads those 64
+                    // tokens of both rows directly -- a warp per group, the same per-token
+                    // arithmetic as the second pass -- and lists no chunk.  Past
+                    // kConsCandCap candidates the chunks holding them are streamed instead.
+                    if (t == 0) {
 #pragma unroll
                         for (int w = 0; w < kDecWords; ++w) gs.dec_mask[w] = 0u;
-                    gbar();
-                    for (int gg = t; gg < G; gg += kGT) {
-                        const bool cg = cthr < INFINITY &&
-                                        ex2(fmaf(gsum[gg], c, -LT)) * (1.f + 0x1p-20f) >= cthr;
-                        if (cg)
-                            atomicOr(&gs.dec_mask[(gg / GPR) >> 5], 1u << ((gg / GPR) & 31));
-                        else
-                            gmax[gg] = 0.f;
+                        gs.ccnt = 0;
                     }
                     gbar();
-                    list_chunks(0u);
+                    auto is_cand = [&](int gg) {
+                        return cthr < INFINITY && ex2(fmaf(gsum[gg], c, -LT)) * (1.f + 0x1p-20f) >= cthr;
+                    };
+                    for (int gg = t; gg < G; gg += kGT) {
+                        if (is_cand(gg)) {
+                            const int ci = atomicAdd(&gs.ccnt, 1);
+                            if (ci < kConsCandCap) gs.ccg[ci] = static_cast<uint16_t>(gg);
+                        } else {
+                            gmax[gg] = 0.f;
+                        }
+                    }
+                    gbar();
+                    const int ncg = gs.ccnt;
+                    if (ncg <= kConsCandCap) {
+                        list_chunks(0u);
+                        const unsigned char *trow = static_cast<const unsigned char *>(P.tgt) +
+                                                    (static_cast<int64_t>(b) * P.tgt_seq_stride + static_cast<int64_t>(k) * P.ld) * S;
+                        const unsigned char *drow = static_cast<const unsigned char *>(P.drf) +
+                                                    (static_cast<int64_t>(b) * P.drf_seq_stride + static_cast<int64_t>(k) * P.ld) * S;
+                        const float nLT = -LT;
+                        // two groups per warp at a time (both groups' loads in flight together)
+                        for (int ci = gw; ci < ncg; ci += 2 * kGW) {
+                            const int ci2 = ci + kGW;
+                            const int ga = gs.ccg[ci], gb2 = ci2 < ncg ? gs.ccg[ci2] : ga;
+                            float zp[4], zq[4];
+                            int ee[4];
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                ee[j] = (j < 2 ? ga : gb2) * kGTok + 2 * lane + (j & 1);
+                                const bool in = ee[j] < V;
+                                zp[j] = in ? load_logit<D>(trow, ee[j]) : -INFINITY;
+                                zq[j] = in ? load_logit<D>(drow, ee[j]) : -INFINITY;
+                            }
+                            float ra = 0.f, rb = 0.f;
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const float r = ee[j] < V ? resid_of(zp[j], zq[j], c, nLT, draft_bias(shape, zq[j], ee[j]) - LD)
+                                                          : 0.f;
+                                if (j < 2) ra = fmaxf(ra, r);
+                                else rb = fmaxf(rb, r);
+                            }
+                            // non-negative values order like their bits (+0 for a zero)
+                            const uint32_t ma = __reduce_max_sync(kFull, __float_as_uint(ra > 0.f ? ra : 0.f));
+                            const uint32_t mb = __reduce_max_sync(kFull, __float_as_uint(rb > 0.f ? rb : 0.f));
+                            if (lane == 0) {
+                                gmax[ga] = __uint_as_float(ma);
+                                if (ci2 < ncg) gmax[gb2] = __uint_as_float(mb);
+                            }
+                        }
+                    } else {
+                        for (int gg = t; gg < G; gg += kGT)
+                            if (is_cand(gg)) atomicOr(&gs.dec_mask[(gg / GPR) >> 5], 1u << ((gg / GPR) & 31));
+                        gbar();
+                        list_chunks(0u);
+                    }
                 }
             }
             }
