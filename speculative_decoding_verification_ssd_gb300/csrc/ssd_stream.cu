@@ -124,6 +124,7 @@ struct GroupShared {
     // computed from direct loads instead of a second pass over their chunks)
     uint16_t ccg[kConsCandCap];
     int ccnt;
+    int rnf;  // consumer group: thread 0's answer whether the sequence rejected earlier
 };
 
 // sigma_{F,C} of one draft row found in the streaming pass ([SSD] item 2): the
@@ -1545,7 +1546,15 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             p_tok = ex2(fmaf(ztx, c, -gT.m)) / gT.S;
             q_tok = ex2(fmaf(zdx, c, draft_bias(shape, zdx, xt) - qm)) / qS;
             accept = (u_k * q_tok < p_tok) ? 1 : 0;
-            if (!(do_verify && !accept)) {
+            // A rejection publishes its bit at once (thread 0; the round trip overlaps the
+            // bound search below).  In verification alone the sequence's units not yet
+            // started then skip their rows; in any mode a rejection after an earlier one
+            // of the sequence draws no bonus (only the first rejection's is used), so its
+            // residual ranks the cache top-F alone, as at an accepted position.
+            const bool rej = do_verify && !accept;
+            uint32_t rej_old = 0;
+            if (t == 0 && rej && k < 32) rej_old = atomicOr(P.seq_reject + b, 1u << k);
+            if (!rej || bnd) {
                 // the residual is not sampled here: it ranks the cache top-F alone (or
                 // nothing).  For t* the target maximum of group g, r(t*) >= p(max z_p) -
                 // q(max z_q), and no token of g exceeds p(max z_p) (a reshaped draft only
@@ -1571,12 +1580,16 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                     cthr = tv > 0.f ? tv : -INFINITY;  // no positive bound: every group
                 }
             }
-            // Verification alone: a rejection publishes its bit now (units of the sequence
-            // not yet started skip their rows), and one after an earlier rejection of the
-            // sequence needs no residual (only the first rejection's bonus is used).
-            if (t == 0 && do_verify && !accept && (P.mode & kModeEarlyExit) && k < 32) {
-                const uint32_t old = atomicOr(P.seq_reject + b, 1u << k);
-                notfirst = (old & ((1u << k) - 1u)) != 0u;
+            if (rej && bnd) {
+                // the whole group needs the answer: the first rejection streams the whole
+                // second pass (its bonus), a later one only its candidate groups
+                if (t == 0) gs.rnf = (rej_old & ((1u << k) - 1u)) != 0u ? 1 : 0;
+                gbar();
+                notfirst = gs.rnf != 0;
+                if (!notfirst) cthr = -INFINITY;
+            } else if (rej) {
+                if (t == 0) notfirst = (rej_old & ((1u << k) - 1u)) != 0u;
+                cthr = -INFINITY;
             }
             if (gated) {
                 if (cthr == INFINITY) {
@@ -1587,10 +1600,13 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                         for (int w = 0; w < kDecWords; ++w) gs.dec_mask[w] = 0u;
                     list_chunks(0u);
                 } else if (cthr == -INFINITY) {
-                    if (t == 0 && notfirst)
+                    // every chunk: the first rejection's bonus, or a cache top-F without a
+                    // positive bound; none for a later rejection that builds no cache
+                    const bool none = notfirst && !bnd;
+                    if (t == 0 && none)
 #pragma unroll
                         for (int w = 0; w < kDecWords; ++w) gs.dec_mask[w] = 0u;
-                    list_chunks(notfirst ? 0u : 0xFFFFFFFFu);  // every chunk, or none
+                    list_chunks(none ? 0u : 0xFFFFFFFFu);
                 } else {
                     // The groups whose bound reaches cthr are the candidates; every other
                     // group's largest residual reads as 0.  Only the candidates' largest
