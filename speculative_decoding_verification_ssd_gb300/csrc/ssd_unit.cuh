@@ -59,8 +59,8 @@ struct UnitParams {
     int32_t *dev_status;
     // persistent streaming kernel only
     uint32_t *unit_counter;  // next unit to hand out (reset by the last CTA to exit)
-    unsigned long long *unit_ends;  // streaming kernel: units taken from the front (low
-                                    // 32 bits) and from the back (high 32 bits) of the order
+    unsigned long long *unit_ends;  // streaming kernel: units handed out (low 32 bits; the
+                                    // high half stays zero)
     uint32_t *exit_counter;  // CTAs that have exited
     int perm_mul;            // unit u -> sequence ((u % B) * perm_mul) % B (coprime to B)
     int wide;                // streaming kernel: both consumer groups of a CTA share each unit
