@@ -104,12 +104,12 @@ typedef struct ssd_reshape_desc {
 } ssd_reshape_desc;
 
 /* Kernel choice for rows on the 16-byte grid (process-wide; rows off the grid
- * always take the cluster kernel).  AUTO: for verification alone, the persistent
- * streaming kernel in its wide form (below); otherwise the streaming kernel when
- * the batch has at least as many units (sequences x (K+1)) as the GPU has SMs --
- * in its wide form below twice as many -- or when sigma_{F,C} is found in the
- * pass, else the cluster kernel, which splits each row across a thread-block
- * cluster.  STREAM / CLUSTER / SLICE force
+ * always take the cluster kernel).  AUTO: for verification alone with fewer
+ * units (sequences x (K+1)) than 8 per SM, the persistent streaming kernel in its
+ * wide form (below); otherwise the streaming kernel when the batch has at least
+ * as many units as the GPU has SMs -- in its wide form below twice as many -- or
+ * when sigma_{F,C} is found in the pass, else the cluster kernel, which splits
+ * each row across a thread-block cluster.  STREAM / CLUSTER / SLICE force
  * one.  SLICE, the slice kernel, splits every row into slices of 16 KB blocks
  * that the whole GPU works on at once and combines the slices' partial results
  * in the workspace; it applies to rows of whole 16-byte vectors (V a multiple of

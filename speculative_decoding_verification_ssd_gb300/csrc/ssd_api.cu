@@ -201,12 +201,12 @@ int run_units(int mode, const void *tgt, const void *drf, int dtype, int B, int 
     // streams at one group's share of an SM; the cluster kernel splits every row
     // across a cluster instead (c2: 8 sequences, K = 5: 38.5 us against 58.7), and
     // so does the streaming kernel's wide form, which puts both consumer groups of
-    // a CTA on each unit.  The wide form pays wherever few units reach a second
-    // pass -- verification alone, where only a sequence's first rejection streams
-    // its rows again (c3: 84.0 against 103.2 us, c2: 38.5 against 39.2 on the
-    // cluster kernel) -- and where a cache build has fewer than two units per SM
-    // (c4: 115.0 against 119.4); a cache build with more keeps two units per SM, so
-    // that one unit's second pass (L2 reads) overlaps the other's first (HBM).
+    // a CTA on each unit.  The wide form pays where units are few for the grid:
+    // verification alone below 8 units per SM (c3, 576 units: 82.5 against 96.0 us;
+    // c2: 38.4 against 37.8 on the cluster kernel; 1280 units: 89.8 against 87.5
+    // for the one-group form) and cache builds below 2 units per SM (c4: 112.5
+    // against 119.0); with more units the one-group form's two units per SM keep
+    // the HBM stream busier.
     const int policy = g_dispatch.load(std::memory_order_relaxed);
     // The slice kernel (rows split into slices scheduled over every SM) needs rows of
     // whole vectors, its own workspace regions and a batch it can order by kind.
@@ -219,7 +219,8 @@ int run_units(int mode, const void *tgt, const void *drf, int dtype, int B, int 
     const bool wide = !sliced && stream_ok && V % (16 / elem) == 0 &&
                       (policy == SSD_DISPATCH_WIDE ||
                        (policy == SSD_DISPATCH_AUTO &&
-                        ((verify && !cache) || (units >= dv->sm_count && units < 2 * dv->sm_count))));
+                        ((verify && !cache && units < 8 * dv->sm_count) ||
+                         (units >= dv->sm_count && units < 2 * dv->sm_count))));
     const bool streaming = !sliced && stream_ok && policy != SSD_DISPATCH_CLUSTER &&
                            (wide || policy == SSD_DISPATCH_STREAM || sig_F != nullptr || units >= dv->sm_count);
     Geometry g;
