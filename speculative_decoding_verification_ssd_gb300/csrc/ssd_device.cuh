@@ -74,8 +74,8 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
-// Waits for phase `parity` of `bar`, polling with try_wait (each poll may
-// suspend the thread for up to kSuspendHintNs or until the phase completes);
+// Waits for phase `parity` of `bar`: one non-blocking test, then polls with try_wait
+// (each poll may suspend the thread for up to kSuspendHintNs or until the phase completes);
 // gives up after limit_ns of wall-clock time (%globaltimer; kWaitLimitNs for
 // mbar_wait_suspend) and returns false (the caller records SSD_DEV_TIMEOUT).  A time bound rather than a poll count keeps roles that legitimately
 // idle for a long stretch of a large launch from giving up early.  The loop
@@ -88,6 +88,9 @@ __device__ __forceinline__ bool mbar_wait_suspend_for(uint64_t *bar, uint32_t pa
         "{\n\t"
         ".reg .pred p;\n\t"
         ".reg .u64 t0, t1;\n\t"
+        // a phase already complete returns before the timer is read (c4: 109.7 -> 106.5 us)
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "@p bra SSD_DONE;\n\t"
         "mov.u64 t0, %%globaltimer;\n"
         "SSD_WAIT:\n\t"
         "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
