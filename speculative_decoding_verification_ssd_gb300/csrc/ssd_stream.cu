@@ -88,7 +88,8 @@ struct __align__(16) Hdr {
     int chunk;  // chunk index within the pass
     int nvec;   // 16-byte vectors per row in this stage
     int b, k;   // sequence and position of the unit
-    int pad0, pad1;
+    int tau;    // the sequence's temperature (float bits), loaded with the unit's claim
+    int xt;     // drafted token x~_k (k < K), likewise
 };
 
 // A finished unit's hand-off from a consumer group to its tail warp.
@@ -445,7 +446,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         };
         // The next unit is claimed and its metadata loaded while the current
         // unit's last stages are issued, so neither round trip stalls the ring.
-        int pf_state = 0, pf_u = 0, pf_b = 0, pf_k = 0;
+        int pf_state = 0, pf_u = 0, pf_b = 0, pf_k = 0, pf_xt = -1;
         float pf_tau = 0.f;
         uint32_t pf_rej = 0;
         // Every ring takes units from the front of the order (a shared counter; the
@@ -463,6 +464,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                 if (pf_u < nunits) {
                     unit_bk(pf_u, pf_b, pf_k);
                     pf_tau = P.temperature[pf_b];
+                    pf_xt = pf_k < K ? P.tokens[static_cast<int64_t>(pf_b) * K + pf_k] : -1;
                     pf_rej = (P.mode & kModeEarlyExit) ? __ldcg(P.seq_reject + pf_b) : 0u;
                 }
                 pf_state = 2;
@@ -506,14 +508,15 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                     ok = push(0, stop, nullptr, nullptr, 0) && push(1, stop, nullptr, nullptr, 0);
                     break;
                 }
-                const int b = pf_b, k = pf_k;
+                const int b = pf_b, k = pf_k, xt = pf_xt;
                 const float tau = pf_tau;
+                const int taub = __float_as_int(tau);
                 const bool sampled = (tau > 0.f) && (tau < INFINITY);
                 const bool pair = sampled && k < K;
                 const bool p2 = pair && (do_verify || (do_cache && P.F[k] > 0));
                 const uint32_t mask = (k >= 32) ? 0xFFFFFFFFu : ((1u << k) - 1u);
                 if ((P.mode & kModeEarlyExit) && k > 0 && (pf_rej & mask) != 0) {
-                    const Hdr sk{u, kPassSkip | (1 << 4), 0, 0, b, k, 0, 0};
+                    const Hdr sk{u, kPassSkip | (1 << 4), 0, 0, b, k, taub, xt};
                     ok = push(0, sk, nullptr, nullptr, 0) && push(1, sk, nullptr, nullptr, 0);
                     if (!ok) break;
                     continue;
@@ -530,11 +533,11 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                 auto chunk_stage = [&](int r, int pass, int chunk, bool last) -> bool {
                     const int64_t off = static_cast<int64_t>(chunk) * cb;
                     const uint32_t bytes = static_cast<uint32_t>(row_bytes - off < cb ? row_bytes - off : cb);
-                    const Hdr hd{u, pass | ((last ? 1 : 0) << 4) | pbit, chunk, static_cast<int>(bytes / 16), b, k, 0, 0};
+                    const Hdr hd{u, pass | ((last ? 1 : 0) << 4) | pbit, chunk, static_cast<int>(bytes / 16), b, k, taub, xt};
                     return push(r, hd, trow + off, drow ? drow + off : nullptr, bytes);
                 };
                 auto end_stage = [&](int r, int pass) -> bool {
-                    const Hdr hd{u, pass | (1 << 4) | pbit, -1, 0, b, k, 0, 0};
+                    const Hdr hd{u, pass | (1 << 4) | pbit, -1, 0, b, k, taub, xt};
                     return push(r, hd, nullptr, nullptr, 0);
                 };
                 for (int c = 0; c < nch && ok; ++c) {
@@ -595,8 +598,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                     mbar_arrive_expect_tx(&gq.full_bar[s], 0);
                     break;
                 }
-                const int b = pf_b, k = pf_k;
+                const int b = pf_b, k = pf_k, xt = pf_xt;
                 const float tau = pf_tau;
+                const int taub = __float_as_int(tau);
                 const bool sampled = (tau > 0.f) && (tau < INFINITY);
                 const bool pair = sampled && k < K;
                 const bool p2 = pair && (do_verify || (do_cache && P.F[k] > 0));
@@ -647,10 +651,10 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                         break;
                     }
                     if (skip) {
-                        gq.hdr[s] = Hdr{u, kPassSkip | (1 << 4), 0, 0, b, k, 0, 0};
+                        gq.hdr[s] = Hdr{u, kPassSkip | (1 << 4), 0, 0, b, k, taub, xt};
                         mbar_arrive_expect_tx(&gq.full_bar[s], 0);
                     } else if (empty_end) {
-                        gq.hdr[s] = Hdr{u, kPassResid | (1 << 4) | (1 << 5), -1, 0, b, k, 0, 0};
+                        gq.hdr[s] = Hdr{u, kPassResid | (1 << 4) | (1 << 5), -1, 0, b, k, taub, xt};
                         mbar_arrive_expect_tx(&gq.full_bar[s], 0);
                     } else {
                         const bool second = i >= nch;
@@ -663,7 +667,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                                                  : chunk == nch - 1;
                         const int code = (second ? kPassResid : kPassStats) | ((last ? 1 : 0) << 4) |
                                          ((pair ? 1 : 0) << 5);
-                        gq.hdr[s] = Hdr{u, code, chunk, static_cast<int>(bytes / 16), b, k, 0, 0};
+                        gq.hdr[s] = Hdr{u, code, chunk, static_cast<int>(bytes / 16), b, k, taub, xt};
                         unsigned char *dst = ring + s * kSB;
                         mbar_arrive_expect_tx(&gq.full_bar[s], bytes * (pair ? 2u : 1u));
                         // evict_first throughout: most second passes are cut to a few chunks,
@@ -1293,7 +1297,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             b = h.b;
             gmax = abase + (u_team * kNBuf + u_buf) * 2 * Gp;
             gsum = gmax + Gp;
-            const float tau = P.temperature[b];
+            const float tau = __int_as_float(h.tau);  // loaded by the producer with the claim
             const bool tau_ok = (tau >= 0.f) && (tau < INFINITY);
             const bool greedy = tau_ok && tau == 0.f;
             sampled = tau_ok && tau > 0.f;
@@ -1301,7 +1305,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             flags = tau_ok ? 0 : SSD_DEV_BAD_TEMPERATURE;
             xt = -1;
             if (k < K) {
-                xt = P.tokens[static_cast<int64_t>(b) * K + k];
+                xt = h.xt;
                 if (xt < 0 || xt >= V) flags |= SSD_DEV_BAD_TOKEN;
             }
             xmask = (greedy && k < K) ? xt : -1;
