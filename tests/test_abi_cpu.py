@@ -46,9 +46,13 @@ def test_strerror_and_version(ssd):
 def test_dispatch_policy(ssd):
     assert ssd.ssd_set_dispatch(ssd.SSD_DISPATCH_STREAM) == ssd.SSD_DISPATCH_AUTO
     assert ssd.ssd_set_dispatch(ssd.SSD_DISPATCH_CLUSTER) == ssd.SSD_DISPATCH_STREAM
-    assert ssd.ssd_set_dispatch(ssd.SSD_DISPATCH_AUTO) == ssd.SSD_DISPATCH_CLUSTER
+    assert ssd.ssd_set_dispatch(ssd.SSD_DISPATCH_SLICE) == ssd.SSD_DISPATCH_CLUSTER
+    assert ssd.ssd_set_dispatch(ssd.SSD_DISPATCH_WIDE) == ssd.SSD_DISPATCH_SLICE
+    assert ssd.ssd_set_dispatch(ssd.SSD_DISPATCH_AUTO) == ssd.SSD_DISPATCH_WIDE
     with pytest.raises(ValueError):
         ssd.ssd_set_dispatch(7)
+    with pytest.raises(ValueError):
+        ssd.ssd_set_dispatch(5)
     assert ssd.lib().ssd_set_dispatch(-3) == -1
     assert ssd.ssd_set_dispatch(ssd.SSD_DISPATCH_AUTO) == ssd.SSD_DISPATCH_AUTO
 
