@@ -64,8 +64,13 @@ namespace {
 constexpr int kGW = kStreamGroupWarps;  // warps per consumer group
 constexpr int kGT = kGW * 32;           // threads per consumer group
 constexpr int kNG = kStreamGroups;      // consumer groups (= rings = tail warps)
-constexpr int kRS = kStreamRingStages;  // stages per ring
-constexpr int kSB = kStreamStageBytes;  // bytes per stage
+// A ring of kStreamRingStages x 16 KB is cut into slots of kSubs stages of the consumers'
+// 16 KB geometry (one wait, header and release per slot; a pair slot is [target row part |
+// draft row part]).  kSubs is set per kernel form: 2 for the wide form without the fused
+// sigma selection (c4 105.2 -> 99.7 us, c2 37.7 -> 36.3), 1 for the others (c5 unchanged at
+// 2, c3 80.4 -> 82.6).
+constexpr int kSubB = kStreamStageBytes;   // bytes per stage (processing geometry)
+constexpr int kRSMax = kStreamRingStages;  // slots per ring at one stage per slot
 constexpr int kGTok = kGroupTokens;     // tokens per group of the group arrays
 constexpr int kNBuf = kStreamBuffers;   // group-array buffers per consumer group
 constexpr int kProducerWarp0 = kNG * kGW;
@@ -107,13 +112,13 @@ struct TailDesc {
 };
 
 struct GroupShared {
-    uint64_t full_bar[kRS];
-    uint64_t empty_bar[kRS];
+    uint64_t full_bar[kRSMax];
+    uint64_t empty_bar[kRSMax];
     uint64_t tail_full[kNBuf];
     uint64_t tail_empty[kNBuf];
     uint64_t dec_bar;         // consumer thread 0 -> producer: the chunks a second pass needs
     uint32_t dec_mask[kDecWords];
-    Hdr hdr[kRS];
+    Hdr hdr[kRSMax];
     TailDesc desc[kNBuf];
     Stat red[kGW];
     // tail-warp scratch
@@ -290,9 +295,14 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     ssd_stream_kernel(const __grid_constant__ UnitParams P) {
     constexpr int VEC = D::kVec, S = D::kBytes;
     constexpr int GV = kGTok / VEC;        // vectors per group
-    constexpr int HALF = kSB / 2;          // bytes per row in a pair stage
+    constexpr int kSubs = (kWide && !kSig) ? 2 : 1;   // stages per ring slot
+    constexpr int kRS = kStreamRingStages / kSubs;     // slots per ring
+    constexpr int kSB = kStreamStageBytes * kSubs;     // bytes per slot
+    static_assert(kRS * kSB == kStreamRingStages * kStreamStageBytes, "ring bytes");
+    constexpr int HALF = kSubB / 2;        // bytes per row in a pair stage
+    constexpr int DOFF = kSB / 2;          // the draft row part's offset in a pair slot
     constexpr int FULL_PAIR = HALF / 16;   // vectors per row in a full pair stage
-    constexpr int FULL_ONE = kSB / 16;     // vectors in a full single-row stage
+    constexpr int FULL_ONE = kSubB / 16;   // vectors in a full single-row stage
     constexpr int GPR = FULL_PAIR / GV;    // groups per row in a pair stage
     constexpr int GPS = FULL_ONE / GV;     // groups in a single-row stage
     constexpr int TPGS = kGT / GPS;        // single rows: threads per group
@@ -300,7 +310,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     constexpr int VPT1 = FULL_PAIR / (kGT / 2), VPTS = GV / TPGS, VPT2 = GV / TPG2;
     constexpr int TPG1 = GV / VPT1;        // pass 1 of a pair: threads per group of one row
     static_assert(VPT1 == 4 && VPTS == 4 && VPT2 == 2, "stage geometry");
-    static_assert((kStreamMaxGroups + GPR - 1) / GPR <= kDecWords * 32, "second-pass chunk list");
+    static_assert((kStreamMaxGroups + GPR * kSubs - 1) / (GPR * kSubs) <= kDecWords * 32, "second-pass chunk list");
     constexpr int LPG = GV < 32 ? GV : 32;  // tail: lanes per group re-read (one vector each)
     constexpr int GPI = 32 / LPG;           // tail: groups per warp iteration
     constexpr int VPL = GV / LPG;           // tail: vectors per lane per group
@@ -515,7 +525,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                 mbar_arrive_expect_tx(&gsh[r].full_bar[s], src_t ? bytes * (src_d ? 2u : 1u) : 0u);
                 if (src_t) {
                     bulk_copy_hint(dst, src_t, bytes, &gsh[r].full_bar[s], pol);
-                    if (src_d) bulk_copy_hint(dst + HALF, src_d, bytes, &gsh[r].full_bar[s], pol);
+                    if (src_d) bulk_copy_hint(dst + DOFF, src_d, bytes, &gsh[r].full_bar[s], pol);
                 }
                 if (r) ++nr1; else ++n;
                 return true;
@@ -548,7 +558,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                     pair ? static_cast<const unsigned char *>(P.drf) +
                                (static_cast<int64_t>(b) * P.drf_seq_stride + static_cast<int64_t>(k) * P.ld) * S
                          : nullptr;
-                const int cb = pair ? HALF : kSB;
+                const int cb = pair ? DOFF : kSB;
                 const int nch = static_cast<int>((row_bytes + cb - 1) / cb);
                 const int pbit = (pair ? 1 : 0) << 5;
                 auto chunk_stage = [&](int r, int pass, int chunk, bool last) -> bool {
@@ -633,7 +643,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                     pair ? static_cast<const unsigned char *>(P.drf) +
                                (static_cast<int64_t>(b) * P.drf_seq_stride + static_cast<int64_t>(k) * P.ld) * S
                          : nullptr;
-                const int cb = pair ? HALF : kSB;
+                const int cb = pair ? DOFF : kSB;
                 const int nch = static_cast<int>((row_bytes + cb - 1) / cb);
                 const int total = skip ? 1 : nch * (p2 ? 2 : 1);
                 // A second pass longer than its unasked stages streams those first; the
@@ -694,7 +704,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                         // evict_first throughout: most second passes are cut to a few chunks,
                         // so holding first-pass rows in L2 for them costs more than it saves
                         bulk_copy_hint(dst, trow + off, bytes, &gq.full_bar[s], pol);
-                        if (pair) bulk_copy_hint(dst + HALF, drow + off, bytes, &gq.full_bar[s], pol);
+                        if (pair) bulk_copy_hint(dst + DOFF, drow + off, bytes, &gq.full_bar[s], pol);
                     }
                     ++n;
                     if (total - i <= 3) pf_step();
@@ -1235,7 +1245,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     bool bnd = false;      // a pair that builds a cache: pass 1 keeps both rows' group maxima
     bool notfirst = false;  // thread 0: a rejection after an earlier one of the sequence (verification alone)
     float cthr = -INFINITY;  // pass 2: residuals of the groups whose upper bound reaches this only
-    const int nch_pair = static_cast<int>((row_bytes + HALF - 1) / HALF);  // chunks of a pair pass
+    const int nch_pair = static_cast<int>((row_bytes + DOFF - 1) / DOFF);  // slots of a pair pass
     float c = 0.f, LT = 0.f, LD = 0.f;
     DraftShape shape{0, 0.f, 0, 0.f};
     Stat st{-INFINITY, 0.f};
@@ -1371,24 +1381,32 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             handoff(kKindPass, 2, 0.f, 0.f);
             continue;
         }
-        const unsigned char *stg = ring + s * kSB;
         const bool stage_pair = (h.code >> 5) & 1;
+        // the slot's stages: chunk index and vector count of each (a header-only slot has none)
+        // (one stage per slot: exactly the slot's header, no loop bookkeeping)
+        const int full_v = stage_pair ? FULL_PAIR : FULL_ONE;
+#pragma unroll 1
+        for (int sj = 0; sj < kSubs; ++sj) {
+        const int hchunk = kSubs == 1 ? h.chunk : h.chunk * kSubs + sj;
+        const int hnvec = kSubs == 1 ? h.nvec : min(full_v, h.nvec - sj * full_v);
+        if (kSubs > 1 && hnvec <= 0) break;
+        const unsigned char *stg = ring + s * kSB + (kSubs == 1 ? 0 : sj * (stage_pair ? HALF : kSubB));
         // the stage holding a row's partial last vector (row stride longer than V)
-        const bool part = vtail != 0 && h.chunk * (stage_pair ? FULL_PAIR : FULL_ONE) + h.nvec == nvec_row;
-        const int pv = part ? h.nvec - 1 : -1;
+        const bool part = vtail != 0 && hchunk * (stage_pair ? FULL_PAIR : FULL_ONE) + hnvec == nvec_row;
+        const int pv = part ? hnvec - 1 : -1;
         // ---- stage processing (a header-only stage just ends a pass) -----------
-        if (active && h.nvec > 0) {
+        if (active && hnvec > 0) {
             if (pass == kPassStats && stage_pair) {
                 // online statistics: threads [0, 128) target, the rest draft
                 uint4 w[VPT1];
-                load_vecs<D, VPT1>(stg + p1_row * HALF, p1_vbase, h.nvec, p1_rot, h.nvec == FULL_PAIR && !part, w);
+                load_vecs<D, VPT1>(stg + p1_row * DOFF, p1_vbase, hnvec, p1_rot, hnvec == FULL_PAIR && !part, w);
                 if (part) mask_partial<D, VPT1>(w, p1_vbase, p1_rot, pv, vtail);
                 const float rm = vecs_max<D, VPT1>(w);
                 if (sig || bnd) {
                     // raw 64-token group maxima: the draft's to gmax (the fused sigma's
                     // candidates, the bound on q), the target's to gsum (the bound on p)
                     const float gm = tpg_max<TPG1>(rm);
-                    const int g = h.chunk * GPR + p1_tr / TPG1;
+                    const int g = hchunk * GPR + p1_tr / TPG1;
                     if (p1_tr % TPG1 == 0 && g < G) (p1_row ? gmax : gsum)[g] = canon_zero(gm);
                 }
                 // a reshaped draft row takes the plain path where none of the thread's
@@ -1396,16 +1414,16 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                 if (p1_row == 0 || !shape.on || !(rm >= shape.thr)) {
                     stat_fold(st, rm * c, [&](float mn) { return vecs_expsum<D, VPT1>(w, c, mn); });
                 } else {
-                    st = reshaped_fold<D, VPT1>(st, stg + HALF, p1_vbase, h.nvec, p1_rot, h.nvec == FULL_PAIR && !part,
-                                                c, shape, h.chunk * (FULL_PAIR * VEC) + p1_vbase * VEC, pv, vtail);
+                    st = reshaped_fold<D, VPT1>(st, stg + DOFF, p1_vbase, hnvec, p1_rot, hnvec == FULL_PAIR && !part,
+                                                c, shape, hchunk * (FULL_PAIR * VEC) + p1_vbase * VEC, pv, vtail);
                 }
             } else if (pass == kPassStats) {
                 // one row: sampled row K (maxima, masses, statistics) or greedy (maxima,
                 // drafted token excluded)
                 uint4 w[VPTS];
-                load_vecs<D, VPTS>(stg, s_vbase, h.nvec, s_rot, h.nvec == FULL_ONE && !part, w);
+                load_vecs<D, VPTS>(stg, s_vbase, hnvec, s_rot, hnvec == FULL_ONE && !part, w);
                 if (part) mask_partial<D, VPTS>(w, s_vbase, s_rot, pv, vtail);
-                const int e0 = h.chunk * (FULL_ONE * VEC) + s_vbase * VEC;
+                const int e0 = hchunk * (FULL_ONE * VEC) + s_vbase * VEC;
                 if (static_cast<unsigned>(xmask - e0) < static_cast<unsigned>(VPTS * VEC)) {
 #pragma unroll
                     for (int kk = 0; kk < VPTS; ++kk) {
@@ -1415,7 +1433,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                     }
                 }
                 const float gm = tpg_max_nan<TPGS>(vecs_max<D, VPTS>(w));
-                const int g = h.chunk * GPS + s_gl;
+                const int g = hchunk * GPS + s_gl;
                 if (sampled) {
                     const float gmc = gm * c;
                     const float vs = vecs_expsum<D, VPTS>(w, c, gmc);
@@ -1432,18 +1450,18 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                 }
             } else {
                 // pass 2 (pair): residual masses and maxima per group
-                const bool full = h.nvec == FULL_PAIR && !part;
+                const bool full = hnvec == FULL_PAIR && !part;
                 float2 acc = make_float2(0.f, 0.f);
                 float mx = 0.f;
-                const int g = h.chunk * GPR + r_gl;
+                const int g = hchunk * GPR + r_gl;
                 // at an accepted position only the groups whose bound reaches cthr
                 const bool cand =
                     cthr == -INFINITY ||
                     (cthr < INFINITY && g < G && ex2(fmaf(gsum[g], c, -LT)) * (1.f + 0x1p-20f) >= cthr);
                 uint4 wt[VPT2], wd[VPT2];
                 if (cand) {
-                    load_vecs<D, VPT2>(stg, r_vbase, h.nvec, r_rot, full, wt);
-                    load_vecs<D, VPT2>(stg + HALF, r_vbase, h.nvec, r_rot, full, wd);
+                    load_vecs<D, VPT2>(stg, r_vbase, hnvec, r_rot, full, wt);
+                    load_vecs<D, VPT2>(stg + DOFF, r_vbase, hnvec, r_rot, full, wd);
                     if (part) {
                         mask_partial<D, VPT2>(wt, r_vbase, r_rot, pv, vtail);
                         mask_partial<D, VPT2>(wd, r_vbase, r_rot, pv, vtail);
@@ -1471,8 +1489,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                         }
                     }
                 } else {
-                    const float2 r2 = reshaped_resid<D, VPT2>(stg, HALF, r_vbase, h.nvec, r_rot, full, c, LT, LD, shape,
-                                                              h.chunk * (FULL_PAIR * VEC) + r_vbase * VEC, pv, vtail);
+                    const float2 r2 = reshaped_resid<D, VPT2>(stg, DOFF, r_vbase, hnvec, r_rot, full, c, LT, LD, shape,
+                                                              hchunk * (FULL_PAIR * VEC) + r_vbase * VEC, pv, vtail);
                     acc.x = r2.x;
                     mx = r2.y;
                 }
@@ -1483,6 +1501,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                     gsum[g] = gsv;
                 }
             }
+        }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&gs.empty_bar[s]);
@@ -1688,7 +1707,10 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                         }
                     } else {
                         for (int gg = t; gg < G; gg += kGT)
-                            if (is_cand(gg)) atomicOr(&gs.dec_mask[(gg / GPR) >> 5], 1u << ((gg / GPR) & 31));
+                            if (is_cand(gg)) {
+                                const int ch = gg / (GPR * kSubs);  // the slot holding group gg
+                                atomicOr(&gs.dec_mask[ch >> 5], 1u << (ch & 31));
+                            }
                         gbar();
                         list_chunks(0u);
                     }
