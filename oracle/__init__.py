@@ -11,10 +11,13 @@ passage).  This module only marshals numpy arrays into it and splits a batch
 across host threads (sequences are independent).
 
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
-(worked table, closed forms, exact enumeration, Monte Carlo, brute force).
-The readings taken where the pages are silent (which uniform draws the bonus,
-the CDF order and boundary, the Z == 0 fallback) have no value on the pages to
-pin against: their parity is "unpinned" beyond internal consistency.
+(worked table, closed forms, exact enumeration, Monte Carlo, brute force,
+library routines).  Where the pages are silent -- which uniform draws the
+bonus, the CDF order and boundary, the Z == 0 fallback -- they fix only the
+law of the draw.  The chi-square and exact-enumeration pins check that law;
+the chosen readings are pinned token by token against numpy's inverse CDF
+(``searchsorted`` over the cumulative weights of scipy's softmax, ascending
+token id) on the same uniforms.
 """
 from __future__ import annotations
 

@@ -35,10 +35,11 @@
  *     logits with the drafted token excluded (tau == 0);
  *   - draft-only cache keys: raw draft logits of row k (of K+1 draft rows), the
  *     drafted token left out for k < K; the reshape at position k uses F = F_k.
- * Parity unpinned: the pages print no value that fixes which uniform draws the
- * bonus or the CDF order and boundary; for those two readings the pins can only
- * check internal consistency.  The Z == 0 fallback is pinned against the p_a it
- * reduces to (its draw and its hit probability), though no page value fixes it.
+ * Where the pages are silent (which uniform draws the bonus, the CDF order and
+ * boundary, the Z == 0 fallback) they fix only the law of the draw: the tests pin
+ * that law (chi-square, exact enumeration) and pin the chosen readings token by
+ * token against numpy's inverse CDF of scipy's softmax on the same uniforms; the
+ * Z == 0 fallback also against its hit probability, the cached mass of p_a.
  */
 #include <math.h>
 #include <stdint.h>
