@@ -5,9 +5,9 @@
 //   * producer warp g (one elected lane) takes units (sequence b, position k)
 //     from a global counter and streams their logit rows with cp.async.bulk
 //     into ring g (4 stages of 16 KB, each guarded by a full/empty mbarrier
-//     pair).  Units whose sequence samples (temperature > 0) and whose
-//     position is below K -- the two-row, two-pass units -- are handed out
-//     first, single rows last, so the grid ends on short units;
+//     pair).  The two-row, two-pass units (sampled sequence, position below
+//     K) go before the greedy rows, so the grid ends on short units (a cache
+//     build puts the sampled rows K first: unit_bk below);
 //   * consumer group g (8 warps) only streams:
 //       pass 1 (HBM)  sampled rows fold every element into per-thread online
 //                     softmax statistics (base 2: m = max z c, S = sum 2^(z c - m),
@@ -372,8 +372,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     // is read only after that grid has completed and its writes are visible.
     asm volatile("griddepcontrol.wait;" ::: "memory");
     __syncthreads();
-    // Unit order: pair units (sampled sequence, k < K) first, then the sampled
-    // rows K, then the other sequences' rows.  Every CTA maps the shared unit
+    // Sequence list of the unit order (unit_bk, below): the sampled sequences
+    // first, then the others.  Every CTA maps the shared unit
     // counter through this list, so it is built the same way everywhere: a
     // stable compaction in ascending b (per-32 ballots, then chunk prefixes).
     const bool use_list = B <= kSchedCap;
