@@ -71,3 +71,34 @@ def test_drafting_follows_softmax_of_the_scaled_logits():
     greedy = synth.sample_draft_tokens(rng, np.broadcast_to(z, (3, 1, z.size)).copy(),
                                        np.zeros(3, np.float32))
     assert (greedy == 3).all()
+
+
+def test_algorithmic_bytes_closed_forms():
+    """The roofline numerator: distinct logit bytes a round must read.  A round reads
+    2K+1 rows of a sampled sequence and K+1 of a greedy one; verification alone stops
+    after the first rejection (2(a+1) rows, or a+1 greedy); a reshape reads each sampled
+    draft row once more.  Counted here row by row from the shapes."""
+    c5 = synth.WORKLOADS["c5"]
+    tau = synth.temperatures(c5)
+    V, K = c5.V, c5.K
+    n_s = int(np.count_nonzero(tau > 0))
+    assert n_s == 128
+    assert synth.algorithmic_bytes(c5, tau) == 128 * 9 * V * 2 + 128 * 5 * V * 2 == 459_669_504
+
+    c2 = synth.WORKLOADS["c2"]
+    tau2 = synth.temperatures(c2)
+    a = np.array([0, 1, 5, 2, 0, 5, 3, 4])      # accepted lengths, K = 5 (5 = every draft)
+    rows = sum(2 * (x + 1) if x < c2.K else 2 * c2.K + 1 for x in a)
+    assert synth.algorithmic_bytes(c2, tau2, a) == rows * c2.V * 2
+
+    c3 = synth.WORKLOADS["c3"]
+    tau3 = synth.temperatures(c3)
+    a3 = np.full(c3.B, 2)
+    extra = int(np.count_nonzero(tau3 > 0)) * c3.K * c3.V * 2   # the reshape's draft rows
+    assert synth.algorithmic_bytes(c3, tau3, a3) == c3.B * 6 * c3.V * 2 + extra
+
+    g = c5.replace(B=4, greedy_first=4)                 # every sequence greedy
+    tg = synth.temperatures(g)
+    assert synth.algorithmic_bytes(g, tg) == 4 * (K + 1) * V * 2
+    gv = g.replace(mode="verify")
+    assert synth.algorithmic_bytes(gv, tg, np.array([0, 1, 4, 2])) == (1 + 2 + 5 + 3) * V * 2
